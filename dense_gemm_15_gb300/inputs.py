@@ -1,0 +1,200 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module holds random draws and storage casts only -- none of the GEMM
+arithmetic.  It is the one piece shared by the tests (which feed the same
+tensors to the CUDA path and to the CPU oracle) and the benchmark.
+
+Recipe (the same for every workload):
+  * generator ``numpy.random.default_rng([seed, workload_id, tensor_id])``
+    (PCG64), seed 0 by default;
+  * values are drawn in float64, then rounded to the storage type by a torch
+    CPU cast (round to nearest even); fp8 values are clamped to +-448 first;
+  * tensors are returned as CPU torch tensors in storage layout (row-major
+    unless a column-major layout is asked for, in which case the returned
+    tensor is the transpose's row-major storage).
+
+Workload ids (the ``workload_id`` seed component):
+  1  fp16 1024^3, D = A.B + C               (case a all ones, case b U[-1,1])
+  2  fp16 4096^3, alpha 1.5, beta 0.5, ReLU  (A,B ~ N(0, 1/sqrt(K)), C ~ N(0,1))
+  3  bf16 Llama-3.3-70B linear layers        (W ~ N(0, 0.02), X ~ N(0, 1), beta 0)
+  4  fp16 grouped, 32 groups, N 4096, K 2048 (M_g ~ U{64..4096}, U[-1,1])
+  5  fp16 stream-K shapes (U[-1,1]) and e4m3 8192^3 (N(0,1) clamped to +-448)
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+TORCH_DTYPE = {
+    "f16": torch.float16,
+    "bf16": torch.bfloat16,
+    "f32": torch.float32,
+    "e4m3": torch.float8_e4m3fn,
+}
+
+E4M3_MAX = 448.0
+
+# Llama-3.3-70B linear layers as (K, N) of the weight [K, N].
+LLAMA70B_LAYERS = {
+    "qkv": (8192, 10240),
+    "o_proj": (8192, 8192),
+    "gate_up": (8192, 57344),
+    "down": (28672, 8192),
+}
+LLAMA70B_TOKENS = (16, 128, 1024, 4096, 8192)
+
+STREAMK_SHAPES = ((256, 256, 65536), (1536, 1536, 16384), (3000, 5000, 7000))
+
+
+def rng(workload_id: int, tensor_id: int, seed: int = 0) -> np.random.Generator:
+    return np.random.default_rng([seed, workload_id, tensor_id])
+
+
+def _store(x64: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x64))
+    if dtype == "e4m3":
+        t = t.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float32)
+    return t.to(TORCH_DTYPE[dtype])
+
+
+def uniform(shape, lo, hi, dtype, workload_id, tensor_id, seed=0) -> torch.Tensor:
+    return _store(rng(workload_id, tensor_id, seed).uniform(lo, hi, size=shape), dtype)
+
+
+def normal(shape, std, dtype, workload_id, tensor_id, seed=0) -> torch.Tensor:
+    return _store(rng(workload_id, tensor_id, seed).normal(0.0, std, size=shape), dtype)
+
+
+def ones(shape, dtype) -> torch.Tensor:
+    return torch.ones(shape, dtype=TORCH_DTYPE[dtype])
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """Raw stored bits of a CPU tensor as a numpy array (uint16 / uint8)."""
+    t = t.contiguous()
+    if t.element_size() == 2:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy()
+    return t.numpy()
+
+
+class Problem:
+    """One GEMM problem instance: operands in storage form plus scalars."""
+
+    def __init__(self, name, A, B, C, M, N, K, alpha=1.0, beta=0.0, relu=False,
+                 a_dtype="f16", b_dtype="f16", c_dtype="f16", d_dtype="f16",
+                 a_col_major=False, b_col_major=False, scale_a=1.0, scale_b=1.0):
+        self.name = name
+        self.A, self.B, self.C = A, B, C
+        self.M, self.N, self.K = M, N, K
+        self.alpha, self.beta, self.relu = alpha, beta, relu
+        self.a_dtype, self.b_dtype = a_dtype, b_dtype
+        self.c_dtype, self.d_dtype = c_dtype, d_dtype
+        self.a_col_major, self.b_col_major = a_col_major, b_col_major
+        self.scale_a, self.scale_b = scale_a, scale_b
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    def __repr__(self):
+        return "Problem(%s, M=%d, N=%d, K=%d)" % (self.name, self.M, self.N, self.K)
+
+
+def _mk(shape_a, shape_b, col_a, col_b):
+    sa = (shape_a[1], shape_a[0]) if col_a else shape_a
+    sb = (shape_b[1], shape_b[0]) if col_b else shape_b
+    return sa, sb
+
+
+def config1(case: str, seed: int = 0) -> Problem:
+    """fp16 1024^3, alpha = beta = 1; case 'a' all ones, case 'b' U[-1,1]."""
+    n = 1024
+    if case == "a":
+        A, B, C = ones((n, n), "f16"), ones((n, n), "f16"), ones((n, n), "f16")
+    else:
+        A = uniform((n, n), -1, 1, "f16", 1, 0, seed)
+        B = uniform((n, n), -1, 1, "f16", 1, 1, seed)
+        C = uniform((n, n), -1, 1, "f16", 1, 2, seed)
+    return Problem("fp16_1024_%s" % ("ones" if case == "a" else "uniform"),
+                   A, B, C, n, n, n, alpha=1.0, beta=1.0)
+
+
+def config2(M=4096, N=4096, K=4096, strong=False, seed=0, tag=None) -> Problem:
+    """fp16, alpha 1.5, beta 0.5, ReLU; A, B ~ N(0, sigma) with sigma = 1/sqrt(K)
+    (or K^-1/4 for the 'strong' variant), C ~ N(0, 1)."""
+    sigma = K ** -0.25 if strong else K ** -0.5
+    wid = 2 if (M, N, K) == (4096, 4096, 4096) else 20 + (M * 7 + N * 3 + K) % 1000
+    A = normal((M, K), sigma, "f16", wid, 0, seed)
+    B = normal((K, N), sigma, "f16", wid, 1, seed)
+    C = normal((M, N), 1.0, "f16", wid, 2, seed)
+    name = tag or ("fp16_%dx%dx%d_relu%s" % (M, N, K, "_strong" if strong else ""))
+    return Problem(name, A, B, C, M, N, K, alpha=1.5, beta=0.5, relu=True)
+
+
+def config3(M: int, layer: str, seed=0) -> Problem:
+    """bf16 Llama-3.3-70B linear layer: X [M, K] ~ N(0,1), W [K, N] ~ N(0, 0.02),
+    beta 0, bf16 out."""
+    K, N = LLAMA70B_LAYERS[layer]
+    lid = list(LLAMA70B_LAYERS).index(layer)
+    X = normal((M, K), 1.0, "bf16", 3, 100000 * lid + M, seed)
+    W = normal((K, N), 0.02, "bf16", 3, 100000 * lid + 99999, seed)
+    return Problem("bf16_llama70b_%s_m%d" % (layer, M), X, W, None, M, N, K,
+                   alpha=1.0, beta=0.0, a_dtype="bf16", b_dtype="bf16",
+                   c_dtype="bf16", d_dtype="bf16")
+
+
+def grouped_sizes(groups=32, lo=64, hi=4096, seed=0):
+    return [int(m) for m in rng(4, 99, seed).integers(lo, hi, size=groups, endpoint=True)]
+
+
+def config4(groups=32, N=4096, K=2048, seed=0, m_sizes=None):
+    """fp16 grouped GEMM, D_g = A_g.B_g + C_g, entries U[-1,1]."""
+    ms = m_sizes if m_sizes is not None else grouped_sizes(groups, seed=seed)
+    probs = []
+    for g, m in enumerate(ms):
+        A = uniform((m, K), -1, 1, "f16", 4, 3 * g + 0, seed)
+        B = uniform((K, N), -1, 1, "f16", 4, 3 * g + 1, seed)
+        C = uniform((m, N), -1, 1, "f16", 4, 3 * g + 2, seed)
+        probs.append(Problem("fp16_grouped_g%d" % g, A, B, C, m, N, K, alpha=1.0, beta=1.0))
+    return probs
+
+
+def config5a(M, N, K, seed=0) -> Problem:
+    """fp16 stream-K stress shape, entries U[-1,1], alpha = beta = 1."""
+    wid = 5
+    tid = 10 * STREAMK_SHAPES.index((M, N, K)) if (M, N, K) in STREAMK_SHAPES else 50 + (M + N + K) % 997
+    A = uniform((M, K), -1, 1, "f16", wid, tid + 0, seed)
+    B = uniform((K, N), -1, 1, "f16", wid, tid + 1, seed)
+    C = uniform((M, N), -1, 1, "f16", wid, tid + 2, seed)
+    return Problem("fp16_streamk_%dx%dx%d" % (M, N, K), A, B, C, M, N, K, alpha=1.0, beta=1.0)
+
+
+def config5b(M=8192, N=8192, K=8192, scale_a=1.0, scale_b=1.0, seed=0) -> Problem:
+    """e4m3 A, B ~ N(0,1) clamped to +-448, per-tensor fp32 scales, bf16 out, beta 0."""
+    A = normal((M, K), 1.0, "e4m3", 5, 100, seed)
+    B = normal((K, N), 1.0, "e4m3", 5, 101, seed)
+    return Problem("e4m3_%dx%dx%d" % (M, N, K), A, B, None, M, N, K, alpha=1.0, beta=0.0,
+                   a_dtype="e4m3", b_dtype="e4m3", c_dtype="bf16", d_dtype="bf16",
+                   scale_a=scale_a, scale_b=scale_b)
+
+
+def random_problem(M, N, K, dtype="f16", out_dtype=None, alpha=1.0, beta=0.0, relu=False,
+                   a_col_major=False, b_col_major=False, seed=0, lo=-1.0, hi=1.0,
+                   scale_a=1.0, scale_b=1.0, wid=9) -> Problem:
+    """A small seeded problem of any shape, layout and dtype, for edge-case tests."""
+    out_dtype = out_dtype or ("bf16" if dtype == "e4m3" else dtype)
+    key = (M * 1_000_003 + N * 10_007 + K * 101 + int(a_col_major) * 2 + int(b_col_major)) % (2**31)
+    sa, sb = _mk((M, K), (K, N), a_col_major, b_col_major)
+    if dtype == "e4m3":
+        A = normal(sa, 1.0, dtype, wid, key + 0, seed)
+        B = normal(sb, 1.0, dtype, wid, key + 1, seed)
+    else:
+        A = uniform(sa, lo, hi, dtype, wid, key + 0, seed)
+        B = uniform(sb, lo, hi, dtype, wid, key + 1, seed)
+    C = uniform((M, N), lo, hi, out_dtype, wid, key + 2, seed) if beta != 0.0 else None
+    return Problem("random_%dx%dx%d" % (M, N, K), A, B, C, M, N, K, alpha=alpha, beta=beta,
+                   relu=relu, a_dtype=dtype, b_dtype=dtype, c_dtype=out_dtype,
+                   d_dtype=out_dtype, a_col_major=a_col_major, b_col_major=b_col_major,
+                   scale_a=scale_a, scale_b=scale_b)

@@ -1,0 +1,66 @@
+"""Comparison of a GPU result against the oracle -- test infrastructure only.
+
+Tolerance for fp16 / bf16 output (element by element):
+
+    |D - D_ref| <= 1e-2 * |alpha| * s_a * s_b * (|A| . |B|)_ij + 1e-3
+                   + u * |beta * C_ij|
+
+with u = 2^-10 for fp16 and 2^-7 for bf16 output.  The first two terms are the
+stated bound of the method's accuracy target; |alpha| and s_a*s_b scale it
+with the product term it bounds (for alpha = s = 1 it is the literal bound),
+and the last term covers the one rounding of the beta*C contribution to the
+output type.  ReLU is 1-Lipschitz, so the same bound holds after it.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import decode, gemm
+
+ROUND_UNIT = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}
+
+
+def bound(absab: np.ndarray, alpha: float, beta: float, c64, out_dtype: str,
+          scale=1.0) -> np.ndarray:
+    b = 1e-2 * abs(alpha) * scale * absab + 1e-3
+    if beta != 0.0 and c64 is not None:
+        b = b + ROUND_UNIT[out_dtype] * np.abs(beta * c64)
+    return b
+
+
+def reference(prob, bits_of, rows=None, threads=None):
+    """(D_ref, |A|.|B|, C as float64) for rows ``rows`` of ``prob``.
+
+    ``bits_of`` maps a CPU tensor to its stored bits (the input module's
+    ``bits``), so this module needs nothing from the CUDA path."""
+    a, b = bits_of(prob.A), bits_of(prob.B)
+    c = bits_of(prob.C) if prob.C is not None else None
+    d_ref = gemm(a, prob.a_dtype, b, prob.b_dtype, c if prob.beta != 0.0 else None,
+                 prob.c_dtype, alpha=prob.alpha, beta=prob.beta, relu=prob.relu,
+                 scale_a=prob.scale_a, scale_b=prob.scale_b,
+                 a_col_major=prob.a_col_major, b_col_major=prob.b_col_major,
+                 rows=rows, threads=threads)
+    absab = gemm(a, prob.a_dtype, b, prob.b_dtype, absolute=True,
+                 a_col_major=prob.a_col_major, b_col_major=prob.b_col_major,
+                 rows=rows, threads=threads)
+    c64 = None
+    if c is not None and prob.beta != 0.0:
+        r0, r1 = (0, prob.M) if rows is None else rows
+        c64 = decode(c[r0:r1], prob.c_dtype)
+    return d_ref, absab, c64
+
+
+def compare(d_bits: np.ndarray, out_dtype: str, d_ref, absab, c64, prob):
+    """Returns (ok, worst ratio |err|/bound, index of worst, count of failures)."""
+    d = decode(d_bits, out_dtype)
+    tol = bound(absab, prob.alpha, prob.beta, c64, out_dtype, prob.scale_a * prob.scale_b)
+    err = np.abs(d - d_ref)
+    ratio = np.where(np.isfinite(err), err / tol, np.inf)
+    # NaN where the reference is NaN too counts as agreement.
+    both_nan = np.isnan(d) & np.isnan(d_ref)
+    ratio = np.where(both_nan, 0.0, ratio)
+    if ratio.size == 0:
+        return True, 0.0, None, 0
+    worst = int(np.argmax(ratio))
+    nbad = int(np.count_nonzero(ratio > 1.0))
+    return nbad == 0, float(ratio.flat[worst]), np.unravel_index(worst, ratio.shape), nbad

@@ -1,0 +1,309 @@
+"""Pins of the CPU oracle against facts fixed outside it: the pages' worked
+examples, closed forms, exact rational brute force on tiny inputs, library
+decoders / rounding, and numpy's float64 matmul.  CPU only."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import check
+from dense_gemm_15_gb300 import inputs
+from conftest import read_golden
+
+F16_ONE = 0x3C00
+
+
+# ---------------------------------------------------------------- decoders
+
+def test_decode_f16_all_patterns_match_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.decode(bits, "f16")
+    ref = bits.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ours[m], ref[m])
+    # signed zeros too
+    assert np.array_equal(np.signbit(ours[m]), np.signbit(ref[m]))
+
+
+def test_decode_bf16_all_patterns_match_torch():
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.decode(bits, "bf16")
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ours[m], ref[m])
+
+
+def test_decode_e4m3_all_patterns_match_torch():
+    bits = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode(bits, "e4m3")
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ours[m], ref[m])
+    assert np.nanmax(np.abs(ours)) == 448.0
+
+
+# ---------------------------------------------------------------- rounding
+
+def _f16_round_cases():
+    g = np.random.default_rng(123)
+    x = np.concatenate([
+        g.standard_normal(20000) * np.exp2(g.integers(-30, 17, 20000)),
+        # exact ties between neighbouring fp16 values
+        (np.arange(0, 4096, dtype=np.float64) + 0.5) * 2.0 ** -24,
+        (np.arange(1024, 2048, dtype=np.float64) + 0.5) * 2.0 ** -5,
+        np.array([65504.0, 65519.0, 65519.999, 65520.0, 65536.0, 1e9,
+                  2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0001, 2.0 ** -14,
+                  2.0 ** -14 - 2.0 ** -25, 0.0, -0.0, 1025.0, 129.0]),
+    ])
+    return np.concatenate([x, -x])
+
+
+def test_round_f16_matches_numpy():
+    x = _f16_round_cases()
+    ours = oracle.round_to(x, "f16")
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_round_bf16_matches_torch_on_float32_values():
+    g = np.random.default_rng(7)
+    x32 = (g.standard_normal(40000) * np.exp2(g.integers(-140, 127, 40000))).astype(np.float32)
+    ties = ((np.arange(128, 256) + 0.5) * 2.0 ** -3).astype(np.float32)
+    x32 = np.concatenate([x32, ties, -ties, np.float32([3.3895314e38, 0.0, -0.0])])
+    ours = oracle.round_to(x32.astype(np.float64), "bf16")
+    ref = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------- the pages' examples
+
+@pytest.mark.parametrize("fixture", ["all_ones_128.txt", "all_ones_1024.txt"])
+def test_all_ones_example(fixture):
+    g = read_golden(fixture)
+    M, N, K = (int(g[k][0][0]) for k in ("M", "N", "K"))
+    a = np.full((M, K), F16_ONE, np.uint16)
+    b = np.full((K, N), F16_ONE, np.uint16)
+    c = np.full((M, N), F16_ONE, np.uint16)
+    d = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=1.0, beta=1.0)
+    assert np.all(d == float(g["expect_all"][0][0]))
+    assert np.all(oracle.round_to(d, "f16") == int(g["expect_bits_all"][0][0], 16))
+
+
+def test_alpha_beta_relu_hand_example():
+    g = read_golden("alpha_beta_relu_2x2.txt")
+    A = np.array([float(v) for v in g["A"][0]]).reshape(2, 2)
+    B = np.array([float(v) for v in g["B"][0]]).reshape(2, 2)
+    C = np.array([float(v) for v in g["C"][0]]).reshape(2, 2)
+    f16 = lambda x: x.astype(np.float16).view(np.uint16)
+    d = oracle.gemm(f16(A), "f16", f16(B), "f16", f16(C), "f16",
+                    alpha=float(g["alpha"][0][0]), beta=float(g["beta"][0][0]),
+                    relu=bool(int(g["relu"][0][0])))
+    expect = np.array([float(v) for v in g["expect"][0]]).reshape(2, 2)
+    assert np.array_equal(d, expect)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def _rand_f16(shape, seed, lo=-1, hi=1):
+    return np.random.default_rng(seed).uniform(lo, hi, shape).astype(np.float16).view(np.uint16)
+
+
+def test_identity_b_returns_a():
+    a = _rand_f16((37, 64), 1)
+    eye = np.eye(64).astype(np.float16).view(np.uint16)
+    d = oracle.gemm(a, "f16", eye, "f16")
+    assert np.array_equal(oracle.round_to(d, "f16"), a)
+
+
+def test_permutation_b_permutes_columns():
+    a = _rand_f16((20, 48), 2)
+    perm = np.random.default_rng(3).permutation(48)
+    P = np.zeros((48, 48))
+    P[perm, np.arange(48)] = 1.0  # column j of A.P is column perm[j] of A
+    d = oracle.gemm(a, "f16", P.astype(np.float16).view(np.uint16), "f16")
+    assert np.array_equal(oracle.round_to(d, "f16"), a[:, perm])
+
+
+def test_rank1_outer_product():
+    g = np.random.default_rng(4)
+    u = g.integers(-4, 5, 24).astype(np.float64)
+    v = g.integers(-4, 5, 40).astype(np.float64)
+    K = 32
+    A = np.repeat(u[:, None], K, axis=1)
+    B = np.repeat(v[None, :], K, axis=0)
+    d = oracle.gemm(A.astype(np.float16).view(np.uint16), "f16",
+                    B.astype(np.float16).view(np.uint16), "f16")
+    assert np.array_equal(d, K * np.outer(u, v))
+
+
+def test_relu_of_negative_products_is_zero():
+    a = np.full((16, 8), 0xBC00, np.uint16)  # -1
+    b = np.full((8, 24), F16_ONE, np.uint16)
+    c = np.zeros((16, 24), np.uint16)
+    d = oracle.gemm(a, "f16", b, "f16", c, "f16", beta=1.0, relu=True)
+    assert np.all(oracle.round_to(d, "f16") == 0)
+
+
+def test_zero_a_gives_rounded_beta_c():
+    c = _rand_f16((9, 33), 5, -10, 10)
+    a = np.zeros((9, 7), np.uint16)
+    b = _rand_f16((7, 33), 6)
+    d = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=1.0, beta=0.5)
+    want = (c.view(np.float16).astype(np.float64) * 0.5).astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.round_to(d, "f16"), want)
+
+
+def test_alpha_beta_linearity_without_relu():
+    p = inputs.random_problem(12, 20, 16, beta=1.0)
+    a, b, c = inputs.bits(p.A), inputs.bits(p.B), inputs.bits(p.C)
+    d1 = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=1.0, beta=0.0)
+    d2 = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=0.0, beta=1.0)
+    d3 = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=2.0, beta=-3.0)
+    assert np.allclose(d3, 2.0 * d1 - 3.0 * d2, rtol=1e-14, atol=1e-14)
+
+
+# ---------------------------------------------------------------- exact brute force
+
+def _exact_values(t: torch.Tensor):
+    """Exact rationals of a stored CPU tensor, decoded by torch (not the oracle)."""
+    return [[Fraction(float(v)) for v in row] for row in t.to(torch.float64).tolist()]
+
+
+def _brute(p):
+    A = _exact_values(p.A)
+    B = _exact_values(p.B)
+    C = _exact_values(p.C) if p.C is not None else None
+    at = (lambda i, k: A[k][i]) if p.a_col_major else (lambda i, k: A[i][k])
+    bt = (lambda k, j: B[j][k]) if p.b_col_major else (lambda k, j: B[k][j])
+    s = Fraction(p.alpha) * Fraction(p.scale_a) * Fraction(p.scale_b)
+    out = np.empty((p.M, p.N))
+    mag = np.empty((p.M, p.N))
+    for i in range(p.M):
+        for j in range(p.N):
+            acc = sum((at(i, k) * bt(k, j) for k in range(p.K)), Fraction(0))
+            absacc = sum((abs(at(i, k) * bt(k, j)) for k in range(p.K)), Fraction(0))
+            v = s * acc
+            if p.beta != 0.0:
+                v += Fraction(p.beta) * C[i][j]
+            if p.relu and v < 0:
+                v = Fraction(0)
+            out[i, j] = float(v)
+            mag[i, j] = float(abs(s) * absacc) + (abs(p.beta) * abs(float(C[i][j])) if p.beta else 0.0)
+    return out, mag
+
+
+def _oracle_of(p, **override):
+    kw = dict(alpha=p.alpha, beta=p.beta, relu=p.relu, scale_a=p.scale_a, scale_b=p.scale_b,
+              a_col_major=p.a_col_major, b_col_major=p.b_col_major)
+    kw.update(override)
+    return oracle.gemm(inputs.bits(p.A), p.a_dtype, inputs.bits(p.B), p.b_dtype,
+                       inputs.bits(p.C) if p.C is not None else None, p.c_dtype, **kw)
+
+
+def _agrees(d, exact, mag, K):
+    return np.all(np.abs(d - exact) <= (K + 4) * 2.0 ** -52 * mag + 1e-300)
+
+
+BRUTE_CASES = []
+for dt in ("f16", "bf16", "e4m3"):
+    for (M, N, K) in ((1, 1, 1), (3, 5, 7), (9, 9, 9), (4, 6, 2), (7, 3, 8)):
+        for cm in ((False, False), (True, False), (False, True), (True, True)):
+            BRUTE_CASES.append((dt, M, N, K, cm))
+
+
+@pytest.mark.parametrize("dt,M,N,K,cm", BRUTE_CASES)
+def test_brute_force_exact(dt, M, N, K, cm):
+    p = inputs.random_problem(M, N, K, dtype=dt, alpha=1.5, beta=0.5 if dt != "e4m3" else -0.75,
+                              relu=(M + N) % 2 == 0, a_col_major=cm[0], b_col_major=cm[1],
+                              scale_a=0.37 if dt == "e4m3" else 1.0,
+                              scale_b=1.7 if dt == "e4m3" else 1.0, lo=-3, hi=3)
+    exact, mag = _brute(p)
+    assert _agrees(_oracle_of(p), exact, mag, K)
+
+
+def test_all_shapes_up_to_9():
+    """Every M, N, K in 1..9 (with a subsample of combinations) against exact sums."""
+    g = np.random.default_rng(11)
+    for _ in range(60):
+        M, N, K = (int(x) for x in g.integers(1, 10, 3))
+        p = inputs.random_problem(M, N, K, beta=1.0, alpha=-2.0, seed=int(g.integers(1 << 30)))
+        exact, mag = _brute(p)
+        assert _agrees(_oracle_of(p), exact, mag, K)
+
+
+# ------------------------------------------------- the pins catch planted mistakes
+
+def test_planted_mistakes_are_caught():
+    """Mistakes planted in the oracle's inputs or arithmetic (on the CPU) must
+    fail the brute-force pin: a transposed operand, a dropped k term, a wrong
+    sign of beta, ReLU applied before the beta*C add."""
+    p = inputs.random_problem(6, 6, 6, beta=0.5, alpha=1.5, relu=True, lo=-3, hi=3)
+    exact, mag = _brute(p)
+    assert _agrees(_oracle_of(p), exact, mag, p.K)
+    # transposed B (square, so the call is well formed)
+    assert not _agrees(_oracle_of(p, b_col_major=True), exact, mag, p.K)
+    # dropped last k term
+    a, b = inputs.bits(p.A), inputs.bits(p.B)
+    c = inputs.bits(p.C)
+    dropped = oracle.gemm(np.ascontiguousarray(a[:, :-1]), "f16", np.ascontiguousarray(b[:-1]),
+                          "f16", c, "f16", alpha=1.5, beta=0.5, relu=True)
+    assert not _agrees(dropped, exact, mag, p.K)
+    # wrong sign of beta
+    assert not _agrees(_oracle_of(p, beta=-0.5), exact, mag, p.K)
+    # ReLU before the beta*C add
+    pre = oracle.gemm(a, "f16", b, "f16", alpha=1.5, relu=True)
+    wrong = pre + 0.5 * oracle.decode(c, "f16")
+    assert not _agrees(wrong, exact, mag, p.K)
+
+
+# ---------------------------------------------------------------- cross-checks
+
+def test_numpy_float64_cross_check():
+    for dt in ("f16", "bf16"):
+        p = inputs.random_problem(64, 96, 80, dtype=dt)
+        d = _oracle_of(p)
+        ref = p.A.to(torch.float64).numpy() @ p.B.to(torch.float64).numpy()
+        assert np.allclose(d, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_row_sampling_and_thread_count_do_not_change_results():
+    p = inputs.random_problem(40, 70, 33, beta=1.0, relu=True)
+    a, b, c = inputs.bits(p.A), inputs.bits(p.B), inputs.bits(p.C)
+    full1 = oracle.gemm(a, "f16", b, "f16", c, "f16", beta=1.0, relu=True, threads=1)
+    full8 = oracle.gemm(a, "f16", b, "f16", c, "f16", beta=1.0, relu=True, threads=8)
+    part = oracle.gemm(a, "f16", b, "f16", c, "f16", beta=1.0, relu=True, rows=(5, 17))
+    assert np.array_equal(full1, full8)
+    assert np.array_equal(part, full1[5:17])
+
+
+def test_absolute_matches_abs_matmul():
+    p = inputs.random_problem(30, 50, 40, dtype="bf16")
+    ab = oracle.gemm(inputs.bits(p.A), "bf16", inputs.bits(p.B), "bf16", absolute=True)
+    ref = np.abs(p.A.to(torch.float64).numpy()) @ np.abs(p.B.to(torch.float64).numpy())
+    assert np.allclose(ab, ref, rtol=1e-12)
+
+
+def test_beta_zero_never_reads_c():
+    a = _rand_f16((4, 4), 8)
+    d = oracle.gemm(a, "f16", a, "f16", None, "f16", beta=0.0)
+    assert np.all(np.isfinite(d))
+
+
+# ---------------------------------------------------------------- the checker
+
+def test_checker_accepts_rounded_reference_and_rejects_perturbation():
+    p = inputs.random_problem(32, 48, 64, beta=0.5, alpha=1.5, relu=True)
+    d_ref, absab, c64 = check.reference(p, inputs.bits)
+    bits = oracle.round_to(d_ref, "f16")
+    ok, ratio, _, _ = check.compare(bits, "f16", d_ref, absab, c64, p)
+    assert ok and ratio < 0.5
+    bad = d_ref.copy()
+    bad[3, 7] += 2.0 * check.bound(absab, p.alpha, p.beta, c64, "f16")[3, 7] + 0.01
+    ok, ratio, idx, nbad = check.compare(oracle.round_to(bad, "f16"), "f16", d_ref, absab, c64, p)
+    assert not ok and nbad == 1 and tuple(idx) == (3, 7)
