@@ -1,0 +1,825 @@
+// C-ABI of gemm15: plans, validation, the host planner (tile shape, schedule,
+// grid, workspace), tensor-map encoding and kernel launches.  See
+// include/gemm15.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/gemm15.h"
+#include "gemm_params.h"
+#include "launch.h"
+
+using namespace g15;
+
+namespace {
+
+constexpr uint32_t PLAN_MAGIC = 0x67313570u;  // "g15p"
+constexpr uint32_t PLAN_DEAD = 0xdeadbeefu;
+
+struct Options {
+    int schedule = 0;
+    int splits = 0;
+    int cta_group = 0;
+    int tile_n = 0;
+    int raster = 0;
+    int grid = 0;
+    int64_t timeout_us = 2000000;  // 2 s
+    int fault_skip_flag = -1;
+};
+
+}  // namespace
+
+struct gemm15_plan {
+    uint32_t magic = PLAN_MAGIC;
+    gemm15_plan_desc_t desc{};
+    int device = 0;
+    int num_sms = 0;
+    int elem = ELEM_F16;       // operand kind
+    int out_elem = ELEM_F16;   // C/D 16-bit kind
+    int32_t* d_status = nullptr;
+    uint32_t* d_flags = nullptr;
+    int flags_cap = 0;
+    float* d_ws = nullptr;
+    size_t ws_cap = 0;
+    GroupEntry* d_groups = nullptr;
+    GroupEntry* h_groups = nullptr;  // pinned staging
+    int groups_cap = 0;
+    cudaEvent_t groups_done = nullptr;
+    void* d_host_path[3] = {nullptr, nullptr, nullptr};  // A, B, C|D for gemm_run_host
+    size_t host_path_cap[3] = {0, 0, 0};
+    float* d_scales = nullptr;  // two floats for gemm_run_host
+    uint32_t epoch = 0;
+    Options opt;
+    gemm15_config_t last{};
+};
+
+namespace {
+
+// ------------------------------------------------------------------ helpers
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool plan_ok(const gemm15_plan* p) { return p != nullptr && p->magic == PLAN_MAGIC; }
+
+int esize_of(gemm15_dtype_t t) {
+    switch (t) {
+        case GEMM15_F16:
+        case GEMM15_BF16: return 2;
+        case GEMM15_F32: return 4;
+        case GEMM15_E4M3: return 1;
+    }
+    return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+CUtensorMapDataType tmap_type(int elem16_or_8) {
+    switch (elem16_or_8) {
+        case ELEM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        case ELEM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;  // fp8 bytes
+    }
+}
+
+// 2-D tiled tensor map with 128-byte swizzle and zero fill out of bounds.
+bool make_tmap(CUtensorMap* map, int elem, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, tmap_type(elem), 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// One problem after layout normalisation: D is row-major M x N.
+struct Prob {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    bool a_kmajor;  // row-major A (K contiguous)
+    const void* B;
+    int64_t ldb;
+    bool b_kmajor;  // column-major B (K contiguous)
+    const void* C;
+    int64_t ldc;
+    void* D;
+    int64_t ldd;
+};
+
+// Column-major C/D: compute D^T = B^T . A^T, which is row-major N x M.
+Prob normalise(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const void* A,
+               int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
+               int64_t ldd) {
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    Prob p{};
+    if (plan->desc.layout_cd == GEMM15_ROW_MAJOR) {
+        p = Prob{M, N, K, A, lda, a_row, B, ldb, !b_row, C, ldc, D, ldd};
+    } else {
+        // A' = B^T (N x K): K contiguous iff B is column-major.
+        // B' = A^T (K x M): K contiguous iff A is row-major.
+        p = Prob{N, M, K, B, ldb, !b_row, A, lda, a_row, C, ldc, D, ldd};
+    }
+    return p;
+}
+
+gemm15_status_t check_operands(const gemm15_plan* plan, const Prob& p, float beta) {
+    const int es = esize_of(plan->desc.a);
+    const int eo = esize_of(plan->desc.d);
+    if (p.M < 0 || p.N < 0 || p.K < 0) return GEMM15_ERR_INVALID_ARG;
+    if (p.M > (1ll << 31) - 256 || p.N > (1ll << 31) - 256 || p.K > (1ll << 31) - 256)
+        return GEMM15_ERR_INVALID_ARG;
+    if (p.M == 0 || p.N == 0) return GEMM15_OK;
+    if (!p.D) return GEMM15_ERR_INVALID_ARG;
+    if (beta != 0.0f && !p.C) return GEMM15_ERR_INVALID_ARG;
+    if (p.K > 0 && (!p.A || !p.B)) return GEMM15_ERR_INVALID_ARG;
+    // leading dimensions must cover the contiguous extent
+    if (p.K > 0) {
+        if (p.lda < (p.a_kmajor ? p.K : p.M)) return GEMM15_ERR_INVALID_ARG;
+        if (p.ldb < (p.b_kmajor ? p.K : p.N)) return GEMM15_ERR_INVALID_ARG;
+        if (!aligned16(p.A) || !aligned16(p.B)) return GEMM15_ERR_ALIGNMENT;
+        if ((p.lda * es) % 16 || (p.ldb * es) % 16) return GEMM15_ERR_ALIGNMENT;
+    }
+    if (p.ldd < p.N) return GEMM15_ERR_INVALID_ARG;
+    if (!aligned16(p.D) || (p.ldd * eo) % 16) return GEMM15_ERR_ALIGNMENT;
+    if (beta != 0.0f) {
+        if (p.ldc < p.N) return GEMM15_ERR_INVALID_ARG;
+        if (!aligned16(p.C) || (p.ldc * eo) % 16) return GEMM15_ERR_ALIGNMENT;
+    }
+    return GEMM15_OK;
+}
+
+// ------------------------------------------------------------------ planner
+
+struct Decision {
+    int bn = 256;
+    int bk = 64;
+    int sched = SCHED_DP;
+    int grid = 1;
+    int32_t m_blocks = 0, n_blocks = 0, tiles = 0, k_blocks = 0;
+    int32_t dp_tiles = 0, splits = 1, raster = 1;
+    int64_t sk_units = 0;
+    size_t ws_bytes = 0;
+    int flags = 0;
+};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+Decision decide(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
+    Decision d;
+    const Options& o = plan->opt;
+    d.bk = plan->elem == ELEM_E4M3 ? 128 : 64;
+    d.bn = o.tile_n ? o.tile_n : (N <= 128 ? 128 : 256);
+    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M));
+    d.n_blocks = static_cast<int32_t>(cdiv(N, d.bn));
+    d.tiles = d.m_blocks * d.n_blocks;
+    d.k_blocks = static_cast<int32_t>(cdiv(K, d.bk));
+    const int G = o.grid > 0 ? std::min(o.grid, plan->num_sms) : plan->num_sms;
+
+    int sched = o.schedule;
+    if (sched == 0) {
+        if (d.tiles >= G) {
+            const int64_t waves = cdiv(d.tiles, G);
+            const double eff = static_cast<double>(d.tiles) / static_cast<double>(waves * G);
+            sched = (eff >= 0.9 || d.k_blocks < 8) ? SCHED_DP : SCHED_SK;
+        } else if (d.k_blocks < 4) {
+            sched = SCHED_DP;
+        } else {
+            sched = (G / d.tiles <= 3) ? SCHED_SK : SCHED_SPLIT;
+        }
+    }
+    d.sched = sched;
+    d.raster = o.raster > 0 ? std::min<int32_t>(o.raster, d.m_blocks) : std::min<int32_t>(d.m_blocks, 16);
+    if (sched == SCHED_DP) {
+        d.grid = static_cast<int>(std::min<int64_t>(G, d.tiles));
+    } else if (sched == SCHED_SK) {
+        d.dp_tiles = d.tiles >= 2 * G ? (d.tiles / G - 1) * G : 0;
+        d.sk_units = static_cast<int64_t>(d.tiles - d.dp_tiles) * d.k_blocks;
+        d.grid = static_cast<int>(std::min<int64_t>(G, d.sk_units));
+        d.ws_bytes = static_cast<size_t>(d.grid) * TILE_M * d.bn * sizeof(float);
+        d.flags = d.grid;
+    } else {
+        int splits = o.splits > 0 ? o.splits : std::max(1, G / std::max<int32_t>(d.tiles, 1));
+        splits = static_cast<int>(std::min<int64_t>(splits, d.k_blocks));
+        splits = std::max(splits, 1);
+        d.splits = splits;
+        d.grid = static_cast<int>(std::min<int64_t>(G, static_cast<int64_t>(d.tiles) * splits));
+        d.ws_bytes = static_cast<size_t>(d.tiles) * splits * TILE_M * d.bn * sizeof(float);
+    }
+    return d;
+}
+
+gemm15_status_t ensure_ws(gemm15_plan* plan, size_t bytes, int flags) {
+    if (bytes > plan->ws_cap) {
+        if (plan->d_ws) cudaFree(plan->d_ws);
+        plan->d_ws = nullptr;
+        plan->ws_cap = 0;
+        size_t cap = std::max(bytes, static_cast<size_t>(1) << 20);
+        if (cudaMalloc(&plan->d_ws, cap) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM15_ERR_OOM;
+        }
+        plan->ws_cap = cap;
+    }
+    if (flags > plan->flags_cap) {
+        if (plan->d_flags) cudaFree(plan->d_flags);
+        plan->d_flags = nullptr;
+        plan->flags_cap = 0;
+        int cap = std::max(flags, 1024);
+        if (cudaMalloc(&plan->d_flags, cap * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM15_ERR_OOM;
+        }
+        if (cudaMemset(plan->d_flags, 0, cap * sizeof(uint32_t)) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        plan->flags_cap = cap;
+    }
+    return GEMM15_OK;
+}
+
+cudaError_t launch_kernel(int elem, int bn, const GemmParams& gp, int grid, cudaStream_t s) {
+    if (elem == ELEM_F16) return bn == 128 ? launch_gemm<ELEM_F16, 128>(gp, grid, s) : launch_gemm<ELEM_F16, 256>(gp, grid, s);
+    if (elem == ELEM_BF16) return bn == 128 ? launch_gemm<ELEM_BF16, 128>(gp, grid, s) : launch_gemm<ELEM_BF16, 256>(gp, grid, s);
+    return bn == 128 ? launch_gemm<ELEM_E4M3, 128>(gp, grid, s) : launch_gemm<ELEM_E4M3, 256>(gp, grid, s);
+}
+
+cudaError_t launch_reduce_kernel(int out_elem, const ReduceParams& rp, cudaStream_t s, int num_sms) {
+    const int64_t work = static_cast<int64_t>(rp.M) * ((rp.N + 7) / 8);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), num_sms * 8)));
+    return out_elem == ELEM_F16 ? launch_reduce<ELEM_F16>(rp, grid, s) : launch_reduce<ELEM_BF16>(rp, grid, s);
+}
+
+// Fills the operand-layout part of the kernel parameters.
+void fill_layout(const gemm15_plan* plan, GemmParams& gp, bool a_kmajor, bool b_kmajor, int bn) {
+    const bool f8 = plan->elem == ELEM_E4M3;
+    const int es = f8 ? 1 : 2;
+    const int bk = 128 / es;
+    const int umma_k = 32 / es;
+    gp.a_kmajor = a_kmajor;
+    gp.b_kmajor = b_kmajor;
+    // K-major, 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart;
+    // one MMA step along K advances 32 bytes inside the swizzle row.
+    // MN-major, 128-byte swizzle: 128-byte MN chunks (one TMA box of BK rows
+    // each) LBO apart, 8-row K groups 1024 B apart; one MMA step along K
+    // advances UMMA_K rows of 128 B.
+    const uint32_t mn_box = static_cast<uint32_t>((128 / es) * bk * es);
+    gp.a_lbo = a_kmajor ? 16u : mn_box;
+    gp.a_sbo = 1024u;
+    gp.a_kstep = a_kmajor ? 32u : static_cast<uint32_t>(umma_k * 128);
+    gp.b_lbo = b_kmajor ? 16u : mn_box;
+    gp.b_sbo = 1024u;
+    gp.b_kstep = b_kmajor ? 32u : static_cast<uint32_t>(umma_k * 128);
+    // instruction descriptor: A/B format 0 = f16 / e4m3, 1 = bf16
+    const uint32_t fmt = plan->elem == ELEM_BF16 ? 1u : 0u;
+    uint32_t idesc = 0;
+    idesc |= 1u << 4;                      // D format f32
+    idesc |= fmt << 7;                     // A format
+    idesc |= fmt << 10;                    // B format
+    idesc |= (a_kmajor ? 0u : 1u) << 15;   // A MN-major
+    idesc |= (b_kmajor ? 0u : 1u) << 16;   // B MN-major
+    idesc |= static_cast<uint32_t>(bn >> 3) << 17;
+    idesc |= static_cast<uint32_t>(TILE_M >> 4) << 24;
+    gp.idesc = idesc;
+}
+
+bool operand_maps(const gemm15_plan* plan, const Prob& p, int bn, CUtensorMap* tA, CUtensorMap* tB) {
+    const bool f8 = plan->elem == ELEM_E4M3;
+    const int es = f8 ? 1 : 2;
+    const uint32_t bk = 128 / es, w = 128 / es;
+    bool ok = true;
+    if (p.a_kmajor)
+        ok &= make_tmap(tA, plan->elem, p.A, p.K, p.M, p.lda * es, bk, TILE_M);
+    else
+        ok &= make_tmap(tA, plan->elem, p.A, p.M, p.K, p.lda * es, w, bk);
+    if (p.b_kmajor)
+        ok &= make_tmap(tB, plan->elem, p.B, p.K, p.N, p.ldb * es, bk, bn);
+    else
+        ok &= make_tmap(tB, plan->elem, p.B, p.N, p.K, p.ldb * es, w, bk);
+    return ok;
+}
+
+bool output_maps(const gemm15_plan* plan, const Prob& p, bool has_c, CUtensorMap* tC, CUtensorMap* tD) {
+    bool ok = make_tmap(tD, plan->out_elem, p.D, p.N, p.M, p.ldd * 2, EPI_COLS, 32);
+    if (has_c) ok &= make_tmap(tC, plan->out_elem, p.C, p.N, p.M, p.ldc * 2, EPI_COLS, 32);
+    else std::memset(tC, 0, sizeof(*tC));
+    return ok;
+}
+
+void record_config(gemm15_plan* plan, const Decision& d, int launches) {
+    gemm15_config_t& c = plan->last;
+    c.cta_group = 1;
+    c.tile_m = TILE_M;
+    c.tile_n = d.bn;
+    c.tile_k = d.bk;
+    c.stages = gemm_stages(plan->elem, d.bn);
+    c.schedule = d.sched;
+    c.grid = d.grid;
+    c.tiles = d.tiles;
+    c.splits = d.sched == SCHED_SPLIT ? d.splits : 1;
+    c.raster = d.raster;
+    c.launches = launches;
+    c.swap_ab = plan->desc.layout_cd == GEMM15_COL_MAJOR ? 1 : 0;
+}
+
+gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float beta,
+                          const float* scale_a, const float* scale_b, cudaStream_t s) {
+    gemm15_status_t st = check_operands(plan, p, beta);
+    if (st != GEMM15_OK) return st;
+    if (p.M == 0 || p.N == 0) {
+        std::memset(&plan->last, 0, sizeof(plan->last));
+        return GEMM15_OK;
+    }
+    const bool has_c = beta != 0.0f;
+    const bool relu = plan->desc.epilogue == GEMM15_EPI_RELU;
+    if (p.K == 0) {
+        ReduceParams rp{};
+        rp.ws = nullptr;
+        rp.splits = 0;
+        rp.tile_n = 256;
+        rp.n_blocks = 1;
+        rp.M = static_cast<int32_t>(p.M);
+        rp.N = static_cast<int32_t>(p.N);
+        rp.C = p.C;
+        rp.ldc = p.ldc;
+        rp.D = p.D;
+        rp.ldd = p.ldd;
+        rp.alpha = alpha;
+        rp.beta = beta;
+        rp.relu = relu;
+        rp.has_c = has_c;
+        if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
+        Decision d;
+        d.sched = SCHED_SPLIT;
+        d.splits = 0;
+        record_config(plan, d, 1);
+        plan->last.grid = 0;
+        return GEMM15_OK;
+    }
+    Decision d = decide(plan, p.M, p.N, p.K);
+    st = ensure_ws(plan, d.ws_bytes, d.flags);
+    if (st != GEMM15_OK) return st;
+
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!operand_maps(plan, p, d.bn, &gp.tmA, &gp.tmB)) return GEMM15_ERR_CUDA;
+    if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return GEMM15_ERR_CUDA;
+    gp.M = static_cast<int32_t>(p.M);
+    gp.N = static_cast<int32_t>(p.N);
+    gp.K = static_cast<int32_t>(p.K);
+    gp.k_blocks = d.k_blocks;
+    gp.m_blocks = d.m_blocks;
+    gp.n_blocks = d.n_blocks;
+    gp.tiles = d.tiles;
+    gp.raster = d.raster;
+    gp.sched = d.sched;
+    gp.dp_tiles = d.dp_tiles;
+    gp.splits = d.splits;
+    gp.has_c = has_c && d.sched != SCHED_SPLIT;
+    gp.sk_units = d.sk_units;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.scale_a = scale_a;
+    gp.scale_b = scale_b;
+    gp.relu = relu;
+    fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn);
+    gp.ws = plan->d_ws;
+    gp.flags = plan->d_flags;
+    gp.status = plan->d_status;
+    gp.epoch = ++plan->epoch == 0 ? ++plan->epoch : plan->epoch;
+    gp.timeout_ns = static_cast<uint64_t>(plan->opt.timeout_us) * 1000ull;
+    gp.fault_skip_flag = plan->opt.fault_skip_flag;
+    gp.groups = nullptr;
+    gp.num_groups = 0;
+    if (launch_kernel(plan->elem, d.bn, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    int launches = 1;
+    if (d.sched == SCHED_SPLIT) {
+        ReduceParams rp{};
+        rp.ws = plan->d_ws;
+        rp.splits = d.splits;
+        rp.tile_n = d.bn;
+        rp.n_blocks = d.n_blocks;
+        rp.M = gp.M;
+        rp.N = gp.N;
+        rp.C = p.C;
+        rp.ldc = p.ldc;
+        rp.D = p.D;
+        rp.ldd = p.ldd;
+        rp.alpha = alpha;
+        rp.beta = beta;
+        rp.scale_a = scale_a;
+        rp.scale_b = scale_b;
+        rp.relu = relu;
+        rp.has_c = has_c;
+        if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
+        ++launches;
+    }
+    record_config(plan, d, launches);
+    return GEMM15_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* gemm15_status_string(gemm15_status_t s) {
+    switch (s) {
+        case GEMM15_OK: return "ok";
+        case GEMM15_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM15_ERR_UNSUPPORTED: return "unsupported type or layout combination";
+        case GEMM15_ERR_ALIGNMENT: return "pointer or leading dimension not 16-byte aligned";
+        case GEMM15_ERR_CUDA: return "CUDA call failed";
+        case GEMM15_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+        case GEMM15_ERR_OOM: return "device memory allocation failed";
+        case GEMM15_ERR_DEVICE_FAULT: return "device reported an internal error";
+        case GEMM15_ERR_NO_DEVICE: return "no sm_103 device available";
+        case GEMM15_ERR_BAD_PLAN: return "invalid or destroyed plan handle";
+    }
+    return "unknown status";
+}
+
+gemm15_status_t gemm_plan_create(gemm15_plan_t* out, const gemm15_plan_desc_t* desc) {
+    if (!out || !desc) return GEMM15_ERR_INVALID_ARG;
+    *out = nullptr;
+    const gemm15_plan_desc_t& d = *desc;
+    auto valid_t = [](int t) { return t >= GEMM15_F16 && t <= GEMM15_E4M3; };
+    auto valid_l = [](int l) { return l == GEMM15_ROW_MAJOR || l == GEMM15_COL_MAJOR; };
+    if (!valid_t(d.a) || !valid_t(d.b) || !valid_t(d.c) || !valid_t(d.d) || !valid_t(d.acc) ||
+        !valid_l(d.layout_a) || !valid_l(d.layout_b) || !valid_l(d.layout_cd) ||
+        (d.epilogue != GEMM15_EPI_LINEAR && d.epilogue != GEMM15_EPI_RELU))
+        return GEMM15_ERR_INVALID_ARG;
+    if (d.acc != GEMM15_F32 || d.a != d.b) return GEMM15_ERR_UNSUPPORTED;
+    int elem, out_elem;
+    if (d.a == GEMM15_F16 && d.c == GEMM15_F16 && d.d == GEMM15_F16) {
+        elem = out_elem = ELEM_F16;
+    } else if (d.a == GEMM15_BF16 && d.c == GEMM15_BF16 && d.d == GEMM15_BF16) {
+        elem = out_elem = ELEM_BF16;
+    } else if (d.a == GEMM15_E4M3 && d.c == GEMM15_BF16 && d.d == GEMM15_BF16) {
+        elem = ELEM_E4M3;
+        out_elem = ELEM_BF16;
+    } else {
+        return GEMM15_ERR_UNSUPPORTED;
+    }
+    int dev = 0, count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+        cudaGetLastError();
+        return GEMM15_ERR_NO_DEVICE;
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM15_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return GEMM15_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return GEMM15_ERR_NO_DEVICE;
+    if (!encode_fn()) return GEMM15_ERR_CUDA;
+
+    gemm15_plan* p = new (std::nothrow) gemm15_plan();
+    if (!p) return GEMM15_ERR_OOM;
+    p->desc = d;
+    p->device = dev;
+    p->num_sms = prop.multiProcessorCount;
+    p->elem = elem;
+    p->out_elem = out_elem;
+    if (cudaMalloc(&p->d_status, sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(p->d_status, 0, sizeof(int32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return GEMM15_ERR_OOM;
+    }
+    if (ensure_ws(p, 0, p->num_sms) != GEMM15_OK) {
+        cudaFree(p->d_status);
+        delete p;
+        return GEMM15_ERR_OOM;
+    }
+    *out = p;
+    return GEMM15_OK;
+}
+
+gemm15_status_t gemm_plan_destroy(gemm15_plan_t plan) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    DeviceGuard g(plan->device);
+    if (plan->groups_done) {
+        cudaEventSynchronize(plan->groups_done);
+        cudaEventDestroy(plan->groups_done);
+    }
+    cudaFree(plan->d_status);
+    cudaFree(plan->d_flags);
+    cudaFree(plan->d_ws);
+    cudaFree(plan->d_groups);
+    if (plan->h_groups) cudaFreeHost(plan->h_groups);
+    for (void* b : plan->d_host_path) cudaFree(b);
+    cudaFree(plan->d_scales);
+    plan->magic = PLAN_DEAD;
+    delete plan;
+    return GEMM15_OK;
+}
+
+gemm15_status_t gemm_run_ex(gemm15_plan_t plan, const void* A, int64_t lda, const void* B,
+                            int64_t ldb, const void* C, int64_t ldc, void* D, int64_t ldd,
+                            int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                            const float* scale_a, const float* scale_b, void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if ((scale_a || scale_b) && plan->elem != ELEM_E4M3) return GEMM15_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    Prob p = normalise(plan, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
+    return run_dense(plan, p, alpha, beta, scale_a, scale_b, static_cast<cudaStream_t>(stream));
+}
+
+gemm15_status_t gemm_run(gemm15_plan_t plan, const void* A, const void* B, const void* C, void* D,
+                         int64_t M, int64_t N, int64_t K, float alpha, float beta, void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
+    return gemm_run_ex(plan, A, a_row ? K : M, B, b_row ? N : K, C, cd_row ? N : M, D,
+                       cd_row ? N : M, M, N, K, alpha, beta, nullptr, nullptr, stream);
+}
+
+gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB, const void* hC,
+                              void* hD, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                              float scale_a, float scale_b, void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (M < 0 || N < 0 || K < 0) return GEMM15_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM15_OK;
+    if (!hD || (K > 0 && (!hA || !hB)) || (beta != 0.0f && !hC)) return GEMM15_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int es = esize_of(plan->desc.a), eo = esize_of(plan->desc.d);
+    const size_t bytes[3] = {static_cast<size_t>(M * K * es), static_cast<size_t>(K * N * es),
+                             static_cast<size_t>(M * N * eo)};
+    for (int i = 0; i < 3; ++i) {
+        const size_t need = (bytes[i] + 255) & ~static_cast<size_t>(255);
+        if (need > plan->host_path_cap[i]) {
+            cudaFree(plan->d_host_path[i]);
+            plan->d_host_path[i] = nullptr;
+            plan->host_path_cap[i] = 0;
+            if (cudaMalloc(&plan->d_host_path[i], std::max<size_t>(need, 256)) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM15_ERR_OOM;
+            }
+            plan->host_path_cap[i] = std::max<size_t>(need, 256);
+        }
+    }
+    if (!plan->d_scales && cudaMalloc(&plan->d_scales, 2 * sizeof(float)) != cudaSuccess)
+        return GEMM15_ERR_OOM;
+    void* dA = plan->d_host_path[0];
+    void* dB = plan->d_host_path[1];
+    void* dCD = plan->d_host_path[2];  // C is copied in and D overwrites it in place
+    if (K > 0) {
+        if (cudaMemcpyAsync(dA, hA, bytes[0], cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(dB, hB, bytes[1], cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+    }
+    if (beta != 0.0f &&
+        cudaMemcpyAsync(dCD, hC, bytes[2], cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    const float* sa = nullptr;
+    const float* sb = nullptr;
+    if (plan->elem == ELEM_E4M3) {
+        float hs[2] = {scale_a, scale_b};
+        // cudaMemcpyAsync from pageable memory completes the host read before returning
+        if (cudaMemcpyAsync(plan->d_scales, hs, sizeof(hs), cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        sa = plan->d_scales;
+        sb = plan->d_scales + 1;
+    }
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
+    Prob p = normalise(plan, M, N, K, dA, a_row ? K : M, dB, b_row ? N : K, dCD, cd_row ? N : M,
+                       dCD, cd_row ? N : M);
+    gemm15_status_t st = run_dense(plan, p, alpha, beta, sa, sb, s);
+    if (st != GEMM15_OK) return st;
+    if (cudaMemcpyAsync(hD, dCD, bytes[2], cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    int32_t status = 0;
+    if (cudaMemcpy(&status, plan->d_status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    return static_cast<gemm15_status_t>(status);
+}
+
+gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* problems,
+                                 int32_t count, float alpha, float beta, void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (count < 0 || (count > 0 && !problems)) return GEMM15_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool has_c = beta != 0.0f;
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
+    const int bn = plan->opt.tile_n ? plan->opt.tile_n : 256;
+    const int bk = plan->elem == ELEM_E4M3 ? 128 : 64;
+
+    // validate every group first: nothing is launched on an argument error
+    std::vector<Prob> probs;
+    probs.reserve(count);
+    for (int32_t i = 0; i < count; ++i) {
+        const gemm15_problem_t& q = problems[i];
+        if (q.M < 0 || q.N < 0 || q.K < 0) return GEMM15_ERR_INVALID_ARG;
+        if (q.M == 0 || q.N == 0) continue;
+        if (q.K == 0) return GEMM15_ERR_UNSUPPORTED;
+        const int64_t lda = q.lda ? q.lda : (a_row ? q.K : q.M);
+        const int64_t ldb = q.ldb ? q.ldb : (b_row ? q.N : q.K);
+        const int64_t ldc = q.ldc ? q.ldc : (cd_row ? q.N : q.M);
+        const int64_t ldd = q.ldd ? q.ldd : (cd_row ? q.N : q.M);
+        Prob p = normalise(plan, q.M, q.N, q.K, q.A, lda, q.B, ldb, q.C, ldc, q.D, ldd);
+        gemm15_status_t st = check_operands(plan, p, beta);
+        if (st != GEMM15_OK) return st;
+        probs.push_back(p);
+    }
+    const int ng = static_cast<int>(probs.size());
+    if (ng == 0) {
+        std::memset(&plan->last, 0, sizeof(plan->last));
+        return GEMM15_OK;
+    }
+    if (ng > plan->groups_cap) {
+        if (plan->groups_done) cudaEventSynchronize(plan->groups_done);
+        cudaFree(plan->d_groups);
+        if (plan->h_groups) cudaFreeHost(plan->h_groups);
+        plan->d_groups = nullptr;
+        plan->h_groups = nullptr;
+        plan->groups_cap = 0;
+        const int cap = std::max(ng, 64);
+        if (cudaMalloc(&plan->d_groups, cap * sizeof(GroupEntry)) != cudaSuccess ||
+            cudaMallocHost(&plan->h_groups, cap * sizeof(GroupEntry)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM15_ERR_OOM;
+        }
+        plan->groups_cap = cap;
+    }
+    if (!plan->groups_done &&
+        cudaEventCreateWithFlags(&plan->groups_done, cudaEventDisableTiming) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    // the previous grouped call's copy must have read the staging buffer
+    if (cudaEventSynchronize(plan->groups_done) != cudaSuccess) return GEMM15_ERR_CUDA;
+
+    const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
+    int32_t tiles = 0;
+    bool mixed_layout = false;
+    for (int i = 0; i < ng; ++i) {
+        const Prob& p = probs[i];
+        if (p.a_kmajor != probs[0].a_kmajor || p.b_kmajor != probs[0].b_kmajor) mixed_layout = true;
+        GroupEntry& e = plan->h_groups[i];
+        std::memset(&e, 0, sizeof(e));
+        if (!operand_maps(plan, p, bn, &e.tmA, &e.tmB)) return GEMM15_ERR_CUDA;
+        if (!output_maps(plan, p, has_c, &e.tmC, &e.tmD)) return GEMM15_ERR_CUDA;
+        e.M = static_cast<int32_t>(p.M);
+        e.N = static_cast<int32_t>(p.N);
+        e.K = static_cast<int32_t>(p.K);
+        e.k_blocks = static_cast<int32_t>(cdiv(p.K, bk));
+        e.m_blocks = static_cast<int32_t>(cdiv(p.M, TILE_M));
+        e.n_blocks = static_cast<int32_t>(cdiv(p.N, bn));
+        e.tile_start = tiles;
+        e.has_c = has_c;
+        e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
+                                        : std::min<int32_t>(e.m_blocks, 16);
+        const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;
+        if (tiles + t > (1ll << 30)) return GEMM15_ERR_INVALID_ARG;
+        tiles += static_cast<int32_t>(t);
+    }
+    if (mixed_layout) return GEMM15_ERR_UNSUPPORTED;  // normalisation is per plan: cannot happen
+    if (cudaMemcpyAsync(plan->d_groups, plan->h_groups, ng * sizeof(GroupEntry),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaEventRecord(plan->groups_done, s) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.tiles = tiles;
+    gp.sched = SCHED_DP;
+    gp.splits = 1;
+    gp.k_blocks = 0;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.relu = plan->desc.epilogue == GEMM15_EPI_RELU;
+    gp.has_c = has_c;
+    fill_layout(plan, gp, probs[0].a_kmajor, probs[0].b_kmajor, bn);
+    gp.ws = plan->d_ws;
+    gp.flags = plan->d_flags;
+    gp.status = plan->d_status;
+    gp.epoch = ++plan->epoch == 0 ? ++plan->epoch : plan->epoch;
+    gp.timeout_ns = static_cast<uint64_t>(plan->opt.timeout_us) * 1000ull;
+    gp.fault_skip_flag = -1;
+    gp.groups = plan->d_groups;
+    gp.num_groups = ng;
+    const int grid = std::min(G, tiles);
+    if (launch_kernel(plan->elem, bn, gp, grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    Decision d;
+    d.bn = bn;
+    d.bk = bk;
+    d.sched = SCHED_DP;
+    d.grid = grid;
+    d.tiles = tiles;
+    d.raster = 16;
+    record_config(plan, d, 1);
+    return GEMM15_OK;
+}
+
+gemm15_status_t gemm_plan_query_error(gemm15_plan_t plan) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM15_ERR_CUDA;
+    int32_t status = 0;
+    if (cudaMemcpy(&status, plan->d_status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    if (status != 0 && cudaMemset(plan->d_status, 0, sizeof(int32_t)) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    if (status < 0 || status > GEMM15_ERR_BAD_PLAN) return GEMM15_ERR_DEVICE_FAULT;
+    return static_cast<gemm15_status_t>(status);
+}
+
+gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option, int64_t v) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    Options& o = plan->opt;
+    switch (option) {
+        case GEMM15_OPT_SCHEDULE:
+            if (v < 0 || v > 3) return GEMM15_ERR_INVALID_ARG;
+            o.schedule = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_SPLITS:
+            if (v < 0 || v > 4096) return GEMM15_ERR_INVALID_ARG;
+            o.splits = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_CTA_GROUP:
+            if (v != 0 && v != 1) return v == 2 ? GEMM15_ERR_UNSUPPORTED : GEMM15_ERR_INVALID_ARG;
+            o.cta_group = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_TILE_N:
+            if (v != 0 && v != 128 && v != 256) return GEMM15_ERR_INVALID_ARG;
+            o.tile_n = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_RASTER:
+            if (v < 0 || v > 4096) return GEMM15_ERR_INVALID_ARG;
+            o.raster = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_GRID:
+            if (v < 0 || v > 100000) return GEMM15_ERR_INVALID_ARG;
+            o.grid = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_TIMEOUT_US:
+            if (v < 1000 || v > 60000000) return GEMM15_ERR_INVALID_ARG;
+            o.timeout_us = v;
+            return GEMM15_OK;
+        case GEMM15_OPT_FAULT_SKIP_FLAG:
+            if (v < -1 || v > 100000) return GEMM15_ERR_INVALID_ARG;
+            o.fault_skip_flag = static_cast<int>(v);
+            return GEMM15_OK;
+    }
+    return GEMM15_ERR_INVALID_ARG;
+}
+
+gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (!out) return GEMM15_ERR_INVALID_ARG;
+    *out = plan->last;
+    return GEMM15_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,720 @@
+// Persistent warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   D = act(alpha * s_a * s_b * (A . B) + beta * C),  act in {identity, ReLU}
+//
+// The operation is the plan/run GEMM of the CUTLASS Python interface
+// ("Python packages associated with CUTLASS", section "CUTLASS Python
+// Interface"; alpha/beta as in the kwkr.cn blog "CUTLASS Python接口" section
+// 3.3; ReLU fused in the epilogue as in "CUTLASS Python 接口全解析" section 2.3).
+// Stream-K and grouped scheduling are the variants listed under "Current
+// functionality" of the CUTLASS README; this kernel is our own design for
+// Blackwell (tcgen05 / TMEM / TMA), not the pre-SM90 kernels the pages use.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: A and B tiles into a STAGES-deep shared ring
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
+//   warps 2..5  epilogue: TMEM -> registers -> alpha/beta/C/ReLU -> 16-bit ->
+//               swizzled shared staging -> TMA store (one 32-row quarter each)
+// The fp32 accumulator lives in TMEM, double-buffered (2 x TILE_N columns),
+// so the epilogue of tile i overlaps the mainloop of tile i+1.
+//
+// Every wait is bounded (p.timeout_ns); when one runs out the kernel records
+// DEV_ERR_TIMEOUT in the status word, every role leaves its loop, in-flight
+// copies and MMAs are drained with a bounded wait, TMEM is freed, and the
+// kernel returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace g15 {
+
+template <int ELEM, int BN>
+struct Traits {
+    static constexpr bool F8 = (ELEM == ELEM_E4M3);
+    static constexpr int ESIZE = F8 ? 1 : 2;           // bytes per A/B element
+    static constexpr int BK = 128 / ESIZE;             // one 128-byte swizzle row of K
+    static constexpr int UMMA_K = 32 / ESIZE;          // K per tcgen05.mma
+    static constexpr int KSTEPS = BK / UMMA_K;         // MMAs per k-block (4)
+    static constexpr int A_STAGE = TILE_M * 128;       // 16 KB
+    static constexpr int B_STAGE = BN * 128;           // 16 or 32 KB
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // 32 KB
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    // barriers: full[S], empty[S], acc_full[2], acc_empty[2], cbar[4][2], drain, epi
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(TMEM_COLS <= 512, "TMEM budget");
+};
+
+template <int ELEM>
+struct OutType;
+template <>
+struct OutType<ELEM_F16> {
+    using T = __half;
+};
+template <>
+struct OutType<ELEM_BF16> {
+    using T = __nv_bfloat16;
+};
+template <>
+struct OutType<ELEM_E4M3> {
+    using T = __nv_bfloat16;
+};
+
+// Packs two fp32 values into two 16-bit outputs (round to nearest even).
+template <int ELEM>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (ELEM == ELEM_F16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+template <int ELEM>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+    if constexpr (ELEM == ELEM_F16) {
+        __half2 h = *reinterpret_cast<__half2*>(&v);
+        return __half22float2(h);
+    } else {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+        return __bfloat1622float2(h);
+    }
+}
+
+// ------------------------------------------------------------------ errors
+
+struct Ctl {
+    volatile uint32_t* abort;  // shared flag: some role gave up
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void raise_error(volatile uint32_t* abort, int32_t* status, int code) {
+    atomicCAS(status, 0, code);
+    *abort = 1u;
+}
+
+static __device__ __noinline__ bool wait_bar_slow(volatile uint32_t* abort, int32_t* status,
+                                           uint64_t timeout_ns, uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                raise_error(abort, status, DEV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Waits for the phase of parity `parity` of `bar`; false if the kernel is
+// aborting or the wait ran out (which starts the abort).
+__device__ __forceinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(c.abort, c.status, c.timeout_ns, bar, parity);
+}
+
+// Bounded wait used only while draining after an abort (ignores the flag).
+static __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > budget_ns) return;
+    }
+}
+
+// ------------------------------------------------------------------ scheduling
+
+// One unit of work of a CTA: k-blocks [kb0, kb1) of output tile `tile`.
+struct Work {
+    int32_t tile;      // linear tile id (within its group)
+    int32_t group;     // group index (0 for dense)
+    int32_t m_blk, n_blk;
+    int32_t kb0, kb1;
+    int32_t kind;      // WK_*
+    int32_t slot;      // workspace slot for partial tiles
+};
+enum : int32_t { WK_FULL = 0, WK_PEER = 1, WK_OWNER = 2, WK_SPLIT = 3 };
+
+struct SchedState {
+    int32_t i;          // data-parallel / split item counter
+    int32_t phase;      // 0 data-parallel, 1 stream-K, 2 done
+    int64_t u, u_end;   // stream-K unit cursor
+};
+
+__device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int64_t cta) {
+    return (p.sk_units * cta) / gridDim.x;
+}
+
+__device__ __forceinline__ void raster_coords(int32_t tile, int32_t m_blocks, int32_t n_blocks,
+                                              int32_t raster, int32_t& mb, int32_t& nb) {
+    const int32_t band_tiles = raster * n_blocks;
+    const int32_t band = tile / band_tiles;
+    const int32_t first_m = band * raster;
+    const int32_t rows = min(raster, m_blocks - first_m);
+    const int32_t local = tile - band * band_tiles;
+    mb = first_m + local % rows;
+    nb = local / rows;
+}
+
+__device__ __forceinline__ void sched_init(const GemmParams& p, SchedState& s) {
+    s.i = 0;
+    s.phase = 0;
+    s.u = 0;
+    s.u_end = 0;
+    if (p.sched == SCHED_SK) {
+        s.u = sk_begin(p, blockIdx.x);
+        s.u_end = sk_begin(p, blockIdx.x + 1);
+    }
+}
+
+__device__ __forceinline__ void fill_coords(const GemmParams& p, Work& w) {
+    if (p.groups) {
+        // locate the group whose tile range holds w.tile (prefix sums ascend)
+        int32_t lo = 0, hi = p.num_groups - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (p.groups[mid].tile_start <= w.tile) lo = mid; else hi = mid - 1;
+        }
+        const GroupEntry& g = p.groups[lo];
+        w.group = lo;
+        raster_coords(w.tile - g.tile_start, g.m_blocks, g.n_blocks, g.raster, w.m_blk, w.n_blk);
+        w.kb0 = 0;
+        w.kb1 = g.k_blocks;
+    } else {
+        w.group = 0;
+        raster_coords(w.tile, p.m_blocks, p.n_blocks, p.raster, w.m_blk, w.n_blk);
+    }
+}
+
+__device__ __forceinline__ bool sched_next(const GemmParams& p, SchedState& s, Work& w) {
+    const int32_t G = gridDim.x;
+    if (p.sched == SCHED_SPLIT) {
+        const int32_t j = blockIdx.x + s.i * G;
+        if (j >= p.tiles * p.splits) return false;
+        ++s.i;
+        w.tile = j / p.splits;
+        const int32_t sp = j - w.tile * p.splits;
+        fill_coords(p, w);
+        w.kb0 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * sp) / p.splits);
+        w.kb1 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (sp + 1)) / p.splits);
+        w.kind = WK_SPLIT;
+        w.slot = (w.m_blk * p.n_blocks + w.n_blk) * p.splits + sp;
+        return true;
+    }
+    const int32_t dp_limit = (p.sched == SCHED_SK) ? p.dp_tiles : p.tiles;
+    if (s.phase == 0) {
+        const int32_t t = blockIdx.x + s.i * G;
+        if (t < dp_limit) {
+            ++s.i;
+            w.tile = t;
+            w.kb0 = 0;
+            w.kb1 = p.k_blocks;
+            fill_coords(p, w);
+            w.kind = WK_FULL;
+            w.slot = 0;
+            return true;
+        }
+        s.phase = (p.sched == SCHED_SK) ? 1 : 2;
+    }
+    if (s.phase == 1) {
+        if (s.u >= s.u_end) {
+            s.phase = 2;
+            return false;
+        }
+        const int32_t kb = p.k_blocks;
+        const int32_t rel = static_cast<int32_t>(s.u / kb);
+        const int64_t tile_u0 = static_cast<int64_t>(rel) * kb;
+        w.tile = p.dp_tiles + rel;
+        fill_coords(p, w);
+        w.kb0 = static_cast<int32_t>(s.u - tile_u0);
+        const int64_t end = min(s.u_end, tile_u0 + kb);
+        w.kb1 = static_cast<int32_t>(end - tile_u0);
+        if (w.kb0 == 0 && w.kb1 == kb) {
+            w.kind = WK_FULL;
+        } else if (w.kb0 == 0) {
+            w.kind = WK_OWNER;
+        } else {
+            w.kind = WK_PEER;
+        }
+        w.slot = blockIdx.x;
+        s.u = end;
+        return true;
+    }
+    return false;
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int ELEM, int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ GemmParams p) {
+    using TR = Traits<ELEM, BN>;
+    using OutT = typename OutType<ELEM>::T;
+    constexpr int STAGES = TR::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte-swizzled TMA / UMMA tiles
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sA = sbase + TR::OFF_A;
+    const uint32_t sB = sbase + TR::OFF_B;
+    const uint32_t sEpi = sbase + TR::OFF_EPI;
+    const uint32_t bar0 = sbase + TR::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    auto c_bar = [&](int q, int b) { return bar0 + 8u * (2 * STAGES + 4 + 2 * q + b); };
+    const uint32_t drain = bar0 + 8u * (2 * STAGES + 4 + 2 * EPI_WARPS);
+    const uint32_t epi_bar = drain + 8u;  // bounded barrier of the 4 epilogue warps
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + TR::OFF_MISC);
+    volatile uint32_t* tmem_slot = misc;
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), EPI_WARPS);
+        }
+        for (int q = 0; q < EPI_WARPS; ++q) {
+            mbar_init(c_bar(q, 0), 1);
+            mbar_init(c_bar(q, 1), 1);
+        }
+        mbar_init(drain, 1);
+        mbar_init(epi_bar, EPI_WARPS);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_u32(misc), TR::TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ============================ TMA producer
+        if (lane == 0) {
+            if (!p.groups) {
+                tma_prefetch_desc(&p.tmA);
+                tma_prefetch_desc(&p.tmB);
+            }
+            SchedState st;
+            sched_init(p, st);
+            Work w;
+            uint32_t n_issued = 0;
+            bool ok = true;
+            int last_group = -1;
+            while (ok && sched_next(p, st, w)) {
+                const CUtensorMap* tA = &p.tmA;
+                const CUtensorMap* tB = &p.tmB;
+                if (p.groups) {
+                    tA = &p.groups[w.group].tmA;
+                    tB = &p.groups[w.group].tmB;
+                    if (w.group != last_group) {
+                        tensormap_acquire(tA);
+                        tensormap_acquire(tB);
+                        last_group = w.group;
+                    }
+                }
+                const int32_t m0 = w.m_blk * TILE_M;
+                const int32_t n0 = w.n_blk * BN;
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    const int s = n_issued % STAGES;
+                    const uint32_t ph = (n_issued / STAGES) & 1u;
+                    if (!wait_bar(ctl, empty_bar(s), ph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), TR::STAGE_BYTES);
+                    const uint32_t dA = sA + s * TR::A_STAGE;
+                    const uint32_t dB = sB + s * TR::B_STAGE;
+                    const int32_t k0 = kb * TR::BK;
+                    if (p.a_kmajor) {
+                        tma_load_2d(dA, tA, full_bar(s), k0, m0);
+                    } else {
+                        constexpr int AW = 128 / TR::ESIZE;  // M elements per 128-byte row
+#pragma unroll
+                        for (int j = 0; j < TILE_M / AW; ++j)
+                            tma_load_2d(dA + j * AW * 128, tA, full_bar(s), m0 + j * AW, k0);
+                    }
+                    if (p.b_kmajor) {
+                        tma_load_2d(dB, tB, full_bar(s), k0, n0);
+                    } else {
+                        constexpr int BW = 128 / TR::ESIZE;  // N elements per 128-byte row
+#pragma unroll
+                        for (int j = 0; j < BN / BW; ++j)
+                            tma_load_2d(dB + j * BW * 128, tB, full_bar(s), n0 + j * BW, k0);
+                    }
+                    ++n_issued;
+                }
+            }
+            if (!ok || *abort_flag) {
+                // let every issued copy land before the CTA's shared memory goes away
+                const uint32_t outstanding = n_issued < STAGES ? n_issued : STAGES;
+                for (uint32_t i = 0; i < outstanding; ++i) {
+                    const uint32_t n = n_issued - 1 - i;
+                    drain_bar(full_bar(n % STAGES), (n / STAGES) & 1u, 200000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer (one thread)
+        if (lane == 0) {
+            const uint64_t adesc0 = sdesc_base(p.a_lbo, p.a_sbo);
+            const uint64_t bdesc0 = sdesc_base(p.b_lbo, p.b_sbo);
+            SchedState st;
+            sched_init(p, st);
+            Work w;
+            uint32_t n_used = 0, n_acc = 0;
+            bool ok = true, issued = false;
+            while (ok && sched_next(p, st, w)) {
+                const uint32_t ab = n_acc & 1u;
+                const uint32_t aph = (n_acc >> 1) & 1u;
+                if (!wait_bar(ctl, acce_bar(ab), aph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + ab * BN;
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    const int s = n_used % STAGES;
+                    const uint32_t ph = (n_used / STAGES) & 1u;
+                    if (!wait_bar(ctl, full_bar(s), ph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = sA + s * TR::A_STAGE;
+                    const uint32_t b_addr = sB + s * TR::B_STAGE;
+#pragma unroll
+                    for (int k = 0; k < TR::KSTEPS; ++k) {
+                        umma<1, TR::F8>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
+                                        sdesc_at(bdesc0, b_addr + k * p.b_kstep), p.idesc,
+                                        (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(empty_bar(s));
+                    ++n_used;
+                }
+                if (!ok) break;
+                umma_commit(accf_bar(ab));
+                ++n_acc;
+            }
+            if (issued && (!ok || *abort_flag)) {
+                umma_commit(drain);
+                drain_bar(drain, 0, 200000000ull);
+            }
+        }
+    } else {
+        // ============================ epilogue warps
+        const int q = warp & 3;                 // TMEM lane quarter of this warp
+        const int e = warp - 2;                 // epilogue warp index (buffers)
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t ebuf0 = sEpi + e * 2 * EPI_BUF_BYTES;
+        float alpha = p.alpha;
+        if (p.scale_a) alpha *= __ldg(p.scale_a);
+        if (p.scale_b) alpha *= __ldg(p.scale_b);
+        const float beta = p.beta;
+        const bool relu = p.relu != 0;
+        constexpr int NCH = BN / EPI_COLS;
+
+        // Bounded barrier of the four epilogue warps (mbarrier with count 4):
+        // release/acquire at CTA scope, and it cannot hang if a warp gives up.
+        uint32_t epi_phase = 0;
+        auto epi_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_bar);
+            const bool r = wait_bar(ctl, epi_bar, epi_phase);
+            epi_phase ^= 1u;
+            return r;
+        };
+
+        SchedState st;
+        sched_init(p, st);
+        Work w;
+        uint32_t n_acc = 0;
+        uint32_t n_chunk = 0;      // chunks staged by this warp (buffer parity)
+        uint32_t c_phase = 0;      // per-buffer C barrier parity bits
+        uint32_t c_pending = 0;    // C loads issued and not yet waited for
+        int last_group = -1;
+        bool ok = true;
+        while (ok && sched_next(p, st, w)) {
+            const uint32_t ab = n_acc & 1u;
+            const uint32_t aph = (n_acc >> 1) & 1u;
+            if (!wait_bar(ctl, accf_bar(ab), aph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+
+            int32_t M = p.M, N = p.N;
+            const CUtensorMap* tC = &p.tmC;
+            const CUtensorMap* tD = &p.tmD;
+            int32_t has_c = p.has_c;
+            if (p.groups) {
+                const GroupEntry& g = p.groups[w.group];
+                M = g.M;
+                N = g.N;
+                tC = &g.tmC;
+                tD = &g.tmD;
+                has_c = g.has_c;
+                if (lane == 0 && w.group != last_group) {
+                    tensormap_acquire(tC);
+                    tensormap_acquire(tD);
+                }
+                last_group = w.group;
+            }
+            const int32_t m0 = w.m_blk * TILE_M;
+            const int32_t n0 = w.n_blk * BN;
+            const int32_t row0 = m0 + q * 32;      // first row of this warp
+            const bool rows_live = row0 < M;
+            const int64_t tile_end_unit =
+                (static_cast<int64_t>(w.tile - p.dp_tiles) + 1) * p.k_blocks;
+
+            // stream-K owner: wait until every peer's partial is published
+            if (w.kind == WK_OWNER) {
+                if (threadIdx.x == 64) {
+                    for (int64_t b = blockIdx.x + 1; b < gridDim.x && sk_begin(p, b) < tile_end_unit; ++b) {
+                        if (sk_begin(p, b) == sk_begin(p, b + 1)) continue;
+                        const uint64_t t0 = globaltimer_ns();
+                        uint32_t it = 0;
+                        while (ld_acquire_gpu(p.flags + b) != p.epoch) {
+                            if ((++it & 15u) == 0) {
+                                if (*abort_flag) break;
+                                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                                    raise_error(ctl.abort, ctl.status, DEV_ERR_TIMEOUT);
+                                    break;
+                                }
+                            }
+                        }
+                        if (*abort_flag) break;
+                    }
+                }
+                if (!epi_sync() || *abort_flag) ok = false;
+            }
+
+            const bool to_ws = (w.kind == WK_PEER || w.kind == WK_SPLIT);
+            const bool stage_c = has_c && !to_ws && rows_live;
+#pragma unroll 1
+            for (int c = 0; ok && rows_live && c < NCH; ++c) {
+                const int32_t col0 = c * EPI_COLS;
+                if (n0 + col0 >= N) break;
+                const uint32_t b = n_chunk & 1u;
+                const uint32_t buf = ebuf0 + b * EPI_BUF_BYTES;
+                if (!to_ws) {
+                    // the store issued two chunks ago from this buffer must have read it
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                    if (stage_c && lane == 0) {
+                        mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
+                        tma_load_2d(buf, tC, c_bar(e, b), n0 + col0, row0);
+                        c_pending |= 1u << b;
+                    }
+                }
+                uint32_t r[2][32];
+                const uint32_t taddr = tmem_base + lane_base + ab * BN + col0;
+                tmem_ld32(taddr, r[0]);
+                tmem_ld32(taddr + 32, r[1]);
+                tmem_ld_wait();
+                float v[64];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = __uint_as_float(r[0][i]);
+                    v[32 + i] = __uint_as_float(r[1][i]);
+                }
+                if (w.kind == WK_OWNER) {
+                    // add the peers' partial tiles in CTA order (deterministic)
+                    for (int64_t pb = blockIdx.x + 1; pb < gridDim.x && sk_begin(p, pb) < tile_end_unit; ++pb) {
+                        if (sk_begin(p, pb) == sk_begin(p, pb + 1)) continue;
+                        const float4* src = reinterpret_cast<const float4*>(
+                            p.ws + static_cast<size_t>(pb) * TILE_M * BN +
+                            static_cast<size_t>(q * 32 + lane) * BN + col0);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float4 t = __ldcg(src + i);
+                            v[4 * i + 0] += t.x;
+                            v[4 * i + 1] += t.y;
+                            v[4 * i + 2] += t.z;
+                            v[4 * i + 3] += t.w;
+                        }
+                    }
+                }
+                if (to_ws) {
+                    float4* dst = reinterpret_cast<float4*>(
+                        p.ws + static_cast<size_t>(w.slot) * TILE_M * BN +
+                        static_cast<size_t>(q * 32 + lane) * BN + col0);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                    continue;
+                }
+                if (stage_c) {
+                    if (!wait_bar(ctl, c_bar(e, b), (c_phase >> b) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    c_phase ^= 1u << b;
+                    c_pending &= ~(1u << b);
+                }
+                uint8_t* bufp = smem + (buf - sbase);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane % 8)
+                    uint4* slot = reinterpret_cast<uint4*>(bufp + lane * 128 + ((j ^ (lane & 7)) << 4));
+                    float o[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) o[t] = alpha * v[8 * j + t];
+                    if (stage_c) {
+                        const uint4 cv = *slot;
+                        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f = unpack2<ELEM>(cw[t]);
+                            o[2 * t] = fmaf(beta, f.x, o[2 * t]);
+                            o[2 * t + 1] = fmaf(beta, f.y, o[2 * t + 1]);
+                        }
+                    }
+                    if (relu) {
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) o[t] = o[t] > 0.0f ? o[t] : (o[t] != o[t] ? o[t] : 0.0f);
+                    }
+                    *slot = make_uint4(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
+                                       pack2<ELEM>(o[4], o[5]), pack2<ELEM>(o[6], o[7]));
+                }
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tD, buf, n0 + col0, row0);
+                    bulk_commit();
+                }
+                ++n_chunk;
+            }
+            // accumulator fully read: hand the TMEM buffer back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(ab));
+            ++n_acc;
+
+            if (w.kind == WK_PEER) {
+                // publish this CTA's partial tile for the owner
+                __threadfence();
+                const bool synced = epi_sync();
+                if (threadIdx.x == 64 && ok && synced && !*abort_flag &&
+                    p.fault_skip_flag != static_cast<int32_t>(blockIdx.x))
+                    st_release_gpu(p.flags + blockIdx.x, p.epoch);
+                if (!synced) ok = false;
+            }
+            if (*abort_flag) ok = false;
+        }
+        // drain outstanding C loads and D stores of this warp
+        if (lane == 0) {
+            for (int b = 0; b < 2; ++b)
+                if (c_pending & (1u << b)) drain_bar(c_bar(e, b), (c_phase >> b) & 1u, 200000000ull);
+            bulk_wait<0>();
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<1>(tmem_base, TR::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ split-K reduction
+
+// D = act(alpha * sum_s partial_s + beta * C) for split-K runs (splits >= 1),
+// or D = act(beta * C) when K == 0 (splits == 0).  Each thread owns 8
+// consecutive columns of one row; partial tiles are summed in split order.
+template <int ELEM>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    using OutT = typename OutType<ELEM>::T;
+    const int64_t nv = (p.N + 7) / 8;
+    const int64_t total = static_cast<int64_t>(p.M) * nv;
+    float alpha = p.alpha;
+    if (p.scale_a) alpha *= __ldg(p.scale_a);
+    if (p.scale_b) alpha *= __ldg(p.scale_b);
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int32_t m = static_cast<int32_t>(idx / nv);
+        const int32_t n = static_cast<int32_t>(idx - static_cast<int64_t>(m) * nv) * 8;
+        float acc[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
+        if (p.splits > 0) {
+            const int32_t mb = m / TILE_M, r = m - mb * TILE_M;
+            const int32_t nb = n / p.tile_n, cc = n - nb * p.tile_n;
+            const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;
+            const float* src = p.ws + static_cast<size_t>(mb * p.n_blocks + nb) * p.splits * tile_elems +
+                               static_cast<size_t>(r) * p.tile_n + cc;
+            for (int32_t s = 0; s < p.splits; ++s) {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+                const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 1);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+                src += tile_elems;
+            }
+        }
+        const int nvalid = min(8, p.N - n);
+        const OutT* crow = reinterpret_cast<const OutT*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
+        OutT* drow = reinterpret_cast<OutT*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
+        float o[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            float x = alpha * acc[t];
+            if (p.has_c && t < nvalid) {
+                float cv;
+                if constexpr (ELEM == ELEM_F16) cv = __half2float(crow[t]);
+                else cv = __bfloat162float(crow[t]);
+                x = fmaf(p.beta, cv, x);
+            }
+            if (p.relu) x = x > 0.0f ? x : (x != x ? x : 0.0f);
+            o[t] = x;
+        }
+        if (nvalid == 8) {
+            *reinterpret_cast<uint4*>(drow) =
+                make_uint4(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
+                           pack2<ELEM>(o[4], o[5]), pack2<ELEM>(o[6], o[7]));
+        } else {
+            for (int t = 0; t < nvalid; ++t) {
+                if constexpr (ELEM == ELEM_F16) drow[t] = __float2half_rn(o[t]);
+                else drow[t] = __float2bfloat16_rn(o[t]);
+            }
+        }
+    }
+}
+
+}  // namespace g15

@@ -1,0 +1,74 @@
+// Kernel parameter blocks shared by the host planner and the sm_103a kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace g15 {
+
+enum ElemKind : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_E4M3 = 2 };
+enum Schedule : int { SCHED_DP = 1, SCHED_SK = 2, SCHED_SPLIT = 3 };
+enum DeviceError : int { DEV_ERR_TIMEOUT = 5, DEV_ERR_FAULT = 7 };
+
+constexpr int TILE_M = 128;         // rows of A per CTA (UMMA M for one SM)
+constexpr int EPI_WARPS = 4;        // epilogue warps (one per 32-lane TMEM quarter)
+constexpr int NUM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int EPI_COLS = 64;        // output columns per epilogue chunk (128 B of 16-bit)
+constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32-row x 128-byte epilogue staging box
+
+// One group of a grouped GEMM as the kernel reads it from device memory.
+struct alignas(128) GroupEntry {
+    CUtensorMap tmA, tmB, tmC, tmD;
+    int32_t M, N, K, k_blocks;
+    int32_t m_blocks, n_blocks, tile_start, has_c;
+    int32_t raster, pad0, pad1, pad2;
+};
+
+struct GemmParams {
+    CUtensorMap tmA, tmB, tmC, tmD;  // dense problem (unused when grouped)
+    int32_t M, N, K;
+    int32_t k_blocks;                 // ceil(K / BK)
+    int32_t m_blocks, n_blocks, tiles;
+    int32_t raster;                   // M-blocks per raster band
+    int32_t sched;                    // Schedule
+    int32_t dp_tiles;                 // SK: tiles done whole before the stream-K region
+    int32_t splits;                   // SPLIT: k-splits per tile
+    int32_t has_c;                    // beta != 0 (C is read)
+    int64_t sk_units;                 // SK: (tiles - dp_tiles) * k_blocks
+    float alpha, beta;
+    const float* scale_a;             // fp8 per-tensor scales (device), or null
+    const float* scale_b;
+    int32_t relu;
+    // operand layouts in shared memory (bytes) and the MMA instruction descriptor
+    uint32_t a_kmajor, b_kmajor;
+    uint32_t a_lbo, a_sbo, a_kstep;
+    uint32_t b_lbo, b_sbo, b_kstep;
+    uint32_t idesc;
+    // workspace and status
+    float* ws;                        // fp32 partial tiles
+    uint32_t* flags;                  // SK partial-ready flags, one per CTA
+    int32_t* status;                  // device status word (0 = ok)
+    uint32_t epoch;                   // launch sequence number (flag value)
+    uint64_t timeout_ns;              // bound of every wait
+    int32_t fault_skip_flag;          // test hook (-1 = off)
+    // grouped problems (device table) or null
+    const GroupEntry* groups;
+    int32_t num_groups;
+};
+
+struct ReduceParams {
+    const float* ws;
+    int32_t splits;                   // 0: no product term (K == 0)
+    int32_t tile_n, n_blocks;
+    int32_t M, N;
+    const void* C;
+    int64_t ldc;
+    void* D;
+    int64_t ldd;
+    float alpha, beta;
+    const float* scale_a;
+    const float* scale_b;
+    int32_t relu, has_c;
+};
+
+}  // namespace g15

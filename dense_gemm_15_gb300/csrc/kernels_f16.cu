@@ -1,0 +1,8 @@
+// Instantiations of the sm_103a GEMM kernels for f16 operands.
+#include "launch_impl.cuh"
+
+namespace g15 {
+template cudaError_t launch_gemm<ELEM_F16, 128>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_gemm<ELEM_F16, 256>(const GemmParams&, int, cudaStream_t);
+template cudaError_t launch_reduce<ELEM_F16>(const ReduceParams&, int, cudaStream_t);
+}  // namespace g15

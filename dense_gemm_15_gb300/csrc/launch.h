@@ -1,0 +1,23 @@
+// Host-side launch entry points of the sm_103a kernels (one translation unit
+// per element type instantiates them).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gemm_params.h"
+
+namespace g15 {
+
+// Persistent tcgen05 GEMM, one-SM tiles of 128 x BN (BN = 128 or 256).
+template <int ELEM, int BN>
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+
+// Split-K reduction / K == 0 epilogue (ELEM selects the 16-bit C/D type).
+template <int ELEM>
+cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream);
+
+// Shared-memory bytes and pipeline depth of a GEMM instantiation.
+int gemm_smem_bytes(int elem, int bn);
+int gemm_stages(int elem, int bn);
+
+}  // namespace g15

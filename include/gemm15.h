@@ -1,0 +1,201 @@
+/*
+ * gemm15 -- dense GEMM D = act(alpha * (A . B) + beta * C) on one GB300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * The operation and the plan/run split follow the CUTLASS Python interface
+ * as the pages describe it:
+ *   - "Python packages associated with CUTLASS" (CUTLASS python/README.md),
+ *     section "CUTLASS Python Interface": a plan is declared with element type
+ *     and layout, then `plan.run(A, B, C, D)` computes D = A . B + C.
+ *   - "CUTLASS Python 接口全解析", section 2.1: element_A/B/C/D/accumulator
+ *     are bound separately at plan construction and cannot change afterwards;
+ *     one plan runs tensors of any shape with matching types.  Section 2.2:
+ *     compilation is separate from execution.  Section 2.3: an elementwise
+ *     activation (ReLU) is fused into the epilogue, and `run()` is
+ *     asynchronous with an explicit `sync()`.
+ *   - kwkr.cn blog "CUTLASS Python接口", section 3.3: the linear combination
+ *     D = alpha * A * B + beta * C with fp32 accumulation.
+ *   - "Python packages associated with CUTLASS", section "Current
+ *     functionality": stream-K and grouped GEMM variants.
+ *   - "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL
+ *     backend", section "CuteDSL 后端支持的功能": FP8 mm and grouped mm.
+ *
+ * Conventions for every entry point:
+ *   - A is M x K, B is K x N, C and D are M x N.  Leading dimensions are in
+ *     elements.  Row-major X with leading dimension ld stores X[i][j] at
+ *     X + i*ld + j; column-major stores it at X + j*ld + i.
+ *   - Matrix pointers are DEVICE pointers on the plan's device (except in
+ *     gemm_run_host), owned by the caller, and must stay valid until the work
+ *     enqueued on `stream` has finished.
+ *   - Every pointer and every leading dimension * element size must be a
+ *     multiple of 16 bytes (tensor-memory-accelerator rule); otherwise the call
+ *     returns GEMM15_ERR_ALIGNMENT and launches nothing.  There is no fallback
+ *     path.
+ *   - Argument errors are returned synchronously and nothing is launched.
+ *     Errors detected on the device (a bounded wait that ran out) are written
+ *     to the plan's status word; read them with gemm_plan_query_error after
+ *     synchronising the stream.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - A plan may be used from one host thread at a time.
+ */
+#ifndef GEMM15_H_
+#define GEMM15_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM15_F16 = 0,  /* IEEE binary16 */
+    GEMM15_BF16 = 1, /* bfloat16 */
+    GEMM15_F32 = 2,  /* binary32: accumulator type only */
+    GEMM15_E4M3 = 3  /* OCP fp8 e4m3 (finite-only variant), A and B only */
+} gemm15_dtype_t;
+
+typedef enum { GEMM15_ROW_MAJOR = 0, GEMM15_COL_MAJOR = 1 } gemm15_layout_t;
+
+/* Epilogue activation, applied after alpha*(A.B) + beta*C ("CUTLASS Python
+ * 接口全解析" section 2.3; kwkr.cn blog section 5.2 applies ReLU after the
+ * linear combination). */
+typedef enum { GEMM15_EPI_LINEAR = 0, GEMM15_EPI_RELU = 1 } gemm15_epilogue_t;
+
+typedef enum {
+    GEMM15_OK = 0,
+    GEMM15_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum, ... */
+    GEMM15_ERR_UNSUPPORTED = 2,  /* type / layout combination not provided */
+    GEMM15_ERR_ALIGNMENT = 3,    /* pointer or leading dimension not 16-byte aligned */
+    GEMM15_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed */
+    GEMM15_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+    GEMM15_ERR_OOM = 6,          /* plan workspace could not be allocated */
+    GEMM15_ERR_DEVICE_FAULT = 7, /* the device reported an internal error */
+    GEMM15_ERR_NO_DEVICE = 8,    /* no sm_103 device available */
+    GEMM15_ERR_BAD_PLAN = 9      /* null, destroyed or foreign plan handle */
+} gemm15_status_t;
+
+typedef struct gemm15_plan* gemm15_plan_t;
+
+/* Plan description: element types and layouts, fixed for the plan's life.
+ * Supported: a == b in {F16, BF16} with c == d == a; or a == b == E4M3 with
+ * c == d == BF16.  acc must be F32.  layout_a / layout_b are free; layout_cd
+ * applies to both C and D. */
+typedef struct {
+    gemm15_dtype_t a, b, c, d, acc;
+    gemm15_layout_t layout_a, layout_b, layout_cd;
+    gemm15_epilogue_t epilogue;
+} gemm15_plan_desc_t;
+
+/* Creates a plan on the current CUDA device: validates the description,
+ * allocates the plan's small device state (status word, stream-K flags) and
+ * resolves the tensor-map encoder.  Kernels are compiled ahead of time into
+ * this library, so this is the whole "compile" step ("CUTLASS Python 接口全解析"
+ * section 2.2).  *out receives the handle, owned by the caller until
+ * gemm_plan_destroy.  Errors: INVALID_ARG (null), UNSUPPORTED (types),
+ * NO_DEVICE, CUDA, OOM. */
+gemm15_status_t gemm_plan_create(gemm15_plan_t* out, const gemm15_plan_desc_t* desc);
+
+/* Frees the plan and all device / pinned memory it owns.  The caller must have
+ * synchronised every stream the plan was used on.  BAD_PLAN for null or
+ * already destroyed handles. */
+gemm15_status_t gemm_plan_destroy(gemm15_plan_t plan);
+
+/* D = act(alpha * (A . B) + beta * C) with packed leading dimensions (lda = K
+ * for row-major A, M for column-major; ldb = N or K; ldc = ldd = N for
+ * row-major C/D, M for column-major).  Asynchronous on `stream`.
+ * M == 0 or N == 0: nothing to do, returns OK.  K == 0: D = act(beta * C).
+ * beta == 0: C is never read and may be NULL.  The plan's workspace grows on
+ * demand (a cudaMalloc outside the stream); do not call a growing shape for the
+ * first time inside stream capture. */
+gemm15_status_t gemm_run(gemm15_plan_t plan, const void* A, const void* B, const void* C,
+                         void* D, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                         void* stream);
+
+/* gemm_run with explicit leading dimensions and, for E4M3 plans, per-tensor
+ * fp32 dequantisation scales: the real value of an fp8 operand element is
+ * scale * stored value, so D = act(alpha * s_a * s_b * (A_q . B_q) + beta * C).
+ * scale_a / scale_b are DEVICE pointers to one float each, or NULL for 1.0;
+ * they are read by the kernel, so they may change between enqueued runs. */
+gemm15_status_t gemm_run_ex(gemm15_plan_t plan, const void* A, int64_t lda, const void* B,
+                            int64_t ldb, const void* C, int64_t ldc, void* D, int64_t ldd,
+                            int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                            const float* scale_a, const float* scale_b, void* stream);
+
+/* End-to-end variant for callers holding HOST buffers (packed layouts as in
+ * gemm_run; pinned memory recommended).  Copies A, B (and C when beta != 0)
+ * into plan-owned device buffers, runs the GEMM and copies D back, all on
+ * `stream`, then synchronises the stream and returns the device status.
+ * scale_a / scale_b are HOST floats here (1.0 for 16-bit plans). */
+gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB,
+                              const void* hC, void* hD, int64_t M, int64_t N, int64_t K,
+                              float alpha, float beta, float scale_a, float scale_b,
+                              void* stream);
+
+/* One problem of a grouped GEMM (device pointers, leading dimensions as in
+ * gemm_run_ex; 0 means packed). */
+typedef struct {
+    int64_t M, N, K;
+    const void* A;
+    const void* B;
+    const void* C;
+    void* D;
+    int64_t lda, ldb, ldc, ldd;
+} gemm15_problem_t;
+
+/* Grouped GEMM: D_g = act(alpha * (A_g . B_g) + beta * C_g) for every g in one
+ * launch ("Python packages associated with CUTLASS", "Current functionality";
+ * "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL backend",
+ * grouped mm).  `problems` is a HOST array of `count` entries, read during the
+ * call only.  The plan copies a problem table (shapes, pointers, tensor maps)
+ * to device memory on `stream`.  Groups with M, N == 0 are skipped; K == 0
+ * groups are not supported (UNSUPPORTED).  Every group must pass the same
+ * alignment rules as gemm_run_ex. */
+gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* problems,
+                                 int32_t count, float alpha, float beta, void* stream);
+
+/* Reads and clears the plan's device status word (GEMM15_OK if no device-side
+ * error was recorded).  Synchronises the plan's device; call it after the
+ * enqueued work has finished, like `args.sync()` ("CUTLASS Python 接口全解析"
+ * section 2.3). */
+gemm15_status_t gemm_plan_query_error(gemm15_plan_t plan);
+
+/* Static description of a status code (never NULL). */
+const char* gemm15_status_string(gemm15_status_t status);
+
+/* Tuning / test options (defaults are the library's own choices). */
+typedef enum {
+    GEMM15_OPT_SCHEDULE = 0,     /* 0 auto, 1 data-parallel, 2 stream-K, 3 split-K + reduce */
+    GEMM15_OPT_SPLITS = 1,       /* split-K: splits per tile (0 = auto) */
+    GEMM15_OPT_CTA_GROUP = 2,    /* 0 auto, 1 one-SM tiles, 2 SM-pair tiles */
+    GEMM15_OPT_TILE_N = 3,       /* 0 auto, 128 or 256 */
+    GEMM15_OPT_RASTER = 4,       /* 0 auto, else M-blocks per raster band */
+    GEMM15_OPT_GRID = 5,         /* 0 auto (one CTA per SM), else max CTAs */
+    GEMM15_OPT_TIMEOUT_US = 6,   /* bound of every device-side wait, microseconds */
+    GEMM15_OPT_FAULT_SKIP_FLAG = 7 /* test hook: stream-K peer CTA that skips its
+                                      partial-ready flag (-1 = none) */
+} gemm15_option_t;
+
+/* Sets an option on the plan; INVALID_ARG for unknown options or values. */
+gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option, int64_t value);
+
+/* The configuration the last run of the plan launched. */
+typedef struct {
+    int32_t cta_group;   /* 1 or 2 */
+    int32_t tile_m, tile_n, tile_k;
+    int32_t stages;
+    int32_t schedule;    /* 1 data-parallel, 2 stream-K, 3 split-K + reduce */
+    int32_t grid;        /* CTAs launched by the GEMM kernel */
+    int32_t tiles;       /* output tiles */
+    int32_t splits;      /* split-K splits per tile (1 otherwise) */
+    int32_t raster;      /* M-blocks per raster band */
+    int32_t launches;    /* kernels launched by the run */
+    int32_t swap_ab;     /* 1 if the run computed D^T = B^T . A^T */
+} gemm15_config_t;
+
+gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM15_H_ */

@@ -1,0 +1,77 @@
+"""The C-ABI library loads and exports every entry point include/gemm15.h
+declares; host-side argument checks behave as documented.  CPU only: no call
+here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_gemm_15_gb300 import binding as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "gemm15.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_lists_expected_functions():
+    names = header_functions()
+    assert set(g.EXPORTED) == set(names), names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = g.load()
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for s in range(10):
+        txt = g.status_string(s)
+        assert txt and txt != "unknown status"
+    assert g.status_string(999) == "unknown status"
+
+
+def test_null_plan_is_rejected_without_device():
+    lib = g.load()
+    assert lib.gemm_plan_destroy(None) == g.ERR_BAD_PLAN
+    assert lib.gemm_run(None, None, None, None, None, 1, 1, 1, 1.0, 0.0, None) == g.ERR_BAD_PLAN
+    assert lib.gemm_plan_query_error(None) == g.ERR_BAD_PLAN
+    assert lib.gemm_plan_set_option(None, 0, 0) == g.ERR_BAD_PLAN
+    assert lib.grouped_gemm_run(None, None, 0, 1.0, 0.0, None) == g.ERR_BAD_PLAN
+
+
+def test_plan_create_argument_checks():
+    lib = g.load()
+    h = ctypes.c_void_p()
+    assert lib.gemm_plan_create(None, None) == g.ERR_INVALID_ARG
+    bad = g.PlanDesc(7, 0, 0, 0, 2, 0, 0, 0, 0)
+    assert lib.gemm_plan_create(ctypes.byref(h), ctypes.byref(bad)) == g.ERR_INVALID_ARG
+    mixed = g.PlanDesc(g.F16, g.BF16, g.F16, g.F16, g.F32, 0, 0, 0, 0)
+    assert lib.gemm_plan_create(ctypes.byref(h), ctypes.byref(mixed)) == g.ERR_UNSUPPORTED
+    acc16 = g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F16, 0, 0, 0, 0)
+    assert lib.gemm_plan_create(ctypes.byref(h), ctypes.byref(acc16)) == g.ERR_UNSUPPORTED
+    f8_f16out = g.PlanDesc(g.E4M3, g.E4M3, g.F16, g.F16, g.F32, 0, 0, 0, 0)
+    assert lib.gemm_plan_create(ctypes.byref(h), ctypes.byref(f8_f16out)) == g.ERR_UNSUPPORTED
+
+
+def test_plan_create_without_gpu_reports_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = g.load()
+    h = ctypes.c_void_p()
+    ok = g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F32, 0, 0, 0, 0)
+    assert lib.gemm_plan_create(ctypes.byref(h), ctypes.byref(ok)) == g.ERR_NO_DEVICE
+    assert h.value is None
+
+
+def test_binding_names_match_c_entry_points():
+    for name in g.EXPORTED:
+        if name == "gemm15_status_string":
+            continue
+        assert callable(getattr(g, name)), name
