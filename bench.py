@@ -1,0 +1,479 @@
+"""GEMM throughput on one GB300 (or N replicas), one JSON line on rank 0.
+
+A step is one call of the hot path: gemm_run (or grouped_gemm_run) on the
+workload's resident device inputs.  Default workload: fp16 4096^3 with
+alpha 1.5, beta 0.5 and a fused ReLU (the second configuration of the target
+list).  The metric is TFLOP/s = 2*M*N*K / time; the L2 is flushed (256 MiB
+write) between timed steps, outside the per-step CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense tensor peak per shape (1 GPU)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm15_api.cu")
+
+
+# ------------------------------------------------------------------ workloads
+
+def workloads():
+    from dense_gemm_15_gb300 import inputs as I
+    w = {
+        "fp16_4096x4096x4096_relu": lambda: [I.config2()],
+        "fp16_1024_uniform": lambda: [I.config1("b")],
+        "fp16_1024_ones": lambda: [I.config1("a")],
+        "fp16_grouped_32": lambda: I.config4(),
+        "e4m3_8192": lambda: [I.config5b()],
+    }
+    for layer in I.LLAMA70B_LAYERS:
+        for m in I.LLAMA70B_TOKENS:
+            w["bf16_llama70b_%s_m%d" % (layer, m)] = (lambda m=m, layer=layer: [I.config3(m, layer)])
+    for (M, N, K) in I.STREAMK_SHAPES:
+        w["fp16_streamk_%dx%dx%d" % (M, N, K)] = (lambda M=M, N=N, K=K: [I.config5a(M, N, K)])
+    return w
+
+
+DEFAULT_WORKLOAD = "fp16_4096x4096x4096_relu"
+
+
+def custom_workload(name):
+    """custom_<f16|bf16|e4m3>_<M>x<N>x<K>[_b<beta>][_relu]: seeded U[-1,1]
+    (N(0,1) for e4m3) operands of any shape, for sweeps and ablations."""
+    from dense_gemm_15_gb300 import inputs as I
+    parts = name.split("_")
+    dtype = parts[1]
+    M, N, K = (int(x) for x in parts[2].split("x"))
+    beta = 0.0
+    relu = False
+    for q in parts[3:]:
+        if q.startswith("b"):
+            beta = float(q[1:])
+        elif q == "relu":
+            relu = True
+    p = I.random_problem(M, N, K, dtype=dtype, beta=beta, relu=relu, alpha=1.0)
+    p.name = name
+    return [p]
+
+
+def get_workload(name):
+    if name.startswith("custom_"):
+        return custom_workload(name)
+    return workloads()[name]()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tensor_peak(dtype, pk, sustained=False):
+    bf16 = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    # nominal dense ratios: fp16 = bf16, fp8 = 2 x bf16
+    return bf16 * (2.0 if dtype == "e4m3" else 1.0)
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_gemm_15_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary,
+    or None when none exists or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(probs):
+    tot = 0
+    for p in probs:
+        ea = 1 if p.a_dtype == "e4m3" else 2
+        tot += p.M * p.K * ea + p.K * p.N * ea + p.M * p.N * 2
+        if p.beta != 0.0:
+            tot += p.M * p.N * 2
+    return tot
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.proc or not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+def cpu_oracle_sample(probs, budget_s=10.0, max_rows=None):
+    """Times the oracle (as it stands) on a bounded row sample of the workload.
+    Returns (flops/s, cores, description, seconds)."""
+    import oracle
+    from dense_gemm_15_gb300 import inputs as I
+    p = max(probs, key=lambda q: q.flops)
+    threads = oracle.default_threads()
+    a, b = I.bits(p.A), I.bits(p.B)
+    c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
+                    relu=p.relu, scale_a=p.scale_a, scale_b=p.scale_b,
+                    a_col_major=p.a_col_major, b_col_major=p.b_col_major,
+                    rows=(0, rows), threads=threads)
+        return time.perf_counter() - t0
+
+    rows = min(p.M, max(1, threads))
+    dt = run(rows)
+    while dt < 0.25 * budget_s and rows < p.M:
+        rows = min(p.M, max(rows + 1, int(rows * min(8.0, 0.5 * budget_s / max(dt, 1e-3)))))
+        if max_rows:
+            rows = min(rows, max_rows)
+        dt = run(rows)
+        if max_rows and rows >= max_rows:
+            break
+    flops = 2.0 * rows * p.N * p.K
+    desc = "rows 0..%d of %s (all N=%d columns, full K=%d)" % (rows, p.name, p.N, p.K)
+    return flops / dt, threads, desc, dt
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def maybe_init_dist(ws, backend):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x, device=None):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x, device=None):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores; each step is the same
+    bounded row sample of the workload, sized so the whole run stays within
+    about two minutes."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from dense_gemm_15_gb300 import inputs as I
+    probs = get_workload(args.workload)
+    per_step = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    _, cores, desc, _ = cpu_oracle_sample(probs, budget_s=per_step)
+    p = max(probs, key=lambda q: q.flops)
+    rows = int(desc.split("..")[1].split()[0])
+    a, b = I.bits(p.A), I.bits(p.B)
+    c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
+
+    def step():
+        oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
+                    relu=p.relu, scale_a=p.scale_a, scale_b=p.scale_b,
+                    a_col_major=p.a_col_major, b_col_major=p.b_col_major,
+                    rows=(0, rows), threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = (time.perf_counter() - t0) / max(1, args.steps)
+    value = 2.0 * rows * p.N * p.K / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": p.M, "N": p.N, "K": p.K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main arm
+
+def run_gpu(args):
+    import torch
+    from dense_gemm_15_gb300 import binding as g
+    from dense_gemm_15_gb300 import inputs as I
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = maybe_init_dist(ws, "nccl")
+    dev = torch.device("cuda", local)
+    probs = get_workload(args.workload)
+    grouped = len(probs) > 1
+    p0 = probs[0]
+    flops = sum(p.flops for p in probs)
+
+    plan = g.Plan(p0.a_dtype, p0.d_dtype, relu=p0.relu)
+    for opt in args.opt or []:
+        k, v = opt.split("=")
+        plan.set(getattr(g, "OPT_" + k.upper()), int(v))
+    dv = []
+    for p in probs:
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = p.C.to(dev) if p.C is not None else None
+        D = torch.empty(p.M, p.N, dtype=I.TORCH_DTYPE[p.d_dtype], device=dev)
+        dv.append((A, B, C, D))
+    scales = None
+    if p0.a_dtype == "e4m3":
+        scales = (torch.tensor([p0.scale_a], device=dev), torch.tensor([p0.scale_b], device=dev))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    table = [dict(M=p.M, N=p.N, K=p.K, A=A, B=B, C=C, D=D) for p, (A, B, C, D) in zip(probs, dv)]
+
+    def step():
+        if grouped:
+            plan.grouped(table, alpha=p0.alpha, beta=p0.beta, stream=stream)
+        else:
+            A, B, C, D = dv[0]
+            plan.run(A, B, C, D, p0.M, p0.N, p0.K, alpha=p0.alpha, beta=p0.beta,
+                     scale_a=scales[0] if scales else None,
+                     scale_b=scales[1] if scales else None, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st = plan.query_error()
+    if st != g.OK:
+        raise RuntimeError("device status after warm-up: " + g.status_string(st))
+    cfg = plan.last_config()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        # give the host a head start so that no step waits for its launch:
+        # every timed step then starts right after the preceding flush
+        torch.cuda._sleep(int(2e6))
+        host = 0.0
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            h0 = time.perf_counter()
+            step()
+            host += time.perf_counter() - h0
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(dist)
+    st = plan.query_error()
+    if st != g.OK:
+        raise RuntimeError("device status after timed steps: " + g.status_string(st))
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_step = sum(ms) / len(ms)
+    ms_step_max = max_over_ranks(dist, ms_step, dev)
+    total_flops = sum_over_ranks(dist, flops, dev)
+    value = total_flops / (ms_step_max * 1e-3) / 1e12
+
+    # end to end through the C ABI with pinned host buffers (single problems)
+    e2e = None
+    if not grouped:
+        hA, hB = p0.A.pin_memory(), p0.B.pin_memory()
+        hC = p0.C.pin_memory() if p0.C is not None else None
+        hD = torch.empty(p0.M, p0.N, dtype=I.TORCH_DTYPE[p0.d_dtype]).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+        for _ in range(2):
+            g.gemm_run_host(plan.handle, hA, hB, hC, hD, p0.M, p0.N, p0.K, p0.alpha, p0.beta,
+                            p0.scale_a, p0.scale_b, stream)
+        barrier(dist)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            s = g.gemm_run_host(plan.handle, hA, hB, hC, hD, p0.M, p0.N, p0.K, p0.alpha,
+                                p0.beta, p0.scale_a, p0.scale_b, stream)
+            if s != g.OK:
+                raise RuntimeError("gemm_run_host: " + g.status_string(s))
+        t_e2e = (time.perf_counter() - t0) / e2e_steps
+        t_e2e = max_over_ranks(dist, t_e2e, dev)
+        h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+        if hC is not None and p0.beta != 0.0:
+            h2d += hC.numel() * hC.element_size()
+        e2e = {"value": total_flops / t_e2e / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hD.numel() * hD.element_size()}
+
+    pk, pk_kind = peaks()
+    peak = tensor_peak(p0.a_dtype, pk)
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                "peak_source": "%s bf16 burst%s" % (pk_kind, " x2 (fp8)" if p0.a_dtype == "e4m3" else ""),
+                "algorithmic_bytes": algorithmic_bytes(probs),
+                "achieved_gbs": algorithmic_bytes(probs) / (ms_step * 1e-3) / 1e9}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        fl_s, cores, desc, secs = cpu_oracle_sample(probs, budget_s=args.cpu_budget)
+        cpu = {"value": fl_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": desc, "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3"}[p0.a_dtype],
+            "data": "synthetic",
+            "config": {"workload": args.workload, "M": p0.M if not grouped else [p.M for p in probs],
+                       "N": p0.N, "K": p0.K, "alpha": p0.alpha, "beta": p0.beta,
+                       "relu": p0.relu, "layout": "row-major A, B, C, D",
+                       "l2": "flushed between steps (256 MiB write, outside the step events)",
+                       "parallelism": "replicas" if ws > 1 else "single",
+                       "kernel": cfg},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * int(cfg.get("launches", 1)),
+            "clocks": clk.summary(),
+            "wall_s_timed_region": wall,
+            "host_us_per_call": 1e6 * host / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--opt", action="append", help="plan option NAME=VALUE (e.g. schedule=1)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--list", action="store_true")
+    args = ap.parse_args(argv)
+    if args.list:
+        print("\n".join(workloads()))
+        return 0
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.workload not in workloads() and not args.workload.startswith("custom_"):
+        ap.error("unknown workload %s (see --list)" % args.workload)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -405,6 +405,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     std::memset(&gp, 0, sizeof(gp));
     if (!operand_maps(plan, p, d.bn, &gp.tmA, &gp.tmB)) return GEMM15_ERR_CUDA;
     if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return GEMM15_ERR_CUDA;
+    gp.D = p.D;
+    gp.ldd = p.ldd;
     gp.M = static_cast<int32_t>(p.M);
     gp.N = static_cast<int32_t>(p.N);
     gp.K = static_cast<int32_t>(p.K);
@@ -717,6 +719,8 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
         e.n_blocks = static_cast<int32_t>(cdiv(p.N, bn));
         e.tile_start = tiles;
         e.has_c = has_c;
+        e.D = p.D;
+        e.ldd = p.ldd;
         e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
                                         : std::min<int32_t>(e.m_blocks, 16);
         const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;

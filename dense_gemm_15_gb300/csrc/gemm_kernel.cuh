@@ -472,16 +472,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         while (ok && sched_next(p, st, w)) {
             const uint32_t ab = n_acc & 1u;
             const uint32_t aph = (n_acc >> 1) & 1u;
-            if (!wait_bar(ctl, accf_bar(ab), aph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
 
             int32_t M = p.M, N = p.N;
             const CUtensorMap* tC = &p.tmC;
             const CUtensorMap* tD = &p.tmD;
             int32_t has_c = p.has_c;
+            OutT* Dptr = static_cast<OutT*>(p.D);
+            int64_t ldd = p.ldd;
             if (p.groups) {
                 const GroupEntry& g = p.groups[w.group];
                 M = g.M;
@@ -489,6 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tC = &g.tmC;
                 tD = &g.tmD;
                 has_c = g.has_c;
+                Dptr = static_cast<OutT*>(g.D);
+                ldd = g.ldd;
                 if (lane == 0 && w.group != last_group) {
                     tensormap_acquire(tC);
                     tensormap_acquire(tD);
@@ -501,6 +500,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool rows_live = row0 < M;
             const int64_t tile_end_unit =
                 (static_cast<int64_t>(w.tile - p.dp_tiles) + 1) * p.k_blocks;
+            const bool to_ws = (w.kind == WK_PEER || w.kind == WK_SPLIT);
+            const bool stage_c = has_c && !to_ws && rows_live;
+            const int nch = min(NCH, (N - n0 + EPI_COLS - 1) / EPI_COLS);
+
+            // C for the first chunk is fetched while the mainloop still runs
+            if (stage_c && lane == 0) {
+                const uint32_t b = n_chunk & 1u;
+                bulk_wait_read<0>();
+                mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
+                tma_load_2d(ebuf0 + b * EPI_BUF_BYTES, tC, c_bar(e, b), n0, row0);
+                c_pending |= 1u << b;
+            }
+
+            if (!wait_bar(ctl, accf_bar(ab), aph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
 
             // stream-K owner: wait until every peer's partial is published
             if (w.kind == WK_OWNER) {
@@ -524,23 +541,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!epi_sync() || *abort_flag) ok = false;
             }
 
-            const bool to_ws = (w.kind == WK_PEER || w.kind == WK_SPLIT);
-            const bool stage_c = has_c && !to_ws && rows_live;
 #pragma unroll 1
-            for (int c = 0; ok && rows_live && c < NCH; ++c) {
+            for (int c = 0; ok && rows_live && c < nch; ++c) {
                 const int32_t col0 = c * EPI_COLS;
-                if (n0 + col0 >= N) break;
                 const uint32_t b = n_chunk & 1u;
                 const uint32_t buf = ebuf0 + b * EPI_BUF_BYTES;
-                if (!to_ws) {
+                if (stage_c) {
+                    // prefetch C of the next chunk into the other buffer once the
+                    // store that last used it has read it
+                    if (c + 1 < nch && lane == 0) {
+                        bulk_wait_read<0>();
+                        mbar_arrive_expect_tx(c_bar(e, b ^ 1u), EPI_BUF_BYTES);
+                        tma_load_2d(ebuf0 + (b ^ 1u) * EPI_BUF_BYTES, tC, c_bar(e, b ^ 1u),
+                                    n0 + col0 + EPI_COLS, row0);
+                        c_pending |= 1u << (b ^ 1u);
+                    }
+                    __syncwarp();
+                } else if (!to_ws) {
                     // the store issued two chunks ago from this buffer must have read it
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();
-                    if (stage_c && lane == 0) {
-                        mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
-                        tma_load_2d(buf, tC, c_bar(e, b), n0 + col0, row0);
-                        c_pending |= 1u << b;
-                    }
                 }
                 uint32_t r[2][32];
                 const uint32_t taddr = tmem_base + lane_base + ab * BN + col0;
@@ -587,16 +607,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     c_phase ^= 1u << b;
                     c_pending &= ~(1u << b);
                 }
-                uint8_t* bufp = smem + (buf - sbase);
+                // The TMA store clips columns only at 16-byte granularity: a last
+                // chunk that ends inside a 16-byte group is written element-wise.
+                const int32_t left = N - (n0 + col0);
+                const bool ragged = left < EPI_COLS && (left & 7) != 0;
+                const int32_t my_row = row0 + lane;
+                OutT* drow = Dptr + static_cast<int64_t>(my_row) * ldd + n0 + col0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane % 8)
-                    uint4* slot = reinterpret_cast<uint4*>(bufp + lane * 128 + ((j ^ (lane & 7)) << 4));
+                    const uint32_t slot = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
                     float o[8];
 #pragma unroll
                     for (int t = 0; t < 8; ++t) o[t] = alpha * v[8 * j + t];
                     if (stage_c) {
-                        const uint4 cv = *slot;
+                        const uint4 cv = ld_shared_v4(slot);
                         const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
@@ -609,16 +634,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int t = 0; t < 8; ++t) o[t] = o[t] > 0.0f ? o[t] : (o[t] != o[t] ? o[t] : 0.0f);
                     }
-                    *slot = make_uint4(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
-                                       pack2<ELEM>(o[4], o[5]), pack2<ELEM>(o[6], o[7]));
+                    if (!ragged) {
+                        st_shared_v4(slot, pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
+                                     pack2<ELEM>(o[4], o[5]), pack2<ELEM>(o[6], o[7]));
+                    } else if (my_row < M) {
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) {
+                            if (8 * j + t < left) {
+                                if constexpr (ELEM == ELEM_F16) drow[8 * j + t] = __float2half_rn(o[t]);
+                                else drow[8 * j + t] = __float2bfloat16_rn(o[t]);
+                            }
+                        }
+                    }
                 }
-                fence_async_shared();
+                if (!ragged) {
+                    fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(tD, buf, n0 + col0, row0);
+                        bulk_commit();
+                    }
+                    ++n_chunk;  // only chunks that stored from their buffer flip it
+                }
                 __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(tD, buf, n0 + col0, row0);
-                    bulk_commit();
-                }
-                ++n_chunk;
             }
             // accumulator fully read: hand the TMEM buffer back to the MMA warp
             tc_fence_before();

@@ -21,11 +21,15 @@ struct alignas(128) GroupEntry {
     CUtensorMap tmA, tmB, tmC, tmD;
     int32_t M, N, K, k_blocks;
     int32_t m_blocks, n_blocks, tile_start, has_c;
-    int32_t raster, pad0, pad1, pad2;
+    int32_t raster, pad0;
+    void* D;                          // for the ragged last column chunk
+    int64_t ldd;
 };
 
 struct GemmParams {
     CUtensorMap tmA, tmB, tmC, tmD;  // dense problem (unused when grouped)
+    void* D;                          // D and its leading dimension (elements), for
+    int64_t ldd;                      // column chunks the TMA store cannot clip exactly
     int32_t M, N, K;
     int32_t k_blocks;                 // ceil(K / BK)
     int32_t m_blocks, n_blocks, tiles;
