@@ -29,7 +29,7 @@ DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3}
 EXPORTED = (
     "gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
     "grouped_gemm_run", "gemm_plan_query_error", "gemm15_status_string",
-    "gemm_plan_set_option", "gemm_plan_last_config",
+    "gemm_plan_set_option", "gemm_plan_last_config", "gemm_run_splitk_noalloc",
 )
 
 
@@ -94,6 +94,9 @@ def load(build_if_missing: bool = True):
         lib.gemm15_status_string.restype = ctypes.c_char_p
         lib.gemm_plan_set_option.argtypes = [vp, st, i64]
         lib.gemm_plan_last_config.argtypes = [vp, ctypes.POINTER(Config)]
+        lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(PlanDesc), vp, i64, vp, i64, vp,
+                                                i64, vp, i64, i64, i64, i64, f32, f32, vp, vp,
+                                                i32, vp, vp]
         for name in EXPORTED:
             if name != "gemm15_status_string":
                 getattr(lib, name).restype = st
@@ -191,6 +194,19 @@ def gemm_plan_last_config(plan):
     cfg = Config()
     _check(load().gemm_plan_last_config(plan, ctypes.byref(cfg)), "gemm_plan_last_config")
     return cfg.as_dict()
+
+
+def gemm_run_splitk_noalloc(a, layout_a, layout_b, layout_cd, relu, A, lda, B, ldb, C, ldc, D,
+                            ldd, M, N, K, alpha=1.0, beta=0.0, scale_a=None, scale_b=None,
+                            splits=1, status=None, stream=None):
+    """Split-K GEMM that allocates no device memory (see include/gemm15.h)."""
+    c = "bf16" if a == "e4m3" else a
+    desc = PlanDesc(DTYPES[a], DTYPES[a], DTYPES[c], DTYPES[c], F32, layout_a, layout_b,
+                    layout_cd, EPI_RELU if relu else EPI_LINEAR)
+    return load().gemm_run_splitk_noalloc(ctypes.byref(desc), _ptr(A), lda, _ptr(B), ldb,
+                                          _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
+                                          _ptr(scale_a), _ptr(scale_b), int(splits),
+                                          _ptr(status), _stream(stream))
 
 
 # ------------------------------------------------------------------ convenience

@@ -194,6 +194,43 @@ typedef struct {
 
 gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out);
 
+/* ---- Split-K GEMM that allocates nothing.  The pages have no counterpart of
+ * this entry point; it exists for callers that cannot call cudaMalloc: code
+ * living inside a host application that owns every byte of device memory (an
+ * inference server or plugin with a fixed budget), and latency-critical loops
+ * where an allocation, which can block and synchronise the device, is not
+ * acceptable.  Plans grow their workspace on demand, so such callers use this
+ * instead.
+ *
+ * Computes the same D = act(alpha * s_a * s_b * (A . B) + beta * C) as
+ * gemm_run_ex, always as split-K: each output tile's K range is cut into
+ * `splits` parts (clamped to the number of K blocks), whose fp32 partial tiles
+ * a second kernel sums in a fixed order.  The partial tiles live in one
+ * file-scope device array of GEMM15_NOALLOC_SCRATCH_BYTES that every GPU which
+ * loads this library holds until the process exits; nothing is allocated per
+ * call.  The arguments are those of gemm_run_ex, with the element types and
+ * layouts taken from `desc` (no plan), plus:
+ *   splits  >= 1; tiles * splits * 128 * tile_n * 4 bytes + 256 must fit in
+ *           GEMM15_NOALLOC_SCRATCH_BYTES (tile_n = 128 if N <= 128, else 256;
+ *           tiles = ceil(M/128) * ceil(N/tile_n)), otherwise the call returns
+ *           GEMM15_ERR_UNSUPPORTED and launches nothing;
+ *   status  optional DEVICE pointer to an int32 that the call clears and the
+ *           kernels set to GEMM15_ERR_TIMEOUT if a bounded wait runs out; NULL
+ *           keeps that word inside the scratch, unreported.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the array and keep the last call's partials, so
+ * calls that overlap on the GPU (other streams, other host threads) race and
+ * give wrong results: serialise them.  Errors as for gemm_run_ex. */
+#define GEMM15_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+gemm15_status_t gemm_run_splitk_noalloc(const gemm15_plan_desc_t* desc, const void* A,
+                                        int64_t lda, const void* B, int64_t ldb, const void* C,
+                                        int64_t ldc, void* D, int64_t ldd, int64_t M, int64_t N,
+                                        int64_t K, float alpha, float beta, const float* scale_a,
+                                        const float* scale_b, int32_t splits, int32_t* status,
+                                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif
