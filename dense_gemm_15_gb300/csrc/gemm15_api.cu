@@ -58,6 +58,7 @@ struct gemm15_plan {
     size_t host_path_cap[3] = {0, 0, 0};
     float* d_scales = nullptr;  // two floats for gemm_run_host
     uint32_t epoch = 0;
+    int pair_clusters = -1;  // resident SM-pair clusters (queried on first use)
     Options opt;
     gemm15_config_t last{};
 };
@@ -194,6 +195,7 @@ gemm15_status_t check_operands(const gemm15_plan* plan, const Prob& p, float bet
 // ------------------------------------------------------------------ planner
 
 struct Decision {
+    int cg = 1;
     int bn = 256;
     int bk = 64;
     int sched = SCHED_DP;
@@ -207,16 +209,36 @@ struct Decision {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-Decision decide(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
+int pair_clusters(gemm15_plan* plan) {
+    if (plan->pair_clusters < 0) plan->pair_clusters = gemm_max_pair_clusters(plan->elem);
+    return plan->pair_clusters;
+}
+
+// Picks the tile shape, schedule and grid for one problem.
+//   - SM-pair 256 x 256 tiles (cta_group::2) when there is at least one full
+//     wave of them: they halve each SM's share of B traffic;
+//   - data-parallel when the last wave is at least 90% full, else stream-K
+//     over the tail waves (all tiles when there is less than one wave), or
+//     split-K with a separate reduction when stream-K would split one tile
+//     over more than 3 units.
+Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     Decision d;
     const Options& o = plan->opt;
     d.bk = plan->elem == ELEM_E4M3 ? 128 : 64;
     d.bn = o.tile_n ? o.tile_n : (N <= 128 ? 128 : 256);
-    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M));
+    const int G1 = o.grid > 0 ? std::min(o.grid, plan->num_sms) : plan->num_sms;
+    int cg = 1;
+    if (d.bn == 256 && o.cta_group != 1) {
+        const int clusters = std::min(pair_clusters(plan), G1 / 2);
+        const int64_t tiles2 = cdiv(M, 2 * TILE_M) * cdiv(N, 256);
+        if (clusters > 0 && (o.cta_group == 2 || (M >= 512 && tiles2 >= clusters))) cg = 2;
+    }
+    d.cg = cg;
+    const int G = cg == 2 ? std::min(pair_clusters(plan), G1 / 2) : G1;  // scheduling units
+    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M * cg));
     d.n_blocks = static_cast<int32_t>(cdiv(N, d.bn));
     d.tiles = d.m_blocks * d.n_blocks;
     d.k_blocks = static_cast<int32_t>(cdiv(K, d.bk));
-    const int G = o.grid > 0 ? std::min(o.grid, plan->num_sms) : plan->num_sms;
 
     int sched = o.schedule;
     if (sched == 0) {
@@ -231,23 +253,27 @@ Decision decide(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
         }
     }
     d.sched = sched;
-    d.raster = o.raster > 0 ? std::min<int32_t>(o.raster, d.m_blocks) : std::min<int32_t>(d.m_blocks, 16);
+    d.raster = o.raster > 0 ? std::min<int32_t>(o.raster, d.m_blocks)
+                            : std::min<int32_t>(d.m_blocks, cg == 2 ? 8 : 16);
+    const size_t half_tile = static_cast<size_t>(TILE_M) * d.bn * sizeof(float);
+    int units = 1;
     if (sched == SCHED_DP) {
-        d.grid = static_cast<int>(std::min<int64_t>(G, d.tiles));
+        units = static_cast<int>(std::min<int64_t>(G, d.tiles));
     } else if (sched == SCHED_SK) {
         d.dp_tiles = d.tiles >= 2 * G ? (d.tiles / G - 1) * G : 0;
         d.sk_units = static_cast<int64_t>(d.tiles - d.dp_tiles) * d.k_blocks;
-        d.grid = static_cast<int>(std::min<int64_t>(G, d.sk_units));
-        d.ws_bytes = static_cast<size_t>(d.grid) * TILE_M * d.bn * sizeof(float);
-        d.flags = d.grid;
+        units = static_cast<int>(std::min<int64_t>(G, d.sk_units));
+        d.ws_bytes = static_cast<size_t>(units) * cg * half_tile;
+        d.flags = units * cg;
     } else {
         int splits = o.splits > 0 ? o.splits : std::max(1, G / std::max<int32_t>(d.tiles, 1));
         splits = static_cast<int>(std::min<int64_t>(splits, d.k_blocks));
         splits = std::max(splits, 1);
         d.splits = splits;
-        d.grid = static_cast<int>(std::min<int64_t>(G, static_cast<int64_t>(d.tiles) * splits));
-        d.ws_bytes = static_cast<size_t>(d.tiles) * splits * TILE_M * d.bn * sizeof(float);
+        units = static_cast<int>(std::min<int64_t>(G, static_cast<int64_t>(d.tiles) * splits));
+        d.ws_bytes = static_cast<size_t>(d.tiles) * cg * splits * half_tile;
     }
+    d.grid = units * cg;
     return d;
 }
 
@@ -279,7 +305,12 @@ gemm15_status_t ensure_ws(gemm15_plan* plan, size_t bytes, int flags) {
     return GEMM15_OK;
 }
 
-cudaError_t launch_kernel(int elem, int bn, const GemmParams& gp, int grid, cudaStream_t s) {
+cudaError_t launch_kernel(int elem, int bn, int cg, const GemmParams& gp, int grid, cudaStream_t s) {
+    if (cg == 2) {
+        if (elem == ELEM_F16) return launch_gemm<ELEM_F16, 256, 2>(gp, grid, s);
+        if (elem == ELEM_BF16) return launch_gemm<ELEM_BF16, 256, 2>(gp, grid, s);
+        return launch_gemm<ELEM_E4M3, 256, 2>(gp, grid, s);
+    }
     if (elem == ELEM_F16) return bn == 128 ? launch_gemm<ELEM_F16, 128>(gp, grid, s) : launch_gemm<ELEM_F16, 256>(gp, grid, s);
     if (elem == ELEM_BF16) return bn == 128 ? launch_gemm<ELEM_BF16, 128>(gp, grid, s) : launch_gemm<ELEM_BF16, 256>(gp, grid, s);
     return bn == 128 ? launch_gemm<ELEM_E4M3, 128>(gp, grid, s) : launch_gemm<ELEM_E4M3, 256>(gp, grid, s);
@@ -292,7 +323,8 @@ cudaError_t launch_reduce_kernel(int out_elem, const ReduceParams& rp, cudaStrea
 }
 
 // Fills the operand-layout part of the kernel parameters.
-void fill_layout(const gemm15_plan* plan, GemmParams& gp, bool a_kmajor, bool b_kmajor, int bn) {
+void fill_layout(const gemm15_plan* plan, GemmParams& gp, bool a_kmajor, bool b_kmajor, int bn,
+                 int cg = 1) {
     const bool f8 = plan->elem == ELEM_E4M3;
     const int es = f8 ? 1 : 2;
     const int bk = 128 / es;
@@ -320,11 +352,12 @@ void fill_layout(const gemm15_plan* plan, GemmParams& gp, bool a_kmajor, bool b_
     idesc |= (a_kmajor ? 0u : 1u) << 15;   // A MN-major
     idesc |= (b_kmajor ? 0u : 1u) << 16;   // B MN-major
     idesc |= static_cast<uint32_t>(bn >> 3) << 17;
-    idesc |= static_cast<uint32_t>(TILE_M >> 4) << 24;
+    idesc |= static_cast<uint32_t>((TILE_M * cg) >> 4) << 24;  // M = 128 or 256 (SM pair)
     gp.idesc = idesc;
 }
 
-bool operand_maps(const gemm15_plan* plan, const Prob& p, int bn, CUtensorMap* tA, CUtensorMap* tB) {
+// bn_box: columns of B one CTA stages (the tile width, or half of it for SM pairs).
+bool operand_maps(const gemm15_plan* plan, const Prob& p, int bn_box, CUtensorMap* tA, CUtensorMap* tB) {
     const bool f8 = plan->elem == ELEM_E4M3;
     const int es = f8 ? 1 : 2;
     const uint32_t bk = 128 / es, w = 128 / es;
@@ -334,7 +367,7 @@ bool operand_maps(const gemm15_plan* plan, const Prob& p, int bn, CUtensorMap* t
     else
         ok &= make_tmap(tA, plan->elem, p.A, p.M, p.K, p.lda * es, w, bk);
     if (p.b_kmajor)
-        ok &= make_tmap(tB, plan->elem, p.B, p.K, p.N, p.ldb * es, bk, bn);
+        ok &= make_tmap(tB, plan->elem, p.B, p.K, p.N, p.ldb * es, bk, bn_box);
     else
         ok &= make_tmap(tB, plan->elem, p.B, p.N, p.K, p.ldb * es, w, bk);
     return ok;
@@ -349,11 +382,11 @@ bool output_maps(const gemm15_plan* plan, const Prob& p, bool has_c, CUtensorMap
 
 void record_config(gemm15_plan* plan, const Decision& d, int launches) {
     gemm15_config_t& c = plan->last;
-    c.cta_group = 1;
-    c.tile_m = TILE_M;
+    c.cta_group = d.cg;
+    c.tile_m = TILE_M * d.cg;
     c.tile_n = d.bn;
     c.tile_k = d.bk;
-    c.stages = gemm_stages(plan->elem, d.bn);
+    c.stages = gemm_stages(plan->elem, d.bn, d.cg);
     c.schedule = d.sched;
     c.grid = d.grid;
     c.tiles = d.tiles;
@@ -403,7 +436,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
 
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
-    if (!operand_maps(plan, p, d.bn, &gp.tmA, &gp.tmB)) return GEMM15_ERR_CUDA;
+    if (!operand_maps(plan, p, d.bn / d.cg, &gp.tmA, &gp.tmB)) return GEMM15_ERR_CUDA;
     if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return GEMM15_ERR_CUDA;
     gp.D = p.D;
     gp.ldd = p.ldd;
@@ -425,7 +458,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.scale_a = scale_a;
     gp.scale_b = scale_b;
     gp.relu = relu;
-    fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn);
+    fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.ws = plan->d_ws;
     gp.flags = plan->d_flags;
     gp.status = plan->d_status;
@@ -434,7 +467,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.fault_skip_flag = plan->opt.fault_skip_flag;
     gp.groups = nullptr;
     gp.num_groups = 0;
-    if (launch_kernel(plan->elem, d.bn, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    if (launch_kernel(plan->elem, d.bn, d.cg, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
     int launches = 1;
     if (d.sched == SCHED_SPLIT) {
         ReduceParams rp{};
@@ -753,7 +786,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     gp.groups = plan->d_groups;
     gp.num_groups = ng;
     const int grid = std::min(G, tiles);
-    if (launch_kernel(plan->elem, bn, gp, grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    if (launch_kernel(plan->elem, bn, 1, gp, grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
     Decision d;
     d.bn = bn;
     d.bk = bk;
@@ -792,7 +825,7 @@ gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option,
             o.splits = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_CTA_GROUP:
-            if (v != 0 && v != 1) return v == 2 ? GEMM15_ERR_UNSUPPORTED : GEMM15_ERR_INVALID_ARG;
+            if (v != 0 && v != 1 && v != 2) return GEMM15_ERR_INVALID_ARG;
             o.cta_group = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_TILE_N:

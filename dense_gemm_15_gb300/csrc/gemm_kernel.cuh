@@ -10,7 +10,7 @@
 // functionality" of the CUTLASS README; this kernel is our own design for
 // Blackwell (tcgen05 / TMEM / TMA), not the pre-SM90 kernels the pages use.
 //
-// One CTA per SM, 192 threads:
+// One CTA per SM (CG = 1) or one SM pair per tile (CG = 2), 192 threads:
 //   warp 0      TMA producer: A and B tiles into a STAGES-deep shared ring
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..5  epilogue: TMEM -> registers -> alpha/beta/C/ReLU -> 16-bit ->
@@ -32,7 +32,11 @@
 
 namespace g15 {
 
-template <int ELEM, int BN>
+// CG = 1: one CTA computes a 128 x BN tile.  CG = 2: an SM pair (a cluster of
+// two CTAs) computes a 256 x BN tile with tcgen05 cta_group::2 -- each CTA
+// stages its own 128 rows of A and its own BN/2 columns of B, and holds its
+// 128 rows of the accumulator in its own TMEM.
+template <int ELEM, int BN, int CG = 1>
 struct Traits {
     static constexpr bool F8 = (ELEM == ELEM_E4M3);
     static constexpr int ESIZE = F8 ? 1 : 2;           // bytes per A/B element
@@ -40,9 +44,10 @@ struct Traits {
     static constexpr int UMMA_K = 32 / ESIZE;          // K per tcgen05.mma
     static constexpr int KSTEPS = BK / UMMA_K;         // MMAs per k-block (4)
     static constexpr int A_STAGE = TILE_M * 128;       // 16 KB
-    static constexpr int B_STAGE = BN * 128;           // 16 or 32 KB
+    static constexpr int B_COLS = BN / CG;             // B columns staged by one CTA
+    static constexpr int B_STAGE = B_COLS * 128;       // 16 or 32 KB
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STAGES = (STAGE_BYTES == 48 * 1024) ? 4 : 6;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // 32 KB
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -150,9 +155,14 @@ struct Work {
     int32_t m_blk, n_blk;
     int32_t kb0, kb1;
     int32_t kind;      // WK_*
-    int32_t slot;      // workspace slot for partial tiles
+    int32_t slot;      // workspace slot for partial tiles (128-row halves)
 };
 enum : int32_t { WK_FULL = 0, WK_PEER = 1, WK_OWNER = 2, WK_SPLIT = 3 };
+
+// Scheduling works on "units": one CTA (CG = 1) or one SM pair (CG = 2).
+struct Unit {
+    int32_t id, count, rank, cg;
+};
 
 struct SchedState {
     int32_t i;          // data-parallel / split item counter
@@ -160,8 +170,8 @@ struct SchedState {
     int64_t u, u_end;   // stream-K unit cursor
 };
 
-__device__ __forceinline__ int64_t sk_begin(const GemmParams& p, int64_t cta) {
-    return (p.sk_units * cta) / gridDim.x;
+__device__ __forceinline__ int64_t sk_begin(const GemmParams& p, const Unit& un, int64_t unit) {
+    return (p.sk_units * unit) / un.count;
 }
 
 __device__ __forceinline__ void raster_coords(int32_t tile, int32_t m_blocks, int32_t n_blocks,
@@ -175,14 +185,14 @@ __device__ __forceinline__ void raster_coords(int32_t tile, int32_t m_blocks, in
     nb = local / rows;
 }
 
-__device__ __forceinline__ void sched_init(const GemmParams& p, SchedState& s) {
+__device__ __forceinline__ void sched_init(const GemmParams& p, const Unit& un, SchedState& s) {
     s.i = 0;
     s.phase = 0;
     s.u = 0;
     s.u_end = 0;
     if (p.sched == SCHED_SK) {
-        s.u = sk_begin(p, blockIdx.x);
-        s.u_end = sk_begin(p, blockIdx.x + 1);
+        s.u = sk_begin(p, un, un.id);
+        s.u_end = sk_begin(p, un, un.id + 1);
     }
 }
 
@@ -205,10 +215,11 @@ __device__ __forceinline__ void fill_coords(const GemmParams& p, Work& w) {
     }
 }
 
-__device__ __forceinline__ bool sched_next(const GemmParams& p, SchedState& s, Work& w) {
-    const int32_t G = gridDim.x;
+__device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, SchedState& s,
+                                           Work& w) {
+    const int32_t G = un.count;
     if (p.sched == SCHED_SPLIT) {
-        const int32_t j = blockIdx.x + s.i * G;
+        const int32_t j = un.id + s.i * G;
         if (j >= p.tiles * p.splits) return false;
         ++s.i;
         w.tile = j / p.splits;
@@ -217,12 +228,13 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, SchedState& s, W
         w.kb0 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * sp) / p.splits);
         w.kb1 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (sp + 1)) / p.splits);
         w.kind = WK_SPLIT;
-        w.slot = (w.m_blk * p.n_blocks + w.n_blk) * p.splits + sp;
+        // slots are indexed by 128-row block so the reduction sees one layout
+        w.slot = ((w.m_blk * un.cg + un.rank) * p.n_blocks + w.n_blk) * p.splits + sp;
         return true;
     }
     const int32_t dp_limit = (p.sched == SCHED_SK) ? p.dp_tiles : p.tiles;
     if (s.phase == 0) {
-        const int32_t t = blockIdx.x + s.i * G;
+        const int32_t t = un.id + s.i * G;
         if (t < dp_limit) {
             ++s.i;
             w.tile = t;
@@ -255,7 +267,7 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, SchedState& s, W
         } else {
             w.kind = WK_PEER;
         }
-        w.slot = blockIdx.x;
+        w.slot = un.id * un.cg + un.rank;
         s.u = end;
         return true;
     }
@@ -264,12 +276,13 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, SchedState& s, W
 
 // ------------------------------------------------------------------ the kernel
 
-template <int ELEM, int BN>
+template <int ELEM, int BN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-    using TR = Traits<ELEM, BN>;
+    using TR = Traits<ELEM, BN, CG>;
     using OutT = typename OutType<ELEM>::T;
     constexpr int STAGES = TR::STAGES;
+    constexpr int TILE_ROWS = TILE_M * CG;  // output rows per tile
 
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled TMA / UMMA tiles
@@ -294,6 +307,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     Ctl ctl{abort_flag, p.status, p.timeout_ns};
+    Unit un;
+    un.cg = CG;
+    un.rank = CG == 2 ? static_cast<int32_t>(cluster_ctarank()) : 0;
+    un.id = static_cast<int32_t>(blockIdx.x) / CG;
+    un.count = static_cast<int32_t>(gridDim.x) / CG;
+    const bool leader = un.rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -302,7 +321,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), EPI_WARPS);
+            mbar_init(acce_bar(b), EPI_WARPS * CG);  // both CTAs' epilogues release
         }
         for (int q = 0; q < EPI_WARPS; ++q) {
             mbar_init(c_bar(q, 0), 1);
@@ -314,11 +333,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_u32(misc), TR::TMEM_COLS);
-        tmem_relinquish<1>();
+        // with CG = 2 one warp of each CTA of the pair allocates collectively
+        tmem_alloc<CG>(smem_u32(misc), TR::TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -330,12 +351,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_prefetch_desc(&p.tmB);
             }
             SchedState st;
-            sched_init(p, st);
+            sched_init(p, un, st);
             Work w;
             uint32_t n_issued = 0;
             bool ok = true;
             int last_group = -1;
-            while (ok && sched_next(p, st, w)) {
+            while (ok && sched_next(p, un, st, w)) {
                 const CUtensorMap* tA = &p.tmA;
                 const CUtensorMap* tB = &p.tmB;
                 if (p.groups) {
@@ -347,8 +368,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         last_group = w.group;
                     }
                 }
-                const int32_t m0 = w.m_blk * TILE_M;
-                const int32_t n0 = w.n_blk * BN;
+                const int32_t m0 = w.m_blk * TILE_ROWS + un.rank * TILE_M;
+                const int32_t n0 = w.n_blk * BN + un.rank * TR::B_COLS;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     const int s = n_issued % STAGES;
                     const uint32_t ph = (n_issued / STAGES) & 1u;
@@ -356,27 +377,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), TR::STAGE_BYTES);
+                    // CG = 2: both CTAs' copies complete on the leader's barrier,
+                    // which the leader arms for the pair's bytes
+                    uint32_t fb = full_bar(s);
+                    if constexpr (CG == 2) fb = map_cluster(fb, 0);
+                    if (leader) mbar_arrive_expect_tx(full_bar(s), CG * TR::STAGE_BYTES);
                     const uint32_t dA = sA + s * TR::A_STAGE;
                     const uint32_t dB = sB + s * TR::B_STAGE;
                     const int32_t k0 = kb * TR::BK;
+                    auto load = [&](uint32_t dst, const CUtensorMap* t, int32_t x, int32_t y) {
+                        if constexpr (CG == 2) tma_load_2d_pair(dst, t, fb, x, y);
+                        else tma_load_2d(dst, t, fb, x, y);
+                    };
                     if (p.a_kmajor) {
-                        tma_load_2d(dA, tA, full_bar(s), k0, m0);
+                        load(dA, tA, k0, m0);
                     } else {
                         constexpr int AW = 128 / TR::ESIZE;  // M elements per 128-byte row
 #pragma unroll
-                        for (int j = 0; j < TILE_M / AW; ++j)
-                            tma_load_2d(dA + j * AW * 128, tA, full_bar(s), m0 + j * AW, k0);
+                        for (int j = 0; j < TILE_M / AW; ++j) load(dA + j * AW * 128, tA, m0 + j * AW, k0);
                     }
                     if (p.b_kmajor) {
-                        tma_load_2d(dB, tB, full_bar(s), k0, n0);
+                        load(dB, tB, k0, n0);
                     } else {
                         constexpr int BW = 128 / TR::ESIZE;  // N elements per 128-byte row
 #pragma unroll
-                        for (int j = 0; j < BN / BW; ++j)
-                            tma_load_2d(dB + j * BW * 128, tB, full_bar(s), n0 + j * BW, k0);
+                        for (int j = 0; j < TR::B_COLS / BW; ++j) load(dB + j * BW * 128, tB, n0 + j * BW, k0);
                     }
                     ++n_issued;
+                }
+            }
+            if (ok && !*abort_flag) {
+                // producer tail: the MMA warp's releases of the last stages land in
+                // this CTA's shared memory (for CG = 2, from the leader); wait for
+                // them so that none arrives after the CTA has exited
+                const uint32_t last = n_issued < STAGES ? n_issued : STAGES;
+                for (uint32_t i = 0; i < last; ++i) {
+                    const uint32_t n = n_issued - 1 - i;
+                    if (!wait_bar(ctl, empty_bar(n % STAGES), (n / STAGES) & 1u)) break;
                 }
             }
             if (!ok || *abort_flag) {
@@ -384,21 +421,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t outstanding = n_issued < STAGES ? n_issued : STAGES;
                 for (uint32_t i = 0; i < outstanding; ++i) {
                     const uint32_t n = n_issued - 1 - i;
-                    drain_bar(full_bar(n % STAGES), (n / STAGES) & 1u, 200000000ull);
+                    if (CG == 1 || leader) drain_bar(full_bar(n % STAGES), (n / STAGES) & 1u, 200000000ull);
+                }
+                if (CG == 2 && !leader) {
+                    // the peer's copies complete on the leader: give them time to land
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 2000000ull) {
+                    }
                 }
             }
         }
     } else if (warp == 1) {
-        // ============================ MMA issuer (one thread)
-        if (lane == 0) {
+        // ============================ MMA issuer (one thread of the leader CTA)
+        if (lane == 0 && leader) {
             const uint64_t adesc0 = sdesc_base(p.a_lbo, p.a_sbo);
             const uint64_t bdesc0 = sdesc_base(p.b_lbo, p.b_sbo);
             SchedState st;
-            sched_init(p, st);
+            sched_init(p, un, st);
             Work w;
             uint32_t n_used = 0, n_acc = 0;
             bool ok = true, issued = false;
-            while (ok && sched_next(p, st, w)) {
+            // completion signals go to the same barrier in every CTA of the pair
+            auto commit = [&](uint32_t bar) {
+                if constexpr (CG == 1) {
+                    umma_commit(bar);
+                } else {
+                    umma_commit_pair(bar);
+                    umma_commit_pair(map_cluster(bar, 1));
+                }
+            };
+            while (ok && sched_next(p, un, st, w)) {
                 const uint32_t ab = n_acc & 1u;
                 const uint32_t aph = (n_acc >> 1) & 1u;
                 if (!wait_bar(ctl, acce_bar(ab), aph ^ 1u)) {
@@ -419,20 +471,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t b_addr = sB + s * TR::B_STAGE;
 #pragma unroll
                     for (int k = 0; k < TR::KSTEPS; ++k) {
-                        umma<1, TR::F8>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
-                                        sdesc_at(bdesc0, b_addr + k * p.b_kstep), p.idesc,
-                                        (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        umma<CG, TR::F8>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
+                                         sdesc_at(bdesc0, b_addr + k * p.b_kstep), p.idesc,
+                                         (kb > w.kb0 || k > 0) ? 1u : 0u);
                     }
                     issued = true;
-                    umma_commit(empty_bar(s));
+                    commit(empty_bar(s));
                     ++n_used;
                 }
                 if (!ok) break;
-                umma_commit(accf_bar(ab));
+                commit(accf_bar(ab));
                 ++n_acc;
             }
             if (issued && (!ok || *abort_flag)) {
-                umma_commit(drain);
+                if constexpr (CG == 1) umma_commit(drain);
+                else umma_commit_pair(drain);
                 drain_bar(drain, 0, 200000000ull);
             }
         }
@@ -461,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
 
         SchedState st;
-        sched_init(p, st);
+        sched_init(p, un, st);
         Work w;
         uint32_t n_acc = 0;
         uint32_t n_chunk = 0;      // chunks staged by this warp (buffer parity)
@@ -469,7 +522,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t c_pending = 0;    // C loads issued and not yet waited for
         int last_group = -1;
         bool ok = true;
-        while (ok && sched_next(p, st, w)) {
+        const int32_t my_slot_unit = un.id * CG + un.rank;
+        while (ok && sched_next(p, un, st, w)) {
             const uint32_t ab = n_acc & 1u;
             const uint32_t aph = (n_acc >> 1) & 1u;
 
@@ -494,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 last_group = w.group;
             }
-            const int32_t m0 = w.m_blk * TILE_M;
+            const int32_t m0 = w.m_blk * TILE_ROWS + un.rank * TILE_M;
             const int32_t n0 = w.n_blk * BN;
             const int32_t row0 = m0 + q * 32;      // first row of this warp
             const bool rows_live = row0 < M;
@@ -519,14 +573,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
 
-            // stream-K owner: wait until every peer's partial is published
+            // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
                 if (threadIdx.x == 64) {
-                    for (int64_t b = blockIdx.x + 1; b < gridDim.x && sk_begin(p, b) < tile_end_unit; ++b) {
-                        if (sk_begin(p, b) == sk_begin(p, b + 1)) continue;
+                    for (int64_t b = un.id + 1; b < un.count && sk_begin(p, un, b) < tile_end_unit; ++b) {
+                        if (sk_begin(p, un, b) == sk_begin(p, un, b + 1)) continue;
+                        const uint32_t* flag = p.flags + b * CG + un.rank;
                         const uint64_t t0 = globaltimer_ns();
                         uint32_t it = 0;
-                        while (ld_acquire_gpu(p.flags + b) != p.epoch) {
+                        while (ld_acquire_gpu(flag) != p.epoch) {
                             if ((++it & 15u) == 0) {
                                 if (*abort_flag) break;
                                 if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -574,11 +629,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     v[32 + i] = __uint_as_float(r[1][i]);
                 }
                 if (w.kind == WK_OWNER) {
-                    // add the peers' partial tiles in CTA order (deterministic)
-                    for (int64_t pb = blockIdx.x + 1; pb < gridDim.x && sk_begin(p, pb) < tile_end_unit; ++pb) {
-                        if (sk_begin(p, pb) == sk_begin(p, pb + 1)) continue;
+                    // add the peer units' partial tiles in unit order (deterministic)
+                    for (int64_t pb = un.id + 1; pb < un.count && sk_begin(p, un, pb) < tile_end_unit; ++pb) {
+                        if (sk_begin(p, un, pb) == sk_begin(p, un, pb + 1)) continue;
                         const float4* src = reinterpret_cast<const float4*>(
-                            p.ws + static_cast<size_t>(pb) * TILE_M * BN +
+                            p.ws + static_cast<size_t>(pb * CG + un.rank) * TILE_M * BN +
                             static_cast<size_t>(q * 32 + lane) * BN + col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -659,9 +714,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
             }
             // accumulator fully read: hand the TMEM buffer back to the MMA warp
+            // (the leader's barrier counts the epilogue warps of both CTAs)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(ab));
+            if (lane == 0) {
+                if constexpr (CG == 1) mbar_arrive(acce_bar(ab));
+                else mbar_arrive_cluster(acce_bar(ab), 0);
+            }
             ++n_acc;
 
             if (w.kind == WK_PEER) {
@@ -669,8 +728,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __threadfence();
                 const bool synced = epi_sync();
                 if (threadIdx.x == 64 && ok && synced && !*abort_flag &&
-                    p.fault_skip_flag != static_cast<int32_t>(blockIdx.x))
-                    st_release_gpu(p.flags + blockIdx.x, p.epoch);
+                    p.fault_skip_flag != un.id)
+                    st_release_gpu(p.flags + my_slot_unit, p.epoch);
                 if (!synced) ok = false;
             }
             if (*abort_flag) ok = false;
@@ -686,9 +745,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    // the pair's MMAs read both CTAs' shared memory and write both TMEMs
+    if constexpr (CG == 2) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<1>(tmem_base, TR::TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, TR::TMEM_COLS);
     }
 }
 

@@ -8,16 +8,21 @@
 
 namespace g15 {
 
-// Persistent tcgen05 GEMM, one-SM tiles of 128 x BN (BN = 128 or 256).
-template <int ELEM, int BN>
+// Persistent tcgen05 GEMM: one-SM tiles of 128 x BN (CG = 1, BN = 128 or 256)
+// or SM-pair tiles of 256 x BN (CG = 2, clusters of two CTAs; grid even).
+template <int ELEM, int BN, int CG = 1>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+
+// Largest number of SM-pair clusters of the CG = 2 kernel resident at once
+// (0 if the query fails).
+int gemm_max_pair_clusters(int elem);
 
 // Split-K reduction / K == 0 epilogue (ELEM selects the 16-bit C/D type).
 template <int ELEM>
 cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream);
 
 // Shared-memory bytes and pipeline depth of a GEMM instantiation.
-int gemm_smem_bytes(int elem, int bn);
-int gemm_stages(int elem, int bn);
+int gemm_smem_bytes(int elem, int bn, int cg);
+int gemm_stages(int elem, int bn, int cg);
 
 }  // namespace g15

@@ -6,21 +6,65 @@
 
 namespace g15 {
 
-template <int ELEM, int BN>
+template <int ELEM, int BN, int CG>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
-    using TR = Traits<ELEM, BN>;
+    using TR = Traits<ELEM, BN, CG>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        err = cudaFuncSetAttribute(gemm_tc_kernel<ELEM, BN>,
+        err = cudaFuncSetAttribute(gemm_tc_kernel<ELEM, BN, CG>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, TR::SMEM_BYTES);
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    gemm_tc_kernel<ELEM, BN><<<grid, NUM_THREADS, TR::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    if constexpr (CG == 1) {
+        gemm_tc_kernel<ELEM, BN, 1><<<grid, NUM_THREADS, TR::SMEM_BYTES, stream>>>(p);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = TR::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<ELEM, BN, 2>, p);
+    }
+}
+
+template <int ELEM>
+int max_pair_clusters() {
+    using TR = Traits<ELEM, 256, 2>;
+    if (cudaFuncSetAttribute(gemm_tc_kernel<ELEM, 256, 2>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TR::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = TR::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<ELEM, 256, 2>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 template <int ELEM>

@@ -288,3 +288,38 @@ def test_nan_padding_never_leaks(a_col, b_col):
     assert torch.all(Dc[:, N:] == 7.0), "columns beyond N were written"
     assert torch.isfinite(Dc[:, :N]).all(), "padding leaked into D"
     assert_matches_oracle(prob, inputs.bits(Dc[:, :N].contiguous()))
+
+
+# ------------------------------------------------------------------ SM-pair tiles
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("shape", [(512, 512, 1024), (300, 784, 2064), (1000, 272, 528)])
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "e4m3"])
+def test_sm_pair_tiles(sched, shape, dtype):
+    """256 x 256 tiles computed by an SM pair (tcgen05 cta_group::2)."""
+    M, N, K = shape
+    prob = inputs.random_problem(M, N, K, dtype=dtype, beta=0.5, alpha=1.5, relu=True)
+    plan = plan_for(prob, schedule=sched, cta_group=2)
+    d = run_gpu(plan, prob)
+    cfg = plan.last_config()
+    assert cfg["cta_group"] == 2 and cfg["tile_m"] == 256 and cfg["schedule"] == sched
+    assert_matches_oracle(prob, d)
+
+
+@pytest.mark.parametrize("a_col,b_col", [(True, False), (False, True), (True, True)])
+def test_sm_pair_tiles_layouts(a_col, b_col):
+    prob = inputs.random_problem(640, 512, 768, beta=1.0, a_col_major=a_col, b_col_major=b_col)
+    plan = plan_for(prob, cta_group=2)
+    assert_matches_oracle(prob, run_gpu(plan, prob))
+    assert plan.last_config()["cta_group"] == 2
+
+
+def test_sm_pair_tiles_chosen_for_large_problems_and_deterministic():
+    prob = inputs.random_problem(4096, 4096, 2048, dtype="bf16")
+    plan = plan_for(prob)
+    d1 = run_gpu(plan, prob)
+    assert plan.last_config()["cta_group"] == 2
+    d2 = run_gpu(plan, prob)
+    assert np.array_equal(d1, d2)
+    for rows in sample_rows(prob.M, count=3, span=16):
+        assert_matches_oracle(prob, d1, rows=rows)
