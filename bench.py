@@ -54,20 +54,25 @@ DEFAULT_WORKLOAD = "fp16_4096x4096x4096_relu"
 
 
 def custom_workload(name):
-    """custom_<f16|bf16|e4m3>_<M>x<N>x<K>[_b<beta>][_relu]: seeded U[-1,1]
+    """custom_<f16|bf16|e4m3>_<M>x<N>x<K>[_b<beta>][_relu][_acol][_bcol]: seeded U[-1,1]
     (N(0,1) for e4m3) operands of any shape, for sweeps and ablations."""
     from dense_gemm_15_gb300 import inputs as I
     parts = name.split("_")
     dtype = parts[1]
     M, N, K = (int(x) for x in parts[2].split("x"))
     beta = 0.0
-    relu = False
+    relu = acol = bcol = False
     for q in parts[3:]:
-        if q.startswith("b"):
-            beta = float(q[1:])
-        elif q == "relu":
+        if q == "relu":
             relu = True
-    p = I.random_problem(M, N, K, dtype=dtype, beta=beta, relu=relu, alpha=1.0)
+        elif q == "acol":
+            acol = True
+        elif q == "bcol":
+            bcol = True
+        elif q.startswith("b"):
+            beta = float(q[1:])
+    p = I.random_problem(M, N, K, dtype=dtype, beta=beta, relu=relu, alpha=1.0,
+                         a_col_major=acol, b_col_major=bcol)
     p.name = name
     return [p]
 
@@ -319,7 +324,9 @@ def run_gpu(args):
     p0 = probs[0]
     flops = sum(p.flops for p in probs)
 
-    plan = g.Plan(p0.a_dtype, p0.d_dtype, relu=p0.relu)
+    plan = g.Plan(p0.a_dtype, p0.d_dtype, relu=p0.relu,
+                  layout_a=g.COL_MAJOR if p0.a_col_major else g.ROW_MAJOR,
+                  layout_b=g.COL_MAJOR if p0.b_col_major else g.ROW_MAJOR)
     for opt in args.opt or []:
         k, v = opt.split("=")
         plan.set(getattr(g, "OPT_" + k.upper()), int(v))
@@ -334,6 +341,15 @@ def run_gpu(args):
         scales = (torch.tensor([p0.scale_a], device=dev), torch.tensor([p0.scale_b], device=dev))
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = (torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+                if args.flush == "write+read" else None)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def l2_flush():
+        flush.zero_()
+        if flush_rd is not None:
+            # leave the L2 holding clean lines: the written ones are evicted here
+            torch.sum(flush_rd, dim=0, out=flush_sink)
     table = [dict(M=p.M, N=p.N, K=p.K, A=A, B=B, C=C, D=D) for p, (A, B, C, D) in zip(probs, dv)]
 
     def step():
@@ -346,7 +362,7 @@ def run_gpu(args):
                      scale_b=scales[1] if scales else None, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush()
         step()
     torch.cuda.synchronize(dev)
     st = plan.query_error()
@@ -365,7 +381,7 @@ def run_gpu(args):
         torch.cuda._sleep(int(2e6))
         host = 0.0
         for i in range(args.steps):
-            flush.zero_()
+            l2_flush()
             starts[i].record(stream)
             h0 = time.perf_counter()
             step()
@@ -377,6 +393,15 @@ def run_gpu(args):
     st = plan.query_error()
     if st != g.OK:
         raise RuntimeError("device status after timed steps: " + g.status_string(st))
+    if args.trace:
+        # one extra, untimed step with the per-CTA timeline on
+        import numpy as np
+        plan.set(g.OPT_TRACE_ITEMS, 64)
+        l2_flush()
+        step()
+        torch.cuda.synchronize(dev)
+        np.save(args.trace, g.gemm_plan_trace(plan.handle))
+        plan.set(g.OPT_TRACE_ITEMS, 0)
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_step = sum(ms) / len(ms)
     ms_step_max = max_over_ranks(dist, ms_step, dev)
@@ -433,7 +458,8 @@ def run_gpu(args):
             "config": {"workload": args.workload, "M": p0.M if not grouped else [p.M for p in probs],
                        "N": p0.N, "K": p0.K, "alpha": p0.alpha, "beta": p0.beta,
                        "relu": p0.relu, "layout": "row-major A, B, C, D",
-                       "l2": "flushed between steps (256 MiB write, outside the step events)",
+                       "l2": ("flushed between steps (256 MiB write%s, outside the step events)"
+                              % (" then 256 MiB read" if args.flush == "write+read" else "")),
                        "parallelism": "replicas" if ws > 1 else "single",
                        "kernel": cfg},
             "pct_of_peak": 100.0 * achieved / peak,
@@ -462,6 +488,9 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--list", action="store_true")
+    ap.add_argument("--trace", help="after timing, save one step's per-CTA timeline (.npy)")
+    ap.add_argument("--flush", choices=["write", "write+read"], default="write",
+                    help="L2 flush between timed steps")
     args = ap.parse_args(argv)
     if args.list:
         print("\n".join(workloads()))

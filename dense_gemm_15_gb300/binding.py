@@ -21,7 +21,7 @@ EPI_LINEAR, EPI_RELU = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, \
     ERR_DEVICE_FAULT, ERR_NO_DEVICE, ERR_BAD_PLAN = range(10)
 OPT_SCHEDULE, OPT_SPLITS, OPT_CTA_GROUP, OPT_TILE_N, OPT_RASTER, OPT_GRID, \
-    OPT_TIMEOUT_US, OPT_FAULT_SKIP_FLAG = range(8)
+    OPT_TIMEOUT_US, OPT_FAULT_SKIP_FLAG, OPT_SK_DP_WAVES, OPT_TRACE_ITEMS = range(10)
 SCHED_AUTO, SCHED_DP, SCHED_SK, SCHED_SPLIT = range(4)
 
 DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3}
@@ -30,6 +30,7 @@ EXPORTED = (
     "gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
     "grouped_gemm_run", "gemm_plan_query_error", "gemm15_status_string",
     "gemm_plan_set_option", "gemm_plan_last_config", "gemm_run_splitk_noalloc",
+    "gemm_plan_trace",
 )
 
 
@@ -94,6 +95,7 @@ def load(build_if_missing: bool = True):
         lib.gemm15_status_string.restype = ctypes.c_char_p
         lib.gemm_plan_set_option.argtypes = [vp, st, i64]
         lib.gemm_plan_last_config.argtypes = [vp, ctypes.POINTER(Config)]
+        lib.gemm_plan_trace.argtypes = [vp, vp, i64, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.gemm_run_splitk_noalloc.argtypes = [ctypes.POINTER(PlanDesc), vp, i64, vp, i64, vp,
                                                 i64, vp, i64, i64, i64, i64, f32, f32, vp, vp,
                                                 i32, vp, vp]
@@ -194,6 +196,18 @@ def gemm_plan_last_config(plan):
     cfg = Config()
     _check(load().gemm_plan_last_config(plan, ctypes.byref(cfg)), "gemm_plan_last_config")
     return cfg.as_dict()
+
+
+def gemm_plan_trace(plan):
+    """Timeline of the plan's last traced launch: uint64 array [ctas, 1 + items, 8]."""
+    import numpy as np
+    lib = load()
+    ctas, items = ctypes.c_int32(), ctypes.c_int32()
+    lib.gemm_plan_trace(plan, None, 0, ctypes.byref(ctas), ctypes.byref(items))
+    out = np.zeros((max(ctas.value, 0), max(items.value, 0) + 1, 8), dtype=np.uint64)
+    _check(lib.gemm_plan_trace(plan, out.ctypes.data, out.nbytes, ctypes.byref(ctas),
+                               ctypes.byref(items)), "gemm_plan_trace")
+    return out
 
 
 def gemm_run_splitk_noalloc(a, layout_a, layout_b, layout_cd, relu, A, lda, B, ldb, C, ldc, D,

@@ -34,6 +34,8 @@ struct Options {
     int grid = 0;
     int64_t timeout_us = 2000000;  // 2 s
     int fault_skip_flag = -1;
+    int sk_dp_waves = -1;
+    int trace_items = 0;
 };
 
 }  // namespace
@@ -59,6 +61,9 @@ struct gemm15_plan {
     float* d_scales = nullptr;  // two floats for gemm_run_host
     uint32_t epoch = 0;
     int pair_clusters = -1;  // resident SM-pair clusters (queried on first use)
+    uint64_t* d_trace = nullptr;  // timeline of the last traced launch
+    size_t trace_cap = 0;         // bytes
+    int trace_ctas = 0;
     Options opt;
     gemm15_config_t last{};
 };
@@ -260,7 +265,11 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     if (sched == SCHED_DP) {
         units = static_cast<int>(std::min<int64_t>(G, d.tiles));
     } else if (sched == SCHED_SK) {
-        d.dp_tiles = d.tiles >= 2 * G ? (d.tiles / G - 1) * G : 0;
+        if (o.sk_dp_waves >= 0)
+            d.dp_tiles = static_cast<int32_t>(std::min<int64_t>(o.sk_dp_waves, d.tiles / G)) * G;
+        else
+            d.dp_tiles = d.tiles >= 2 * G ? (d.tiles / G - 1) * G : 0;
+        if (d.dp_tiles >= d.tiles) d.dp_tiles = d.tiles - 1;
         d.sk_units = static_cast<int64_t>(d.tiles - d.dp_tiles) * d.k_blocks;
         units = static_cast<int>(std::min<int64_t>(G, d.sk_units));
         d.ws_bytes = static_cast<size_t>(units) * cg * half_tile;
@@ -396,6 +405,29 @@ void record_config(gemm15_plan* plan, const Decision& d, int launches) {
     c.swap_ab = plan->desc.layout_cd == GEMM15_COL_MAJOR ? 1 : 0;
 }
 
+// Points the kernel at a zeroed timeline buffer when tracing is on.
+gemm15_status_t attach_trace(gemm15_plan* plan, GemmParams& gp, int grid, cudaStream_t s) {
+    gp.trace = nullptr;
+    gp.trace_items = 0;
+    if (plan->opt.trace_items <= 0) return GEMM15_OK;
+    const size_t bytes = static_cast<size_t>(grid) * (plan->opt.trace_items + 1) * TRACE_WORDS * 8;
+    if (bytes > plan->trace_cap) {
+        cudaFree(plan->d_trace);
+        plan->d_trace = nullptr;
+        plan->trace_cap = 0;
+        if (cudaMalloc(&plan->d_trace, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM15_ERR_OOM;
+        }
+        plan->trace_cap = bytes;
+    }
+    if (cudaMemsetAsync(plan->d_trace, 0, bytes, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    gp.trace = plan->d_trace;
+    gp.trace_items = plan->opt.trace_items;
+    plan->trace_ctas = grid;
+    return GEMM15_OK;
+}
+
 gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float beta,
                           const float* scale_a, const float* scale_b, cudaStream_t s) {
     gemm15_status_t st = check_operands(plan, p, beta);
@@ -440,6 +472,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return GEMM15_ERR_CUDA;
     gp.D = p.D;
     gp.ldd = p.ldd;
+    gp.C = has_c ? p.C : nullptr;
+    gp.ldc = p.ldc;
     gp.M = static_cast<int32_t>(p.M);
     gp.N = static_cast<int32_t>(p.N);
     gp.K = static_cast<int32_t>(p.K);
@@ -467,6 +501,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.fault_skip_flag = plan->opt.fault_skip_flag;
     gp.groups = nullptr;
     gp.num_groups = 0;
+    st = attach_trace(plan, gp, d.grid, s);
+    if (st != GEMM15_OK) return st;
     if (launch_kernel(plan->elem, d.bn, d.cg, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
     int launches = 1;
     if (d.sched == SCHED_SPLIT) {
@@ -585,6 +621,7 @@ gemm15_status_t gemm_plan_destroy(gemm15_plan_t plan) {
     if (plan->h_groups) cudaFreeHost(plan->h_groups);
     for (void* b : plan->d_host_path) cudaFree(b);
     cudaFree(plan->d_scales);
+    cudaFree(plan->d_trace);
     plan->magic = PLAN_DEAD;
     delete plan;
     return GEMM15_OK;
@@ -754,6 +791,8 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
         e.has_c = has_c;
         e.D = p.D;
         e.ldd = p.ldd;
+        e.C = has_c ? p.C : nullptr;
+        e.ldc = p.ldc;
         e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
                                         : std::min<int32_t>(e.m_blocks, 16);
         const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;
@@ -786,6 +825,10 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     gp.groups = plan->d_groups;
     gp.num_groups = ng;
     const int grid = std::min(G, tiles);
+    {
+        gemm15_status_t tst = attach_trace(plan, gp, grid, s);
+        if (tst != GEMM15_OK) return tst;
+    }
     if (launch_kernel(plan->elem, bn, 1, gp, grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
     Decision d;
     d.bn = bn;
@@ -844,12 +887,38 @@ gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option,
             if (v < 1000 || v > 60000000) return GEMM15_ERR_INVALID_ARG;
             o.timeout_us = v;
             return GEMM15_OK;
+        case GEMM15_OPT_SK_DP_WAVES:
+            if (v < -1 || v > 100000) return GEMM15_ERR_INVALID_ARG;
+            o.sk_dp_waves = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_TRACE_ITEMS:
+            if (v < 0 || v > 65536) return GEMM15_ERR_INVALID_ARG;
+            o.trace_items = static_cast<int>(v);
+            return GEMM15_OK;
         case GEMM15_OPT_FAULT_SKIP_FLAG:
             if (v < -1 || v > 100000) return GEMM15_ERR_INVALID_ARG;
             o.fault_skip_flag = static_cast<int>(v);
             return GEMM15_OK;
     }
     return GEMM15_ERR_INVALID_ARG;
+}
+
+gemm15_status_t gemm_plan_trace(gemm15_plan_t plan, void* out, int64_t capacity, int32_t* ctas,
+                                int32_t* items) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (ctas) *ctas = plan->trace_ctas;
+    if (items) *items = plan->opt.trace_items;
+    if (!plan->d_trace || plan->opt.trace_items <= 0 || !out) return GEMM15_ERR_INVALID_ARG;
+    const size_t bytes =
+        static_cast<size_t>(plan->trace_ctas) * (plan->opt.trace_items + 1) * TRACE_WORDS * 8;
+    if (capacity < 0 || static_cast<size_t>(capacity) < bytes || bytes > plan->trace_cap)
+        return GEMM15_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM15_ERR_CUDA;
+    if (cudaMemcpy(out, plan->d_trace, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM15_ERR_CUDA;
+    return GEMM15_OK;
 }
 
 gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out) {

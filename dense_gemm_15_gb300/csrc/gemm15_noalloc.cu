@@ -209,6 +209,8 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
         if (!ok) return GEMM15_ERR_CUDA;
         gp.D = D;
         gp.ldd = ldd;
+        gp.C = nullptr;  // split-K parts never read C; the reduction does
+        gp.ldc = 0;
         gp.M = static_cast<int32_t>(m);
         gp.N = static_cast<int32_t>(n);
         gp.K = static_cast<int32_t>(K);

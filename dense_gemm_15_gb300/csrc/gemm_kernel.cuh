@@ -274,6 +274,13 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
     return false;
 }
 
+// ------------------------------------------------------------------ tracing
+
+__device__ __forceinline__ uint64_t* trace_rec(const GemmParams& p, int32_t item) {
+    if (!p.trace || item >= p.trace_items) return nullptr;
+    return p.trace + (static_cast<size_t>(blockIdx.x) * (p.trace_items + 1) + 1 + item) * TRACE_WORDS;
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int ELEM, int BN, int CG>
@@ -313,6 +320,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     un.id = static_cast<int32_t>(blockIdx.x) / CG;
     un.count = static_cast<int32_t>(gridDim.x) / CG;
     const bool leader = un.rank == 0;
+    uint64_t* trace_hdr =
+        p.trace ? p.trace + static_cast<size_t>(blockIdx.x) * (p.trace_items + 1) * TRACE_WORDS : nullptr;
+    if (trace_hdr && threadIdx.x == 0) {
+        trace_hdr[0] = globaltimer_ns();
+        trace_hdr[1] = smid();
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -330,8 +343,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(drain, 1);
         mbar_init(epi_bar, EPI_WARPS);
         *abort_flag = 0u;
+        misc[2] = 0u;  // set by the first epilogue thread just before the final barrier
         fence_mbar_init();
     }
+    __syncwarp();
     if (warp == 1) {
         // with CG = 2 one warp of each CTA of the pair allocates collectively
         tmem_alloc<CG>(smem_u32(misc), TR::TMEM_COLS);
@@ -458,6 +473,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                uint64_t* tr = trace_rec(p, static_cast<int32_t>(n_acc));
+                if (tr) tr[2] = globaltimer_ns();
                 const uint32_t d_tmem = tmem_base + ab * BN;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     const int s = n_used % STAGES;
@@ -481,6 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 commit(accf_bar(ab));
+                if (tr) tr[3] = globaltimer_ns();
                 ++n_acc;
             }
             if (issued && (!ok || *abort_flag)) {
@@ -572,6 +590,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            uint64_t* tr = (threadIdx.x == 64) ? trace_rec(p, static_cast<int32_t>(n_acc)) : nullptr;
+            if (tr) {
+                tr[0] = static_cast<uint32_t>(w.tile) | (static_cast<uint64_t>(w.kind) << 32);
+                tr[1] = static_cast<uint32_t>(w.kb0) | (static_cast<uint64_t>(w.kb1) << 32);
+                tr[4] = globaltimer_ns();
+                tr[7] = 0;
+            }
 
             // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
@@ -596,6 +621,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!epi_sync() || *abort_flag) ok = false;
             }
 
+            if (tr) tr[5] = globaltimer_ns();
 #pragma unroll 1
             for (int c = 0; ok && rows_live && c < nch; ++c) {
                 const int32_t col0 = c * EPI_COLS;
@@ -721,6 +747,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if constexpr (CG == 1) mbar_arrive(acce_bar(ab));
                 else mbar_arrive_cluster(acce_bar(ab), 0);
             }
+            if (tr) tr[6] = globaltimer_ns();
             ++n_acc;
 
             if (w.kind == WK_PEER) {
@@ -728,8 +755,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __threadfence();
                 const bool synced = epi_sync();
                 if (threadIdx.x == 64 && ok && synced && !*abort_flag &&
-                    p.fault_skip_flag != un.id)
+                    p.fault_skip_flag != un.id) {
                     st_release_gpu(p.flags + my_slot_unit, p.epoch);
+                    if (tr) tr[7] = globaltimer_ns();
+                }
                 if (!synced) ok = false;
             }
             if (*abort_flag) ok = false;
@@ -743,8 +772,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     }
 
+    // lanes 1..31 of the producer and MMA warps wait here for their lane 0, so
+    // that every warp reaches the CTA barrier converged
+    __syncwarp();
+    if (trace_hdr && threadIdx.x == 64) *reinterpret_cast<volatile uint32_t*>(misc + 2) = 1u;
     tc_fence_before();
     __syncthreads();
+    if (trace_hdr && threadIdx.x == 0) {
+        // 1 if the first epilogue thread's write before the barrier is visible after it
+        trace_hdr[4] = *reinterpret_cast<volatile uint32_t*>(misc + 2);
+        trace_hdr[2] = globaltimer_ns();
+    }
+    if (trace_hdr && threadIdx.x == 64) trace_hdr[3] = globaltimer_ns();
     // the pair's MMAs read both CTAs' shared memory and write both TMEMs
     if constexpr (CG == 2) cluster_sync();
     if (warp == 1) {

@@ -12,7 +12,7 @@ enum DeviceError : int { DEV_ERR_TIMEOUT = 5, DEV_ERR_FAULT = 7 };
 
 constexpr int TILE_M = 128;         // rows of A per CTA (UMMA M for one SM)
 constexpr int EPI_WARPS = 4;        // epilogue warps (one per 32-lane TMEM quarter)
-constexpr int NUM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, then epilogue
 constexpr int EPI_COLS = 64;        // output columns per epilogue chunk (128 B of 16-bit)
 constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32-row x 128-byte epilogue staging box
 
@@ -24,12 +24,16 @@ struct alignas(128) GroupEntry {
     int32_t raster, pad0;
     void* D;                          // for the ragged last column chunk
     int64_t ldd;
+    const void* C;                    // read directly by the epilogue
+    int64_t ldc;
 };
 
 struct GemmParams {
     CUtensorMap tmA, tmB, tmC, tmD;  // dense problem (unused when grouped)
     void* D;                          // D and its leading dimension (elements), for
     int64_t ldd;                      // column chunks the TMA store cannot clip exactly
+    const void* C;                    // C and its leading dimension (elements); the
+    int64_t ldc;                      // epilogue reads C straight into registers
     int32_t M, N, K;
     int32_t k_blocks;                 // ceil(K / BK)
     int32_t m_blocks, n_blocks, tiles;
@@ -58,7 +62,19 @@ struct GemmParams {
     // grouped problems (device table) or null
     const GroupEntry* groups;
     int32_t num_groups;
+    // optional timeline: per CTA a header record then one record per work
+    // item, TRACE_WORDS 64-bit words each (null = off)
+    uint64_t* trace;
+    int32_t trace_items;
 };
+
+constexpr int TRACE_WORDS = 8;
+// header record: [0] globaltimer at kernel start, [1] SM id, [2] / [3]
+// globaltimer after the final CTA barrier seen by thread 0 / the first
+// epilogue thread, [4] 1 if thread 0 saw the first epilogue thread's
+// pre-barrier write after the barrier.  item record: [0] tile | kind << 32, [1] kb0 | kb1 << 32,
+// [2] MMA start, [3] MMA issue done, [4] accumulator ready (epilogue),
+// [5] chunk loop start, [6] epilogue done, [7] partial published.
 
 struct ReduceParams {
     const float* ws;

@@ -171,8 +171,13 @@ typedef enum {
     GEMM15_OPT_RASTER = 4,       /* 0 auto, else M-blocks per raster band */
     GEMM15_OPT_GRID = 5,         /* 0 auto (one CTA per SM), else max CTAs */
     GEMM15_OPT_TIMEOUT_US = 6,   /* bound of every device-side wait, microseconds */
-    GEMM15_OPT_FAULT_SKIP_FLAG = 7 /* test hook: stream-K peer CTA that skips its
-                                      partial-ready flag (-1 = none) */
+    GEMM15_OPT_FAULT_SKIP_FLAG = 7, /* test hook: stream-K peer unit that skips its
+                                       partial-ready flag (-1 = none) */
+    GEMM15_OPT_SK_DP_WAVES = 8,    /* stream-K: full waves run data-parallel before
+                                      the stream-K region (-1 = auto) */
+    GEMM15_OPT_TRACE_ITEMS = 9     /* record a per-CTA timeline of up to this many
+                                      work items per launch (0 = off); read it
+                                      with gemm_plan_trace */
 } gemm15_option_t;
 
 /* Sets an option on the plan; INVALID_ARG for unknown options or values. */
@@ -193,6 +198,20 @@ typedef struct {
 } gemm15_config_t;
 
 gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out);
+
+/* Copies the timeline of the plan's last traced GEMM-kernel launch (see
+ * GEMM15_OPT_TRACE_ITEMS) into the HOST buffer `out` of `capacity` bytes, after
+ * synchronising the plan's device.  Layout: for each of *ctas CTAs, one header
+ * record then *items item records, 8 uint64 each (globaltimer nanoseconds).
+ * Header: start, SM id, time after the final CTA barrier seen by thread 0 and
+ * by the first epilogue thread, 1 if thread 0 saw after that barrier a value
+ * the first epilogue thread wrote before it.  Item: tile | kind << 32 (0 whole tile, 1
+ * stream-K peer part, 2 stream-K owner part, 3 split-K part), kb0 | kb1 << 32,
+ * MMA start, MMA issued, accumulator ready, epilogue chunks start, epilogue
+ * done, partial published; unused items are zero.  INVALID_ARG if tracing is
+ * off or `capacity` is too small (*ctas and *items are still set). */
+gemm15_status_t gemm_plan_trace(gemm15_plan_t plan, void* out, int64_t capacity, int32_t* ctas,
+                                int32_t* items);
 
 /* ---- Split-K GEMM that allocates nothing.  The pages have no counterpart of
  * this entry point; it exists for callers that cannot call cudaMalloc: code

@@ -323,3 +323,32 @@ def test_sm_pair_tiles_chosen_for_large_problems_and_deterministic():
     assert np.array_equal(d1, d2)
     for rows in sample_rows(prob.M, count=3, span=16):
         assert_matches_oracle(prob, d1, rows=rows)
+
+
+def test_timeline_trace_covers_every_k_block_once():
+    prob = inputs.random_problem(512, 768, 4096, beta=1.0)
+    plan = plan_for(prob, schedule=g.SCHED_SK, cta_group=2, trace_items=16)
+    assert_matches_oracle(prob, run_gpu(plan, prob))
+    tr = g.gemm_plan_trace(plan.handle)
+    cfg = plan.last_config()
+    assert tr.shape == (cfg["grid"], 17, 8)
+    kb_total = (4096 + 63) // 64
+    covered = {}
+    for cta in range(tr.shape[0]):
+        hdr = tr[cta, 0]
+        assert hdr[0] > 0 and hdr[2] >= hdr[0]
+        assert hdr[4] == 1, "the final CTA barrier did not order the epilogue before thread 0"
+        if cta % 2:  # the pair's second CTA mirrors the first one's items
+            continue
+        for rec in tr[cta, 1:]:
+            if rec[4] == 0:
+                continue
+            tile = int(rec[0] & 0xffffffff)
+            kb0, kb1 = int(rec[1] & 0xffffffff), int(rec[1] >> 32)
+            assert rec[2] <= rec[3] and rec[4] <= rec[6]
+            covered.setdefault(tile, []).append((kb0, kb1))
+    assert len(covered) == cfg["tiles"]
+    for tile, parts in covered.items():
+        parts.sort()
+        assert parts[0][0] == 0 and parts[-1][1] == kb_total
+        assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
