@@ -219,13 +219,15 @@ int pair_clusters(gemm15_plan* plan) {
     return plan->pair_clusters;
 }
 
-// Picks the tile shape, schedule and grid for one problem.
+// Picks the tile shape, schedule and grid for one problem (thresholds set
+// from measurements of the target shapes on GB300):
 //   - SM-pair 256 x 256 tiles (cta_group::2) when there is at least one full
 //     wave of them: they halve each SM's share of B traffic;
-//   - data-parallel when the last wave is at least 90% full, else stream-K
-//     over the tail waves (all tiles when there is less than one wave), or
-//     split-K with a separate reduction when stream-K would split one tile
-//     over more than 3 units.
+//   - at least one wave: data-parallel when the last wave is at least 80%
+//     full, else stream-K over the tail waves;
+//   - less than one wave: split-K with a separate reduction when at least two
+//     splits per tile fit (stream-K otherwise), unless K is short (fewer than
+//     32 k-blocks), where data-parallel 128 x 128 tiles win.
 Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     Decision d;
     const Options& o = plan->opt;
@@ -240,21 +242,28 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     }
     d.cg = cg;
     const int G = cg == 2 ? std::min(pair_clusters(plan), G1 / 2) : G1;  // scheduling units
-    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M * cg));
-    d.n_blocks = static_cast<int32_t>(cdiv(N, d.bn));
-    d.tiles = d.m_blocks * d.n_blocks;
     d.k_blocks = static_cast<int32_t>(cdiv(K, d.bk));
+    auto set_tiles = [&]() {
+        d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M * cg));
+        d.n_blocks = static_cast<int32_t>(cdiv(N, d.bn));
+        d.tiles = d.m_blocks * d.n_blocks;
+    };
+    set_tiles();
 
     int sched = o.schedule;
     if (sched == 0) {
         if (d.tiles >= G) {
             const int64_t waves = cdiv(d.tiles, G);
             const double eff = static_cast<double>(d.tiles) / static_cast<double>(waves * G);
-            sched = (eff >= 0.9 || d.k_blocks < 8) ? SCHED_DP : SCHED_SK;
-        } else if (d.k_blocks < 4) {
+            sched = (eff >= 0.8 || d.k_blocks < 8) ? SCHED_DP : SCHED_SK;
+        } else if (d.k_blocks < 32) {
             sched = SCHED_DP;
+            if (!o.tile_n && cg == 1 && d.bn == 256) {
+                d.bn = 128;  // twice the tiles to spread a short-K problem
+                set_tiles();
+            }
         } else {
-            sched = (G / d.tiles <= 3) ? SCHED_SK : SCHED_SPLIT;
+            sched = (G / d.tiles >= 2) ? SCHED_SPLIT : SCHED_SK;
         }
     }
     d.sched = sched;
