@@ -235,10 +235,13 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     d.bn = o.tile_n ? o.tile_n : (N <= 128 ? 128 : 256);
     const int G1 = o.grid > 0 ? std::min(o.grid, plan->num_sms) : plan->num_sms;
     int cg = 1;
-    if (d.bn == 256 && o.cta_group != 1) {
+    // SM-pair tiles 256 x 128 exist for 16-bit operands only (an fp8 half-tile
+    // of B would be narrower than one 128-byte swizzle row)
+    const bool pair_ok = d.bn == 256 || plan->elem != ELEM_E4M3;
+    if (pair_ok && o.cta_group != 1) {
         const int clusters = std::min(pair_clusters(plan), G1 / 2);
         const int64_t tiles2 = cdiv(M, 2 * TILE_M) * cdiv(N, 256);
-        if (clusters > 0 && (o.cta_group == 2 || (M >= 512 && tiles2 >= clusters))) cg = 2;
+        if (clusters > 0 && (o.cta_group == 2 || (d.bn == 256 && M >= 512 && tiles2 >= clusters))) cg = 2;
     }
     d.cg = cg;
     const int G = cg == 2 ? std::min(pair_clusters(plan), G1 / 2) : G1;  // scheduling units
@@ -325,8 +328,8 @@ gemm15_status_t ensure_ws(gemm15_plan* plan, size_t bytes, int flags) {
 
 cudaError_t launch_kernel(int elem, int bn, int cg, const GemmParams& gp, int grid, cudaStream_t s) {
     if (cg == 2) {
-        if (elem == ELEM_F16) return launch_gemm<ELEM_F16, 256, 2>(gp, grid, s);
-        if (elem == ELEM_BF16) return launch_gemm<ELEM_BF16, 256, 2>(gp, grid, s);
+        if (elem == ELEM_F16) return bn == 128 ? launch_gemm<ELEM_F16, 128, 2>(gp, grid, s) : launch_gemm<ELEM_F16, 256, 2>(gp, grid, s);
+        if (elem == ELEM_BF16) return bn == 128 ? launch_gemm<ELEM_BF16, 128, 2>(gp, grid, s) : launch_gemm<ELEM_BF16, 256, 2>(gp, grid, s);
         return launch_gemm<ELEM_E4M3, 256, 2>(gp, grid, s);
     }
     if (elem == ELEM_F16) return bn == 128 ? launch_gemm<ELEM_F16, 128>(gp, grid, s) : launch_gemm<ELEM_F16, 256>(gp, grid, s);

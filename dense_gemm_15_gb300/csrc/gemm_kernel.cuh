@@ -47,7 +47,11 @@ struct Traits {
     static constexpr int B_COLS = BN / CG;             // B columns staged by one CTA
     static constexpr int B_STAGE = B_COLS * 128;       // 16 or 32 KB
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = (STAGE_BYTES == 48 * 1024) ? 4 : 6;
+    // as many stages as fit next to the 32 KB of epilogue staging (at most 8)
+    static constexpr int STAGES_FIT = (232448 - 1024 - 256 - EPI_WARPS * 2 * EPI_BUF_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    // an N-major B stage is whole 128-byte swizzle rows of N
+    static_assert(B_COLS * ESIZE >= 128 && (B_COLS * ESIZE) % 128 == 0, "B columns per CTA");
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // 32 KB
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -99,6 +103,13 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
         __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
         return __bfloat1622float2(h);
     }
+}
+
+// max(x, 0) that keeps NaN (one max.NaN instruction).
+__device__ __forceinline__ float relu_nan(float x) {
+    float r;
+    asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(x));
+    return r;
 }
 
 // ------------------------------------------------------------------ errors
@@ -713,7 +724,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     if (relu) {
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) o[t] = o[t] > 0.0f ? o[t] : (o[t] != o[t] ? o[t] : 0.0f);
+                        for (int t = 0; t < 8; ++t) o[t] = relu_nan(o[t]);
                     }
                     if (!ragged) {
                         st_shared_v4(slot, pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
@@ -839,7 +850,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
                 else cv = __bfloat162float(crow[t]);
                 x = fmaf(p.beta, cv, x);
             }
-            if (p.relu) x = x > 0.0f ? x : (x != x ? x : 0.0f);
+            if (p.relu) x = relu_nan(x);
             o[t] = x;
         }
         if (nvalid == 8) {

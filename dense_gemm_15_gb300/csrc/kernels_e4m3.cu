@@ -8,12 +8,15 @@ template cudaError_t launch_gemm<ELEM_E4M3, 256, 2>(const GemmParams&, int, cuda
 template int max_pair_clusters<ELEM_E4M3>();
 
 int gemm_smem_bytes(int elem, int bn, int cg) {
-    if (cg == 2) return Traits<ELEM_F16, 256, 2>::SMEM_BYTES;
+    if (cg == 2) return bn == 128 ? Traits<ELEM_F16, 128, 2>::SMEM_BYTES : Traits<ELEM_F16, 256, 2>::SMEM_BYTES;
     if (elem == ELEM_E4M3) return bn == 128 ? Traits<ELEM_E4M3, 128>::SMEM_BYTES : Traits<ELEM_E4M3, 256>::SMEM_BYTES;
     return bn == 128 ? Traits<ELEM_F16, 128>::SMEM_BYTES : Traits<ELEM_F16, 256>::SMEM_BYTES;
 }
 int gemm_stages(int elem, int bn, int cg) {
-    if (cg == 2) return elem == ELEM_E4M3 ? Traits<ELEM_E4M3, 256, 2>::STAGES : Traits<ELEM_F16, 256, 2>::STAGES;
+    if (cg == 2) {
+        if (elem == ELEM_E4M3) return Traits<ELEM_E4M3, 256, 2>::STAGES;
+        return bn == 128 ? Traits<ELEM_F16, 128, 2>::STAGES : Traits<ELEM_F16, 256, 2>::STAGES;
+    }
     if (elem == ELEM_E4M3) return bn == 128 ? Traits<ELEM_E4M3, 128>::STAGES : Traits<ELEM_E4M3, 256>::STAGES;
     return bn == 128 ? Traits<ELEM_F16, 128>::STAGES : Traits<ELEM_F16, 256>::STAGES;
 }

@@ -352,3 +352,17 @@ def test_timeline_trace_covers_every_k_block_once():
         parts.sort()
         assert parts[0][0] == 0 and parts[-1][1] == kb_total
         assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
+
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("dtype,a_col,b_col", [("f16", False, False), ("bf16", True, False),
+                                               ("f16", False, True), ("bf16", True, True)])
+def test_sm_pair_tiles_256x128(sched, dtype, a_col, b_col):
+    """256 x 128 tiles on an SM pair (each CTA stages 64 columns of B)."""
+    prob = inputs.random_problem(520, 392, 1096, dtype=dtype, beta=0.5, alpha=1.5, relu=True,
+                                 a_col_major=a_col, b_col_major=b_col)
+    plan = plan_for(prob, schedule=sched, cta_group=2, tile_n=128)
+    d = run_gpu(plan, prob)
+    cfg = plan.last_config()
+    assert cfg["cta_group"] == 2 and cfg["tile_m"] == 256 and cfg["tile_n"] == 128
+    assert_matches_oracle(prob, d)
