@@ -223,8 +223,11 @@ int pair_clusters(gemm15_plan* plan) {
 // from measurements of the target shapes on GB300):
 //   - SM-pair 256 x 256 tiles (cta_group::2) when there is at least one full
 //     wave of them: they halve each SM's share of B traffic;
-//   - at least one wave: data-parallel when the last wave is at least 80%
-//     full, else stream-K over the tail waves;
+//   - at least one wave: data-parallel when the last wave is at least 95%
+//     full, or at least 80% full while A and B together exceed 64 MiB (then
+//     stream-K's units, which sweep different k ranges of tiles that share
+//     operands at the same time, lose more to L2 misses than the tail wave
+//     costs); stream-K over the tail waves otherwise;
 //   - less than one wave: split-K with a separate reduction when at least two
 //     splits per tile fit (stream-K otherwise), unless K is short (fewer than
 //     32 k-blocks), where data-parallel 128 x 128 tiles win.
@@ -258,7 +261,10 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
         if (d.tiles >= G) {
             const int64_t waves = cdiv(d.tiles, G);
             const double eff = static_cast<double>(d.tiles) / static_cast<double>(waves * G);
-            sched = (eff >= 0.8 || d.k_blocks < 8) ? SCHED_DP : SCHED_SK;
+            const int64_t esize = plan->elem == ELEM_E4M3 ? 1 : 2;
+            const bool operands_fit_l2 = (M + N) * K * esize <= (int64_t{64} << 20);
+            const bool dp = eff >= 0.95 || (eff >= 0.8 && !operands_fit_l2) || d.k_blocks < 8;
+            sched = dp ? SCHED_DP : SCHED_SK;
         } else if (d.k_blocks < 32) {
             sched = SCHED_DP;
             if (!o.tile_n && cg == 1 && d.bn == 256) {

@@ -47,18 +47,28 @@ struct Traits {
     static constexpr int B_COLS = BN / CG;             // B columns staged by one CTA
     static constexpr int B_STAGE = B_COLS * 128;       // 16 or 32 KB
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    // as many stages as fit next to the 32 KB of epilogue staging (at most 8)
-    static constexpr int STAGES_FIT = (232448 - 1024 - 256 - EPI_WARPS * 2 * EPI_BUF_BYTES) / STAGE_BYTES;
+    // Epilogue staging: one 32 x 64 box per warp and output chunk of the tile
+    // when that leaves room for six stages (the whole C tile is then fetched
+    // as soon as the tile starts), else a ring of two boxes per warp (the rest
+    // of the C tile is then prefetched into L2 when the tile starts).
+    static constexpr int NCH = BN / EPI_COLS;          // output chunks per tile row
+    static constexpr int SMEM_FIXED = 232448 - 1024 - 256;
+    static constexpr int STAGES_WHOLE = (SMEM_FIXED - EPI_WARPS * NCH * EPI_BUF_BYTES) / STAGE_BYTES;
+    static constexpr int EPI_BUFS = (NCH <= 2 || STAGES_WHOLE >= 6) ? NCH : 2;
+    static constexpr bool EPI_WHOLE = EPI_BUFS == NCH;
+    static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+    // as many stages as fit next to the epilogue staging (at most 8)
+    static constexpr int STAGES_FIT = (SMEM_FIXED - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     // an N-major B stage is whole 128-byte swizzle rows of N
     static_assert(B_COLS * ESIZE >= 128 && (B_COLS * ESIZE) % 128 == 0, "B columns per CTA");
-    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // 32 KB
+    static_assert(EPI_BUFS <= 8, "C barrier parity bits");
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    // barriers: full[S], empty[S], acc_full[2], acc_empty[2], cbar[4][2], drain, epi
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 2;
+    // barriers: full[S], empty[S], acc_full[2], acc_empty[2], cbar[4][EPI_BUFS], drain, epi
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_BUFS * EPI_WARPS + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
@@ -175,10 +185,20 @@ struct Unit {
     int32_t id, count, rank, cg;
 };
 
+// A stream-K unit's range [u0, u_end) of (tile, k-block) iterations holds at
+// most one peer piece (its start, inside a tile), whole tiles, and at most one
+// owner piece (its end: the k = 0 head of a tile).  The pieces are taken in the
+// order peer, owner, whole tiles: the peer piece first because an earlier
+// unit's owner waits for it, the owner piece before the whole tiles so that
+// its wait for later units' peer pieces and its longer fix-up epilogue overlap
+// the whole tiles' mainloop instead of trailing it.
 struct SchedState {
     int32_t i;          // data-parallel / split item counter
     int32_t phase;      // 0 data-parallel, 1 stream-K, 2 done
-    int64_t u, u_end;   // stream-K unit cursor
+    int32_t step;       // stream-K: 0 peer piece, 1 owner piece, 2 whole tiles
+    int64_t u0, u_end;  // stream-K range of this unit
+    int64_t u;          // stream-K: end of the peer piece, then cursor over whole tiles
+    int64_t o_begin;    // stream-K: start of the owner piece (u_end if none)
 };
 
 __device__ __forceinline__ int64_t sk_begin(const GemmParams& p, const Unit& un, int64_t unit) {
@@ -199,11 +219,17 @@ __device__ __forceinline__ void raster_coords(int32_t tile, int32_t m_blocks, in
 __device__ __forceinline__ void sched_init(const GemmParams& p, const Unit& un, SchedState& s) {
     s.i = 0;
     s.phase = 0;
-    s.u = 0;
-    s.u_end = 0;
+    s.step = 0;
+    s.u0 = s.u = s.u_end = s.o_begin = 0;
     if (p.sched == SCHED_SK) {
-        s.u = sk_begin(p, un, un.id);
+        const int64_t kb = p.k_blocks;
+        s.u0 = sk_begin(p, un, un.id);
         s.u_end = sk_begin(p, un, un.id + 1);
+        // end of the peer piece (u0 itself when the range starts on a tile)
+        s.u = (s.u0 % kb) ? min(s.u_end, (s.u0 / kb + 1) * kb) : s.u0;
+        // start of the owner piece (u_end when the range ends on a tile)
+        const int64_t last_tile = (s.u_end / kb) * kb;
+        s.o_begin = (s.u_end % kb && last_tile >= s.u) ? last_tile : s.u_end;
     }
 }
 
@@ -259,18 +285,37 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
         s.phase = (p.sched == SCHED_SK) ? 1 : 2;
     }
     if (s.phase == 1) {
-        if (s.u >= s.u_end) {
-            s.phase = 2;
-            return false;
-        }
         const int32_t kb = p.k_blocks;
-        const int32_t rel = static_cast<int32_t>(s.u / kb);
+        int64_t b0 = -1, b1 = -1;  // the next piece, [b0, b1) within one tile
+        if (s.step == 0) {
+            s.step = 1;
+            if (s.u > s.u0) {
+                b0 = s.u0;
+                b1 = s.u;
+            }
+        }
+        if (b0 < 0 && s.step == 1) {
+            s.step = 2;
+            if (s.o_begin < s.u_end) {
+                b0 = s.o_begin;
+                b1 = s.u_end;
+            }
+        }
+        if (b0 < 0) {
+            if (s.u >= s.o_begin) {
+                s.phase = 2;
+                return false;
+            }
+            b0 = s.u;
+            b1 = s.u + kb;
+            s.u = b1;
+        }
+        const int32_t rel = static_cast<int32_t>(b0 / kb);
         const int64_t tile_u0 = static_cast<int64_t>(rel) * kb;
         w.tile = p.dp_tiles + rel;
         fill_coords(p, w);
-        w.kb0 = static_cast<int32_t>(s.u - tile_u0);
-        const int64_t end = min(s.u_end, tile_u0 + kb);
-        w.kb1 = static_cast<int32_t>(end - tile_u0);
+        w.kb0 = static_cast<int32_t>(b0 - tile_u0);
+        w.kb1 = static_cast<int32_t>(b1 - tile_u0);
         if (w.kb0 == 0 && w.kb1 == kb) {
             w.kind = WK_FULL;
         } else if (w.kb0 == 0) {
@@ -279,7 +324,6 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
             w.kind = WK_PEER;
         }
         w.slot = un.id * un.cg + un.rank;
-        s.u = end;
         return true;
     }
     return false;
@@ -315,8 +359,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    auto c_bar = [&](int q, int b) { return bar0 + 8u * (2 * STAGES + 4 + 2 * q + b); };
-    const uint32_t drain = bar0 + 8u * (2 * STAGES + 4 + 2 * EPI_WARPS);
+    constexpr int EPI_BUFS = TR::EPI_BUFS;
+    auto c_bar = [&](int q, int b) { return bar0 + 8u * (2 * STAGES + 4 + EPI_BUFS * q + b); };
+    const uint32_t drain = bar0 + 8u * (2 * STAGES + 4 + EPI_BUFS * EPI_WARPS);
     const uint32_t epi_bar = drain + 8u;  // bounded barrier of the 4 epilogue warps
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + TR::OFF_MISC);
     volatile uint32_t* tmem_slot = misc;
@@ -347,10 +392,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), EPI_WARPS * CG);  // both CTAs' epilogues release
         }
-        for (int q = 0; q < EPI_WARPS; ++q) {
-            mbar_init(c_bar(q, 0), 1);
-            mbar_init(c_bar(q, 1), 1);
-        }
+        for (int q = 0; q < EPI_WARPS; ++q)
+            for (int b = 0; b < EPI_BUFS; ++b) mbar_init(c_bar(q, b), 1);
         mbar_init(drain, 1);
         mbar_init(epi_bar, EPI_WARPS);
         *abort_flag = 0u;
@@ -523,13 +566,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;                 // TMEM lane quarter of this warp
         const int e = warp - 2;                 // epilogue warp index (buffers)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t ebuf0 = sEpi + e * 2 * EPI_BUF_BYTES;
+        const uint32_t ebuf0 = sEpi + e * EPI_BUFS * EPI_BUF_BYTES;
         float alpha = p.alpha;
         if (p.scale_a) alpha *= __ldg(p.scale_a);
         if (p.scale_b) alpha *= __ldg(p.scale_b);
         const float beta = p.beta;
         const bool relu = p.relu != 0;
-        constexpr int NCH = BN / EPI_COLS;
+        constexpr int NCH = TR::NCH;
+        constexpr bool WHOLE = TR::EPI_WHOLE;  // one staging box per chunk of the tile
+        // Stream-K partial tiles are stored in groups of four columns: float4
+        // (warp quarter q, column group g, lane) sits at (q * BN/4 + g) * 32 + lane,
+        // so that each warp-wide float4 access covers 512 contiguous bytes.
+        auto peer_off = [&](int32_t col0) -> size_t {
+            return (static_cast<size_t>(q) * (BN / 4) + col0 / 4) * 32 + lane;
+        };
+        // this thread's first float4 of chunk col0 in unit pb's partial tile
+        auto peer_src = [&](int64_t pb, int32_t col0) -> const float4* {
+            return reinterpret_cast<const float4*>(p.ws + static_cast<size_t>(pb * CG + un.rank) * TILE_M * BN) +
+                   peer_off(col0);
+        };
+        // the first unit >= pb that holds part of the tile ending at unit
+        // iteration tile_end (a peer of its owner), or -1
+        auto next_peer = [&](int64_t pb, int64_t tile_end) -> int64_t {
+            for (; pb < un.count && sk_begin(p, un, pb) < tile_end; ++pb)
+                if (sk_begin(p, un, pb) != sk_begin(p, un, pb + 1)) return pb;
+            return -1;
+        };
 
         // Bounded barrier of the four epilogue warps (mbarrier with count 4):
         // release/acquire at CTA scope, and it cannot hang if a warp gives up.
@@ -546,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         sched_init(p, un, st);
         Work w;
         uint32_t n_acc = 0;
-        uint32_t n_chunk = 0;      // chunks staged by this warp (buffer parity)
+        uint32_t n_chunk = 0;      // chunks stored by this warp (ring buffer parity)
         uint32_t c_phase = 0;      // per-buffer C barrier parity bits
         uint32_t c_pending = 0;    // C loads issued and not yet waited for
         int last_group = -1;
@@ -587,14 +649,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool stage_c = has_c && !to_ws && rows_live;
             const int nch = min(NCH, (N - n0 + EPI_COLS - 1) / EPI_COLS);
 
-            // C for the first chunk is fetched while the mainloop still runs
-            if (stage_c && lane == 0) {
+            // C is fetched while the mainloop still runs: the whole tile when
+            // every chunk has its own box, else the first chunk, with the rest
+            // prefetched into L2
+            if (WHOLE && !to_ws && lane == 0) {
+                bulk_wait_read<0>();  // the previous tile's stores have read their boxes
+                if (stage_c) {
+                    for (int c = 0; c < nch; ++c) {
+                        mbar_arrive_expect_tx(c_bar(e, c), EPI_BUF_BYTES);
+                        tma_load_2d(ebuf0 + c * EPI_BUF_BYTES, tC, c_bar(e, c), n0 + c * EPI_COLS, row0);
+                        c_pending |= 1u << c;
+                    }
+                }
+            } else if (!WHOLE && stage_c && lane == 0) {
+                // the latest store read the other box; the one before it read this one
                 const uint32_t b = n_chunk & 1u;
-                bulk_wait_read<0>();
+                bulk_wait_read<1>();
                 mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
                 tma_load_2d(ebuf0 + b * EPI_BUF_BYTES, tC, c_bar(e, b), n0, row0);
                 c_pending |= 1u << b;
+                for (int c = 1; c < nch; ++c) tma_prefetch_l2_2d(tC, n0 + c * EPI_COLS, row0);
             }
+            __syncwarp();  // lane 0's wait for the stores orders the warp's writes to the boxes
 
             if (!wait_bar(ctl, accf_bar(ab), aph)) {
                 ok = false;
@@ -612,8 +688,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
                 if (threadIdx.x == 64) {
-                    for (int64_t b = un.id + 1; b < un.count && sk_begin(p, un, b) < tile_end_unit; ++b) {
-                        if (sk_begin(p, un, b) == sk_begin(p, un, b + 1)) continue;
+                    for (int64_t b = next_peer(un.id + 1, tile_end_unit); b >= 0;
+                         b = next_peer(b + 1, tile_end_unit)) {
                         const uint32_t* flag = p.flags + b * CG + un.rank;
                         const uint64_t t0 = globaltimer_ns();
                         uint32_t it = 0;
@@ -636,9 +712,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
             for (int c = 0; ok && rows_live && c < nch; ++c) {
                 const int32_t col0 = c * EPI_COLS;
-                const uint32_t b = n_chunk & 1u;
+                const uint32_t b = WHOLE ? static_cast<uint32_t>(c) : (n_chunk & 1u);
                 const uint32_t buf = ebuf0 + b * EPI_BUF_BYTES;
-                if (stage_c) {
+                if (WHOLE) {
+                    // nothing to wait for: the boxes were freed when the tile started
+                } else if (stage_c) {
                     // prefetch C of the next chunk into the other buffer once the
                     // store that last used it has read it
                     if (c + 1 < nch && lane == 0) {
@@ -667,14 +745,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (w.kind == WK_OWNER) {
                     // add the peer units' partial tiles in unit order (deterministic)
-                    for (int64_t pb = un.id + 1; pb < un.count && sk_begin(p, un, pb) < tile_end_unit; ++pb) {
-                        if (sk_begin(p, un, pb) == sk_begin(p, un, pb + 1)) continue;
-                        const float4* src = reinterpret_cast<const float4*>(
-                            p.ws + static_cast<size_t>(pb * CG + un.rank) * TILE_M * BN +
-                            static_cast<size_t>(q * 32 + lane) * BN + col0);
+                    for (int64_t pb = next_peer(un.id + 1, tile_end_unit); pb >= 0;
+                         pb = next_peer(pb + 1, tile_end_unit)) {
+                        const float4* src = peer_src(pb, col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float4 t = __ldcg(src + i);
+                            const float4 t = __ldcg(src + 32 * i);
                             v[4 * i + 0] += t.x;
                             v[4 * i + 1] += t.y;
                             v[4 * i + 2] += t.z;
@@ -683,12 +759,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (to_ws) {
-                    float4* dst = reinterpret_cast<float4*>(
-                        p.ws + static_cast<size_t>(w.slot) * TILE_M * BN +
-                        static_cast<size_t>(q * 32 + lane) * BN + col0);
+                    float4* dst = reinterpret_cast<float4*>(p.ws + static_cast<size_t>(w.slot) * TILE_M * BN);
+                    if (w.kind == WK_PEER) {
+                        // read back only by the owner's epilogue, in the same layout
+                        dst += peer_off(col0);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                        for (int i = 0; i < 16; ++i)
+                            __stcg(dst + 32 * i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                    } else {
+                        // split-K partials: row-major tiles, as the reduction kernel reads them
+                        dst += (static_cast<size_t>(q * 32 + lane) * BN + col0) / 4;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                    }
                     continue;
                 }
                 if (stage_c) {
@@ -705,16 +789,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool ragged = left < EPI_COLS && (left & 7) != 0;
                 const int32_t my_row = row0 + lane;
                 OutT* drow = Dptr + static_cast<int64_t>(my_row) * ldd + n0 + col0;
+                // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane % 8)
+                auto slot_of = [&](int j) { return buf + lane * 128 + ((j ^ (lane & 7)) << 4); };
+                // all eight C loads first: each store below writes the box they read
+                uint4 cvs[8];
+                if (stage_c) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cvs[j] = ld_shared_v4(slot_of(j));
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane % 8)
-                    const uint32_t slot = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                    const uint32_t slot = slot_of(j);
                     float o[8];
 #pragma unroll
                     for (int t = 0; t < 8; ++t) o[t] = alpha * v[8 * j + t];
                     if (stage_c) {
-                        const uint4 cv = ld_shared_v4(slot);
-                        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+                        const uint32_t cw[4] = {cvs[j].x, cvs[j].y, cvs[j].z, cvs[j].w};
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
                             const float2 f = unpack2<ELEM>(cw[t]);
@@ -774,11 +864,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (*abort_flag) ok = false;
         }
-        // drain outstanding C loads and D stores of this warp
+        // drain outstanding C loads; D stores must have read their boxes before
+        // the shared memory goes away (their global writes complete with the grid)
         if (lane == 0) {
-            for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < EPI_BUFS; ++b)
                 if (c_pending & (1u << b)) drain_bar(c_bar(e, b), (c_phase >> b) & 1u, 200000000ull);
-            bulk_wait<0>();
+            bulk_wait_read<0>();
         }
         __syncwarp();
     }

@@ -109,6 +109,14 @@ __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
 }
 
 // 2-D tiled load into this CTA's shared memory, completion on `bar`.
+// Prefetch of one tensor-map box into L2 (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,
                                             int32_t x, int32_t y) {
     asm volatile(

@@ -1,6 +1,8 @@
 """Parity of the GEMM variants against the oracle: stream-K and split-K
 schedules, grouped GEMM, fp8 e4m3 with per-tensor scales, column-major C/D,
 padded leading dimensions, K == 0 and the bounded-wait timeout path."""
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -352,6 +354,26 @@ def test_timeline_trace_covers_every_k_block_once():
         parts.sort()
         assert parts[0][0] == 0 and parts[-1][1] == kb_total
         assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
+
+
+@pytest.mark.parametrize("cg,grid", [(1, 4), (2, 8)])
+def test_stream_k_takes_peer_then_owner_then_whole_tiles(cg, grid):
+    """Four units over six tiles of 64 k-blocks: 96 k-blocks each, so every
+    unit holds a whole tile and a peer or an owner piece; each unit runs its
+    peer piece, then its owner piece, then its whole tiles."""
+    m = 128 * cg
+    prob = inputs.random_problem(2 * m, 768, 4096, beta=1.0, relu=True)
+    plan = plan_for(prob, schedule=g.SCHED_SK, cta_group=cg, grid=grid, trace_items=8)
+    assert_matches_oracle(prob, run_gpu(plan, prob))
+    cfg = plan.last_config()
+    assert cfg["grid"] == grid and cfg["tiles"] == 6
+    tr = g.gemm_plan_trace(plan.handle)
+    seen = []
+    for cta in range(0, grid, cg):
+        kinds = "".join("FPOS"[int(rec[0] >> 32)] for rec in tr[cta, 1:] if rec[4] != 0)
+        assert re.fullmatch(r"P?O?F*", kinds), kinds
+        seen.append(kinds)
+    assert seen == ["OF", "PF", "OF", "PF"]
 
 
 @pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
