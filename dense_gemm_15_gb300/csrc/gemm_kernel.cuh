@@ -27,6 +27,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "gemm_params.h"
 #include "ptx.cuh"
 
@@ -572,6 +574,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (p.scale_b) alpha *= __ldg(p.scale_b);
         const float beta = p.beta;
         const bool relu = p.relu != 0;
+        // C, D and the peers' partial tiles are each touched once here: let L2
+        // evict them before the A and B tiles that other CTAs still read
+        const uint64_t pol_once = l2_policy_evict_first();
         constexpr int NCH = TR::NCH;
         constexpr bool WHOLE = TR::EPI_WHOLE;  // one staging box per chunk of the tile
         // Stream-K partial tiles are stored in groups of four columns: float4
@@ -657,7 +662,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (stage_c) {
                     for (int c = 0; c < nch; ++c) {
                         mbar_arrive_expect_tx(c_bar(e, c), EPI_BUF_BYTES);
-                        tma_load_2d(ebuf0 + c * EPI_BUF_BYTES, tC, c_bar(e, c), n0 + c * EPI_COLS, row0);
+                        tma_load_2d_hint(ebuf0 + c * EPI_BUF_BYTES, tC, c_bar(e, c), n0 + c * EPI_COLS, row0, pol_once);
                         c_pending |= 1u << c;
                     }
                 }
@@ -666,7 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t b = n_chunk & 1u;
                 bulk_wait_read<1>();
                 mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
-                tma_load_2d(ebuf0 + b * EPI_BUF_BYTES, tC, c_bar(e, b), n0, row0);
+                tma_load_2d_hint(ebuf0 + b * EPI_BUF_BYTES, tC, c_bar(e, b), n0, row0, pol_once);
                 c_pending |= 1u << b;
                 for (int c = 1; c < nch; ++c) tma_prefetch_l2_2d(tC, n0 + c * EPI_COLS, row0);
             }
@@ -722,8 +727,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (c + 1 < nch && lane == 0) {
                         bulk_wait_read<0>();
                         mbar_arrive_expect_tx(c_bar(e, b ^ 1u), EPI_BUF_BYTES);
-                        tma_load_2d(ebuf0 + (b ^ 1u) * EPI_BUF_BYTES, tC, c_bar(e, b ^ 1u),
-                                    n0 + col0 + EPI_COLS, row0);
+                        tma_load_2d_hint(ebuf0 + (b ^ 1u) * EPI_BUF_BYTES, tC, c_bar(e, b ^ 1u),
+                                         n0 + col0 + EPI_COLS, row0, pol_once);
                         c_pending |= 1u << (b ^ 1u);
                     }
                     __syncwarp();
@@ -750,7 +755,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const float4* src = peer_src(pb, col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float4 t = __ldcg(src + 32 * i);
+                            const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
                             v[4 * i + 0] += t.x;
                             v[4 * i + 1] += t.y;
                             v[4 * i + 2] += t.z;
@@ -791,40 +796,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 OutT* drow = Dptr + static_cast<int64_t>(my_row) * ldd + n0 + col0;
                 // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane % 8)
                 auto slot_of = [&](int j) { return buf + lane * 128 + ((j ^ (lane & 7)) << 4); };
-                // all eight C loads first: each store below writes the box they read
-                uint4 cvs[8];
-                if (stage_c) {
+                // alpha * acc (+ beta * C) (ReLU) -> 16-bit pairs; the C and ReLU
+                // variants are separate straight-line code (no branch between the
+                // eight groups), and all eight C loads come before any store
+                uint32_t pk[8][4];
+                auto convert = [&](auto has_c, auto has_relu) {
+                    uint4 cvs[8];
+                    if constexpr (decltype(has_c)::value) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) cvs[j] = ld_shared_v4(slot_of(j));
-                }
+                        for (int j = 0; j < 8; ++j) cvs[j] = ld_shared_v4(slot_of(j));
+                    }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t slot = slot_of(j);
-                    float o[8];
+                    for (int j = 0; j < 8; ++j) {
+                        float o[8];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) o[t] = alpha * v[8 * j + t];
-                    if (stage_c) {
-                        const uint32_t cw[4] = {cvs[j].x, cvs[j].y, cvs[j].z, cvs[j].w};
+                        for (int t = 0; t < 8; ++t) o[t] = alpha * v[8 * j + t];
+                        if constexpr (decltype(has_c)::value) {
+                            const uint32_t cw[4] = {cvs[j].x, cvs[j].y, cvs[j].z, cvs[j].w};
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const float2 f = unpack2<ELEM>(cw[t]);
-                            o[2 * t] = fmaf(beta, f.x, o[2 * t]);
-                            o[2 * t + 1] = fmaf(beta, f.y, o[2 * t + 1]);
+                            for (int t = 0; t < 4; ++t) {
+                                const float2 f = unpack2<ELEM>(cw[t]);
+                                o[2 * t] = fmaf(beta, f.x, o[2 * t]);
+                                o[2 * t + 1] = fmaf(beta, f.y, o[2 * t + 1]);
+                            }
                         }
-                    }
-                    if (relu) {
+                        if constexpr (decltype(has_relu)::value) {
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) o[t] = relu_nan(o[t]);
+                            for (int t = 0; t < 8; ++t) o[t] = relu_nan(o[t]);
+                        }
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) pk[j][t] = pack2<ELEM>(o[2 * t], o[2 * t + 1]);
                     }
-                    if (!ragged) {
-                        st_shared_v4(slot, pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
-                                     pack2<ELEM>(o[4], o[5]), pack2<ELEM>(o[6], o[7]));
-                    } else if (my_row < M) {
+                };
+                if (stage_c) {
+                    if (relu) convert(std::true_type{}, std::true_type{});
+                    else convert(std::true_type{}, std::false_type{});
+                } else {
+                    if (relu) convert(std::false_type{}, std::true_type{});
+                    else convert(std::false_type{}, std::false_type{});
+                }
+                if (!ragged) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) st_shared_v4(slot_of(j), pk[j][0], pk[j][1], pk[j][2], pk[j][3]);
+                } else if (my_row < M) {
+                    // the rounded values are stored element-wise from their 16-bit pairs
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
 #pragma unroll
                         for (int t = 0; t < 8; ++t) {
                             if (8 * j + t < left) {
-                                if constexpr (ELEM == ELEM_F16) drow[8 * j + t] = __float2half_rn(o[t]);
-                                else drow[8 * j + t] = __float2bfloat16_rn(o[t]);
+                                const uint16_t h = static_cast<uint16_t>(pk[j][t >> 1] >> (16 * (t & 1)));
+                                reinterpret_cast<uint16_t*>(drow)[8 * j + t] = h;
                             }
                         }
                     }
@@ -833,7 +855,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     fence_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(tD, buf, n0 + col0, row0);
+                        tma_store_2d_hint(tD, buf, n0 + col0, row0, pol_once);
                         bulk_commit();
                     }
                     ++n_chunk;  // only chunks that stored from their buffer flip it

@@ -108,7 +108,6 @@ __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
                  : "memory");
 }
 
-// 2-D tiled load into this CTA's shared memory, completion on `bar`.
 // Prefetch of one tensor-map box into L2 (no shared memory, no completion signal).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -117,6 +116,7 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, 
                  : "memory");
 }
 
+// 2-D tiled load into this CTA's shared memory, completion on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar,
                                             int32_t x, int32_t y) {
     asm volatile(
@@ -136,6 +136,43 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// L2 cache policy that evicts the lines it touches first (data used once).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// TMA tile load / store with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src, int32_t x,
+                                                  int32_t y, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
+// 16-byte global load that bypasses L1, with an L2 cache policy (kept after
+// the barrier that orders it behind the producer's release).
+__device__ __forceinline__ float4 ld_global_cg_hint(const float4* p, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(pol)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x,
