@@ -331,6 +331,12 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
     return false;
 }
 
+// True when the item sched_next returned last was a unit's final stream-K
+// item (nothing follows it in this unit).
+__device__ __forceinline__ bool sched_sk_last(const SchedState& s) {
+    return s.phase == 1 && s.step == 2 && s.u >= s.o_begin;
+}
+
 // ------------------------------------------------------------------ tracing
 
 __device__ __forceinline__ uint64_t* trace_rec(const GemmParams& p, int32_t item) {
@@ -677,19 +683,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             __syncwarp();  // lane 0's wait for the stores orders the warp's writes to the boxes
 
-            if (!wait_bar(ctl, accf_bar(ab), aph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint64_t* tr = (threadIdx.x == 64) ? trace_rec(p, static_cast<int32_t>(n_acc)) : nullptr;
-            if (tr) {
-                tr[0] = static_cast<uint32_t>(w.tile) | (static_cast<uint64_t>(w.kind) << 32);
-                tr[1] = static_cast<uint32_t>(w.kb0) | (static_cast<uint64_t>(w.kb1) << 32);
-                tr[4] = globaltimer_ns();
-                tr[7] = 0;
-            }
-
             // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
                 if (threadIdx.x == 64) {
@@ -711,6 +704,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!epi_sync() || *abort_flag) ok = false;
+            }
+
+            // A stream-K owner item that ends its unit leaves the other TMEM
+            // accumulator idle (the MMA warp has no further item): the sum of
+            // the peers' partial tiles is loaded into it while this item's
+            // mainloop still runs, so the fix-up reads TMEM instead of L2.
+            const int64_t pb0 = w.kind == WK_OWNER ? next_peer(un.id + 1, tile_end_unit) : -1;
+            const bool preload = pb0 >= 0 && sched_sk_last(st) && ok;
+            if (preload && rows_live) {
+                // 32 columns at a time: the first peer's values, plus any further peers'
+                for (int h = 0; h < 2 * nch; ++h) {
+                    const int32_t col0 = (h >> 1) * EPI_COLS;
+                    const int i0 = (h & 1) * 8;  // float4 groups of this half of the chunk
+                    uint32_t r[32];
+                    const float4* src0 = peer_src(pb0, col0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 t = ld_global_cg_hint(src0 + 32 * (i0 + i), pol_once);
+                        r[4 * i + 0] = __float_as_uint(t.x);
+                        r[4 * i + 1] = __float_as_uint(t.y);
+                        r[4 * i + 2] = __float_as_uint(t.z);
+                        r[4 * i + 3] = __float_as_uint(t.w);
+                    }
+                    for (int64_t pb = next_peer(pb0 + 1, tile_end_unit); pb >= 0;
+                         pb = next_peer(pb + 1, tile_end_unit)) {
+                        const float4* src = peer_src(pb, col0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 t = ld_global_cg_hint(src + 32 * (i0 + i), pol_once);
+                            r[4 * i + 0] = __float_as_uint(__uint_as_float(r[4 * i + 0]) + t.x);
+                            r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + t.y);
+                            r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + t.z);
+                            r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + t.w);
+                        }
+                    }
+                    tmem_st32(tmem_base + lane_base + (ab ^ 1u) * BN + col0 + (h & 1) * 32, r);
+                }
+                tmem_st_wait();
+            }
+
+            if (!wait_bar(ctl, accf_bar(ab), aph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint64_t* tr = (threadIdx.x == 64) ? trace_rec(p, static_cast<int32_t>(n_acc)) : nullptr;
+            if (tr) {
+                tr[0] = static_cast<uint32_t>(w.tile) | (static_cast<uint64_t>(w.kind) << 32);
+                tr[1] = static_cast<uint32_t>(w.kb0) | (static_cast<uint64_t>(w.kb1) << 32);
+                tr[4] = globaltimer_ns();
+                tr[7] = 0;
             }
 
             if (tr) tr[5] = globaltimer_ns();
@@ -748,7 +792,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     v[i] = __uint_as_float(r[0][i]);
                     v[32 + i] = __uint_as_float(r[1][i]);
                 }
-                if (w.kind == WK_OWNER) {
+                if (preload) {
+                    // the peers' sum, staged in the idle accumulator
+                    const uint32_t paddr = tmem_base + lane_base + (ab ^ 1u) * BN + col0;
+                    tmem_ld32(paddr, r[0]);
+                    tmem_ld32(paddr + 32, r[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] += __uint_as_float(r[0][i]);
+                        v[32 + i] += __uint_as_float(r[1][i]);
+                    }
+                } else if (w.kind == WK_OWNER) {
                     // add the peer units' partial tiles in unit order (deterministic)
                     for (int64_t pb = next_peer(un.id + 1, tile_end_unit); pb >= 0;
                          pb = next_peer(pb + 1, tile_end_unit)) {

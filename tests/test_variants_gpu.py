@@ -376,6 +376,25 @@ def test_stream_k_takes_peer_then_owner_then_whole_tiles(cg, grid):
     assert seen == ["OF", "PF", "OF", "PF"]
 
 
+@pytest.mark.parametrize("cg,units,N", [(1, 4, 200), (2, 4, 200), (1, 3, 392), (2, 3, 392)])
+def test_stream_k_owner_that_ends_its_unit(cg, units, N):
+    """Owner pieces that are the last item of their unit stage the peers'
+    partial sum in the idle TMEM accumulator: one tile over four units (three
+    peers) and two tiles over three units (one peer each)."""
+    prob = inputs.random_problem(128 * cg - 8, N, 4096, beta=0.5, alpha=1.5, relu=True)
+    plan = plan_for(prob, schedule=g.SCHED_SK, cta_group=cg, grid=units * cg, tile_n=256,
+                    trace_items=4)
+    d = run_gpu(plan, prob)
+    assert_matches_oracle(prob, d)
+    assert np.array_equal(d, run_gpu(plan, prob)), "stream-K fix-up is not deterministic"
+    cfg = plan.last_config()
+    assert cfg["grid"] == units * cg and cfg["schedule"] == g.SCHED_SK
+    tr = g.gemm_plan_trace(plan.handle)
+    kinds = ["".join("FPOS"[int(rec[0] >> 32)] for rec in tr[u * cg, 1:] if rec[4] != 0)
+             for u in range(units)]
+    assert kinds == (["O", "P", "P", "P"] if units == 4 else ["O", "PO", "P"]), kinds
+
+
 @pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
 @pytest.mark.parametrize("dtype,a_col,b_col", [("f16", False, False), ("bf16", True, False),
                                                ("f16", False, True), ("bf16", True, True)])
