@@ -290,8 +290,9 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
         if (d.dp_tiles >= d.tiles) d.dp_tiles = d.tiles - 1;
         d.sk_units = static_cast<int64_t>(d.tiles - d.dp_tiles) * d.k_blocks;
         units = static_cast<int>(std::min<int64_t>(G, d.sk_units));
-        d.ws_bytes = static_cast<size_t>(units) * cg * half_tile;
-        d.flags = units * cg;
+        // per unit and CTA: a tail piece and a head piece may each leave a partial tile
+        d.ws_bytes = static_cast<size_t>(2 * units) * cg * half_tile;
+        d.flags = 2 * units * cg;
     } else {
         int splits = o.splits > 0 ? o.splits : std::max(1, G / std::max<int32_t>(d.tiles, 1));
         splits = static_cast<int>(std::min<int64_t>(splits, d.k_blocks));

@@ -178,8 +178,11 @@ struct Work {
     int32_t m_blk, n_blk;
     int32_t kb0, kb1;
     int32_t kind;      // WK_*
-    int32_t slot;      // workspace slot for partial tiles (128-row halves)
+    int32_t slot;      // workspace slot (and flag) of a partial tile (128-row halves)
+    int32_t h0, h1;    // stream-K: first and last unit holding a piece of this tile
 };
+// A stream-K tile split across units has one owner, the unit expected to
+// finish its piece last, which adds the others' partial tiles (peers).
 enum : int32_t { WK_FULL = 0, WK_PEER = 1, WK_OWNER = 2, WK_SPLIT = 3 };
 
 // Scheduling works on "units": one CTA (CG = 1) or one SM pair (CG = 2).
@@ -188,23 +191,48 @@ struct Unit {
 };
 
 // A stream-K unit's range [u0, u_end) of (tile, k-block) iterations holds at
-// most one peer piece (its start, inside a tile), whole tiles, and at most one
-// owner piece (its end: the k = 0 head of a tile).  The pieces are taken in the
-// order peer, owner, whole tiles: the peer piece first because an earlier
-// unit's owner waits for it, the owner piece before the whole tiles so that
-// its wait for later units' peer pieces and its longer fix-up epilogue overlap
-// the whole tiles' mainloop instead of trailing it.
+// most one tail piece (its start, inside a tile), whole tiles, and at most one
+// head piece (its end: the k = 0 head of a tile).  The pieces are taken in the
+// order tail, head, whole tiles, so that pieces of split tiles finish early
+// and their fix-up overlaps the whole tiles' mainloop instead of trailing it.
 struct SchedState {
     int32_t i;          // data-parallel / split item counter
     int32_t phase;      // 0 data-parallel, 1 stream-K, 2 done
-    int32_t step;       // stream-K: 0 peer piece, 1 owner piece, 2 whole tiles
+    int32_t step;       // stream-K: 0 tail piece, 1 head piece, 2 whole tiles
     int64_t u0, u_end;  // stream-K range of this unit
-    int64_t u;          // stream-K: end of the peer piece, then cursor over whole tiles
-    int64_t o_begin;    // stream-K: start of the owner piece (u_end if none)
+    int64_t u;          // stream-K: end of the tail piece, then cursor over whole tiles
+    int64_t o_begin;    // stream-K: start of the head piece (u_end if none)
 };
 
 __device__ __forceinline__ int64_t sk_begin(const GemmParams& p, const Unit& un, int64_t unit) {
     return (p.sk_units * unit) / un.count;
+}
+
+// The unit whose range holds stream-K iteration x.
+__device__ __forceinline__ int32_t sk_unit_of(const GemmParams& p, const Unit& un, int64_t x) {
+    int64_t u = (x * un.count) / p.sk_units;  // sk_begin(u) <= x up to rounding
+    while (u > 0 && sk_begin(p, un, u) > x) --u;
+    while (u + 1 < un.count && sk_begin(p, un, u + 1) <= x) ++u;
+    return static_cast<int32_t>(u);
+}
+
+// Iterations unit v runs before its piece of the tile [t0, t0 + k_blocks) is
+// done, in its piece order (tail piece, head piece, whole tiles): the piece's
+// length, plus the unit's leading piece when this piece is the tile's head
+// and the unit's range starts inside an earlier tile.
+__device__ __forceinline__ int64_t sk_piece_finish(const GemmParams& p, const Unit& un, int32_t v,
+                                                   int64_t t0) {
+    const int64_t kb = p.k_blocks;
+    const int64_t b = sk_begin(p, un, v), e = sk_begin(p, un, v + 1);
+    const int64_t len = min(e, t0 + kb) - max(b, t0);
+    if (b >= t0 || b % kb == 0) return len;
+    return (min(e, (b / kb + 1) * kb) - b) + len;
+}
+
+// Workspace slot / flag of unit v's partial tile: each unit holds at most a
+// tail piece (slot 2v) and a head piece (slot 2v + 1) of split tiles.
+__device__ __forceinline__ int32_t sk_slot(const Unit& un, int32_t v, bool head) {
+    return (2 * v + (head ? 1 : 0)) * un.cg + un.rank;
 }
 
 __device__ __forceinline__ void raster_coords(int32_t tile, int32_t m_blocks, int32_t n_blocks,
@@ -227,9 +255,9 @@ __device__ __forceinline__ void sched_init(const GemmParams& p, const Unit& un, 
         const int64_t kb = p.k_blocks;
         s.u0 = sk_begin(p, un, un.id);
         s.u_end = sk_begin(p, un, un.id + 1);
-        // end of the peer piece (u0 itself when the range starts on a tile)
+        // end of the tail piece (u0 itself when the range starts on a tile)
         s.u = (s.u0 % kb) ? min(s.u_end, (s.u0 / kb + 1) * kb) : s.u0;
-        // start of the owner piece (u_end when the range ends on a tile)
+        // start of the head piece (u_end when the range ends on a tile)
         const int64_t last_tile = (s.u_end / kb) * kb;
         s.o_begin = (s.u_end % kb && last_tile >= s.u) ? last_tile : s.u_end;
     }
@@ -267,6 +295,7 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
         w.kb0 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * sp) / p.splits);
         w.kb1 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (sp + 1)) / p.splits);
         w.kind = WK_SPLIT;
+        w.h0 = w.h1 = un.id;
         // slots are indexed by 128-row block so the reduction sees one layout
         w.slot = ((w.m_blk * un.cg + un.rank) * p.n_blocks + w.n_blk) * p.splits + sp;
         return true;
@@ -282,6 +311,7 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
             fill_coords(p, w);
             w.kind = WK_FULL;
             w.slot = 0;
+            w.h0 = w.h1 = un.id;
             return true;
         }
         s.phase = (p.sched == SCHED_SK) ? 1 : 2;
@@ -318,23 +348,35 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
         fill_coords(p, w);
         w.kb0 = static_cast<int32_t>(b0 - tile_u0);
         w.kb1 = static_cast<int32_t>(b1 - tile_u0);
+        w.slot = sk_slot(un, un.id, w.kb0 == 0);
+        w.h0 = w.h1 = un.id;
         if (w.kb0 == 0 && w.kb1 == kb) {
             w.kind = WK_FULL;
-        } else if (w.kb0 == 0) {
-            w.kind = WK_OWNER;
         } else {
-            w.kind = WK_PEER;
+            // owner: the holder with the latest expected finish (lowest unit on ties)
+            w.h0 = sk_unit_of(p, un, tile_u0);
+            w.h1 = sk_unit_of(p, un, tile_u0 + kb - 1);
+            int32_t owner = w.h0;
+            int64_t best = -1;
+            for (int32_t v = w.h0; v <= w.h1; ++v) {
+                const int64_t f = sk_piece_finish(p, un, v, tile_u0);
+                if (f > best) {
+                    best = f;
+                    owner = v;
+                }
+            }
+            w.kind = owner == un.id ? WK_OWNER : WK_PEER;
         }
-        w.slot = un.id * un.cg + un.rank;
         return true;
     }
     return false;
 }
 
 // True when the item sched_next returned last was a unit's final stream-K
-// item (nothing follows it in this unit).
+// item (nothing follows it in this unit): no head piece still to come (it
+// has been taken, or there is none) and no whole tile left.
 __device__ __forceinline__ bool sched_sk_last(const SchedState& s) {
-    return s.phase == 1 && s.step == 2 && s.u >= s.o_begin;
+    return s.phase == 1 && (s.step == 2 || s.o_begin >= s.u_end) && s.u >= s.o_begin;
 }
 
 // ------------------------------------------------------------------ tracing
@@ -591,17 +633,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         auto peer_off = [&](int32_t col0) -> size_t {
             return (static_cast<size_t>(q) * (BN / 4) + col0 / 4) * 32 + lane;
         };
-        // this thread's first float4 of chunk col0 in unit pb's partial tile
-        auto peer_src = [&](int64_t pb, int32_t col0) -> const float4* {
-            return reinterpret_cast<const float4*>(p.ws + static_cast<size_t>(pb * CG + un.rank) * TILE_M * BN) +
+        // this thread's first float4 of chunk col0 in peer unit v's partial tile
+        // of the tile held by units [w.h0, w.h1] (h0 holds its head)
+        auto peer_src = [&](const Work& w, int32_t v, int32_t col0) -> const float4* {
+            const int32_t slot = sk_slot(un, v, v == w.h0);
+            return reinterpret_cast<const float4*>(p.ws + static_cast<size_t>(slot) * TILE_M * BN) +
                    peer_off(col0);
         };
-        // the first unit >= pb that holds part of the tile ending at unit
-        // iteration tile_end (a peer of its owner), or -1
-        auto next_peer = [&](int64_t pb, int64_t tile_end) -> int64_t {
-            for (; pb < un.count && sk_begin(p, un, pb) < tile_end; ++pb)
-                if (sk_begin(p, un, pb) != sk_begin(p, un, pb + 1)) return pb;
-            return -1;
+        // the first peer >= v of the tile held by units [w.h0, w.h1], or -1
+        auto next_peer = [&](const Work& w, int32_t v) -> int32_t {
+            if (v == un.id) ++v;
+            return v <= w.h1 ? v : -1;
         };
 
         // Bounded barrier of the four epilogue warps (mbarrier with count 4):
@@ -624,7 +666,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t c_pending = 0;    // C loads issued and not yet waited for
         int last_group = -1;
         bool ok = true;
-        const int32_t my_slot_unit = un.id * CG + un.rank;
         while (ok && sched_next(p, un, st, w)) {
             const uint32_t ab = n_acc & 1u;
             const uint32_t aph = (n_acc >> 1) & 1u;
@@ -654,8 +695,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int32_t n0 = w.n_blk * BN;
             const int32_t row0 = m0 + q * 32;      // first row of this warp
             const bool rows_live = row0 < M;
-            const int64_t tile_end_unit =
-                (static_cast<int64_t>(w.tile - p.dp_tiles) + 1) * p.k_blocks;
             const bool to_ws = (w.kind == WK_PEER || w.kind == WK_SPLIT);
             const bool stage_c = has_c && !to_ws && rows_live;
             const int nch = min(NCH, (N - n0 + EPI_COLS - 1) / EPI_COLS);
@@ -686,9 +725,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
                 if (threadIdx.x == 64) {
-                    for (int64_t b = next_peer(un.id + 1, tile_end_unit); b >= 0;
-                         b = next_peer(b + 1, tile_end_unit)) {
-                        const uint32_t* flag = p.flags + b * CG + un.rank;
+                    for (int32_t v = next_peer(w, w.h0); v >= 0; v = next_peer(w, v + 1)) {
+                        const uint32_t* flag = p.flags + sk_slot(un, v, v == w.h0);
                         const uint64_t t0 = globaltimer_ns();
                         uint32_t it = 0;
                         while (ld_acquire_gpu(flag) != p.epoch) {
@@ -710,36 +748,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // accumulator idle (the MMA warp has no further item): the sum of
             // the peers' partial tiles is loaded into it while this item's
             // mainloop still runs, so the fix-up reads TMEM instead of L2.
-            const int64_t pb0 = w.kind == WK_OWNER ? next_peer(un.id + 1, tile_end_unit) : -1;
+            const int32_t pb0 = w.kind == WK_OWNER ? next_peer(w, w.h0) : -1;
             const bool preload = pb0 >= 0 && sched_sk_last(st) && ok;
             if (preload && rows_live) {
-                // 32 columns at a time: the first peer's values, plus any further peers'
-                for (int h = 0; h < 2 * nch; ++h) {
-                    const int32_t col0 = (h >> 1) * EPI_COLS;
-                    const int i0 = (h & 1) * 8;  // float4 groups of this half of the chunk
-                    uint32_t r[32];
-                    const float4* src0 = peer_src(pb0, col0);
+                // two chunks of the first peer in flight: chunk c + 1 is requested
+                // before chunk c is summed and written to TMEM
+                float4 ps[2][16];
+                auto request = [&](float4 (&dst)[16], int c) {
+                    const float4* src0 = peer_src(w, pb0, c * EPI_COLS);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 t = ld_global_cg_hint(src0 + 32 * (i0 + i), pol_once);
-                        r[4 * i + 0] = __float_as_uint(t.x);
-                        r[4 * i + 1] = __float_as_uint(t.y);
-                        r[4 * i + 2] = __float_as_uint(t.z);
-                        r[4 * i + 3] = __float_as_uint(t.w);
-                    }
-                    for (int64_t pb = next_peer(pb0 + 1, tile_end_unit); pb >= 0;
-                         pb = next_peer(pb + 1, tile_end_unit)) {
-                        const float4* src = peer_src(pb, col0);
+                    for (int i = 0; i < 16; ++i) dst[i] = ld_global_cg_hint(src0 + 32 * i, pol_once);
+                };
+                auto finish = [&](float4 (&cur)[16], int c) {
+                    const int32_t col0 = c * EPI_COLS;
+                    for (int32_t pb = next_peer(w, pb0 + 1); pb >= 0; pb = next_peer(w, pb + 1)) {
+                        const float4* src = peer_src(w, pb, col0);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 t = ld_global_cg_hint(src + 32 * (i0 + i), pol_once);
-                            r[4 * i + 0] = __float_as_uint(__uint_as_float(r[4 * i + 0]) + t.x);
-                            r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + t.y);
-                            r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + t.z);
-                            r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + t.w);
+                        for (int i = 0; i < 16; ++i) {
+                            const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
+                            cur[i].x += t.x;
+                            cur[i].y += t.y;
+                            cur[i].z += t.z;
+                            cur[i].w += t.w;
                         }
                     }
-                    tmem_st32(tmem_base + lane_base + (ab ^ 1u) * BN + col0 + (h & 1) * 32, r);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r[32];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            r[4 * i + 0] = __float_as_uint(cur[8 * h + i].x);
+                            r[4 * i + 1] = __float_as_uint(cur[8 * h + i].y);
+                            r[4 * i + 2] = __float_as_uint(cur[8 * h + i].z);
+                            r[4 * i + 3] = __float_as_uint(cur[8 * h + i].w);
+                        }
+                        tmem_st32(tmem_base + lane_base + (ab ^ 1u) * BN + col0 + h * 32, r);
+                    }
+                };
+                request(ps[0], 0);
+                for (int c = 0; c < nch; c += 2) {
+                    if (c + 1 < nch) request(ps[1], c + 1);
+                    finish(ps[0], c);
+                    if (c + 1 < nch) {
+                        if (c + 2 < nch) request(ps[0], c + 2);
+                        finish(ps[1], c + 1);
+                    }
                 }
                 tmem_st_wait();
             }
@@ -805,9 +858,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else if (w.kind == WK_OWNER) {
                     // add the peer units' partial tiles in unit order (deterministic)
-                    for (int64_t pb = next_peer(un.id + 1, tile_end_unit); pb >= 0;
-                         pb = next_peer(pb + 1, tile_end_unit)) {
-                        const float4* src = peer_src(pb, col0);
+                    for (int32_t pb = next_peer(w, w.h0); pb >= 0; pb = next_peer(w, pb + 1)) {
+                        const float4* src = peer_src(w, pb, col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
@@ -934,7 +986,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool synced = epi_sync();
                 if (threadIdx.x == 64 && ok && synced && !*abort_flag &&
                     p.fault_skip_flag != un.id) {
-                    st_release_gpu(p.flags + my_slot_unit, p.epoch);
+                    st_release_gpu(p.flags + w.slot, p.epoch);
                     if (tr) tr[7] = globaltimer_ns();
                 }
                 if (!synced) ok = false;

@@ -356,11 +356,25 @@ def test_timeline_trace_covers_every_k_block_once():
         assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
 
 
+def _sk_items(tr, cta, k_blocks):
+    """(piece positions, kinds) of one CTA's traced items: T a tile's tail
+    (k0 > 0), H its head (k0 = 0, ends inside), F whole; P a peer, O the owner."""
+    pos, kinds = "", ""
+    for rec in tr[cta, 1:]:
+        if rec[4] == 0:
+            continue
+        kb0, kb1 = int(rec[1] & 0xffffffff), int(rec[1] >> 32)
+        pos += "T" if kb0 > 0 else ("F" if kb1 == k_blocks else "H")
+        kinds += "FPOS"[int(rec[0] >> 32)]
+    return pos, kinds
+
+
 @pytest.mark.parametrize("cg,grid", [(1, 4), (2, 8)])
-def test_stream_k_takes_peer_then_owner_then_whole_tiles(cg, grid):
+def test_stream_k_takes_tail_then_head_then_whole_tiles(cg, grid):
     """Four units over six tiles of 64 k-blocks: 96 k-blocks each, so every
-    unit holds a whole tile and a peer or an owner piece; each unit runs its
-    peer piece, then its owner piece, then its whole tiles."""
+    unit holds a whole tile and a tail or a head piece; each unit runs its
+    tail piece, then its head piece, then its whole tiles.  Head and tail of a
+    split tile finish together here, and the lower unit owns the tile."""
     m = 128 * cg
     prob = inputs.random_problem(2 * m, 768, 4096, beta=1.0, relu=True)
     plan = plan_for(prob, schedule=g.SCHED_SK, cta_group=cg, grid=grid, trace_items=8)
@@ -368,12 +382,27 @@ def test_stream_k_takes_peer_then_owner_then_whole_tiles(cg, grid):
     cfg = plan.last_config()
     assert cfg["grid"] == grid and cfg["tiles"] == 6
     tr = g.gemm_plan_trace(plan.handle)
-    seen = []
-    for cta in range(0, grid, cg):
-        kinds = "".join("FPOS"[int(rec[0] >> 32)] for rec in tr[cta, 1:] if rec[4] != 0)
-        assert re.fullmatch(r"P?O?F*", kinds), kinds
-        seen.append(kinds)
-    assert seen == ["OF", "PF", "OF", "PF"]
+    items = [_sk_items(tr, cta, 64) for cta in range(0, grid, cg)]
+    assert all(re.fullmatch(r"T?H?F*", pos) for pos, _ in items), items
+    assert items == [("HF", "OF"), ("TF", "PF"), ("HF", "OF"), ("TF", "PF")]
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+def test_stream_k_owner_is_the_holder_that_finishes_last(cg):
+    """Three tiles over five units (ranges 0/38/76/115/153/192 of 64-k-block
+    tiles): tile 1 is held by units 1 (head, 12 k-blocks after a 26-k-block
+    tail), 2 (39, its only piece) and 3 (13); tile 2 by units 3 (head, 25 after
+    13) and 4 (39).  Units 2 and 4 finish last and own tiles 1 and 2 although
+    they hold no head piece; units 1 and 3 each publish two partial tiles."""
+    prob = inputs.random_problem(128 * cg, 768, 4096, beta=0.5, alpha=-1.25, relu=False)
+    plan = plan_for(prob, schedule=g.SCHED_SK, cta_group=cg, grid=5 * cg, tile_n=256,
+                    trace_items=4)
+    d = run_gpu(plan, prob)
+    assert_matches_oracle(prob, d)
+    assert np.array_equal(d, run_gpu(plan, prob)), "stream-K fix-up is not deterministic"
+    tr = g.gemm_plan_trace(plan.handle)
+    items = [_sk_items(tr, u * cg, 64) for u in range(5)]
+    assert items == [("H", "O"), ("TH", "PP"), ("T", "O"), ("TH", "PP"), ("T", "O")], items
 
 
 @pytest.mark.parametrize("cg,units,N", [(1, 4, 200), (2, 4, 200), (1, 3, 392), (2, 3, 392)])
