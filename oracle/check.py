@@ -3,13 +3,17 @@
 Tolerance for fp16 / bf16 output (element by element):
 
     |D - D_ref| <= 1e-2 * |alpha| * s_a * s_b * (|A| . |B|)_ij + 1e-3
-                   + u * |beta * C_ij|
+                   + u * (|beta * C_ij| + |bias_j|)
+                   [+ u * |D_ref_ij| for sigmoid and tanh]
 
 with u = 2^-10 for fp16 and 2^-7 for bf16 output.  The first two terms are the
 stated bound of the method's accuracy target; |alpha| and s_a*s_b scale it
 with the product term it bounds (for alpha = s = 1 it is the literal bound),
-and the last term covers the one rounding of the beta*C contribution to the
-output type.  ReLU is 1-Lipschitz, so the same bound holds after it.
+and the u terms cover the one rounding of the result to the output type
+where the relative term does not: the beta*C and bias contributions, and the
+value of a bounded activation (sigmoid, tanh), which need not be small where
+|A|.|B| is.  ReLU, sigmoid (1/4) and tanh are 1-Lipschitz, so the bound on the
+linear combination holds after them.
 """
 from __future__ import annotations
 
@@ -21,11 +25,19 @@ ROUND_UNIT = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}
 
 
 def bound(absab: np.ndarray, alpha: float, beta: float, c64, out_dtype: str,
-          scale=1.0) -> np.ndarray:
+          scale=1.0, bias64=None, d_ref=None) -> np.ndarray:
     b = 1e-2 * abs(alpha) * scale * absab + 1e-3
     if beta != 0.0 and c64 is not None:
         b = b + ROUND_UNIT[out_dtype] * np.abs(beta * c64)
+    if bias64 is not None:
+        b = b + ROUND_UNIT[out_dtype] * np.abs(bias64)[None, :]
+    if d_ref is not None:
+        b = b + ROUND_UNIT[out_dtype] * np.abs(np.nan_to_num(d_ref))
     return b
+
+
+def _act(prob):
+    return getattr(prob, "act", None) or ("relu" if prob.relu else "linear")
 
 
 def reference(prob, bits_of, rows=None, threads=None):
@@ -35,8 +47,10 @@ def reference(prob, bits_of, rows=None, threads=None):
     ``bits``), so this module needs nothing from the CUDA path."""
     a, b = bits_of(prob.A), bits_of(prob.B)
     c = bits_of(prob.C) if prob.C is not None else None
+    bias = getattr(prob, "bias", None)
     d_ref = gemm(a, prob.a_dtype, b, prob.b_dtype, c if prob.beta != 0.0 else None,
-                 prob.c_dtype, alpha=prob.alpha, beta=prob.beta, relu=prob.relu,
+                 prob.c_dtype, alpha=prob.alpha, beta=prob.beta, act=_act(prob),
+                 bias=bits_of(bias) if bias is not None else None, bias_dtype=prob.d_dtype,
                  scale_a=prob.scale_a, scale_b=prob.scale_b,
                  a_col_major=prob.a_col_major, b_col_major=prob.b_col_major,
                  rows=rows, threads=threads)
@@ -50,10 +64,20 @@ def reference(prob, bits_of, rows=None, threads=None):
     return d_ref, absab, c64
 
 
+def _bits16(t):
+    """Stored bits of a 16-bit CPU tensor (without importing the input module)."""
+    import torch
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
 def compare(d_bits: np.ndarray, out_dtype: str, d_ref, absab, c64, prob):
     """Returns (ok, worst ratio |err|/bound, index of worst, count of failures)."""
     d = decode(d_bits, out_dtype)
-    tol = bound(absab, prob.alpha, prob.beta, c64, out_dtype, prob.scale_a * prob.scale_b)
+    bias = getattr(prob, "bias", None)
+    bias64 = decode(bias.view(np.uint16) if isinstance(bias, np.ndarray) else _bits16(bias),
+                    out_dtype) if bias is not None else None
+    tol = bound(absab, prob.alpha, prob.beta, c64, out_dtype, prob.scale_a * prob.scale_b,
+                bias64=bias64, d_ref=d_ref if _act(prob) in ("sigmoid", "tanh") else None)
     err = np.abs(d - d_ref)
     ratio = np.where(np.isfinite(err), err / tol, np.inf)
     # NaN where the reference is NaN too counts as agreement.

@@ -8,7 +8,7 @@
  * What it computes (plain definition, no blocking, no reordering of the sum):
  *
  *     D[i,j] = act( alpha * s_a * s_b * sum_{k=0..K-1} x(A[i,k]) * x(B[k,j])
- *                   + beta * x(C[i,j]) )
+ *                   + beta * x(C[i,j]) + x(bias[j]) )
  *
  *   - "D = A*B + C" for a RowMajor fp16 plan is the worked example of
  *     "Python packages associated with CUTLASS" (CUTLASS python/README.md),
@@ -16,10 +16,14 @@
  *   - alpha and beta are the linear-combination coefficients of the
  *     GemmArguments in the kwkr.cn blog "CUTLASS Python接口", section 3.3
  *     (D = alpha * A * B + beta * C), which also states fp32 accumulation.
- *   - act is identity or ReLU; ReLU is applied to the whole linear
- *     combination, after the beta*C add ("CUTLASS Python 接口全解析" section
- *     2.3 fuses the activation into the epilogue; the kwkr.cn blog section 5.2
- *     applies ReLU to alpha*(A*B) + beta*C + bias).
+ *   - act is identity, ReLU, sigmoid or tanh, applied to the whole sum, after
+ *     the beta*C and bias adds ("CUTLASS Python 接口全解析" section 2.3 fuses the
+ *     activation into the epilogue; the kwkr.cn blog section 5.2 applies ReLU
+ *     to alpha*(A*B) + beta*C + bias, with a bias vector of length N added to
+ *     every row; "Generating State-of-the-Art GEMMs with TorchInductor's
+ *     CuteDSL backend", roadmap section, names ReLU, Sigmoid and Tanh as
+ *     epilogue activations).  sigmoid(v) = 1 / (1 + e^-v); tanh is the C
+ *     library's.  The bias is optional (absent = 0).
  *   - s_a, s_b are per-tensor dequantisation scales of fp8 operands (real value
  *     = s * stored value); they are 1 for 16-bit operands.  FP8 mm support is
  *     listed in "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL
@@ -173,7 +177,8 @@ typedef struct {
     double* D; int64_t ldd;      /* D[(i - row_begin) * ldd + j] */
     int64_t M, N, K;
     double alpha, beta, scale_a, scale_b;
-    int relu;
+    int act;                     /* 0 identity, 1 ReLU, 2 sigmoid, 3 tanh */
+    const void* bias; int bias_dtype;  /* N elements, or NULL */
     int absolute;                /* 1: compute sum |a||b| (error bound), no epilogue */
     int64_t row_begin, row_end;
     const double* Bd;            /* B decoded to double, K x N row-major, or NULL */
@@ -217,7 +222,13 @@ static void oracle_row(const oracle_job* j, int64_t i, double* acc) {
     for (int64_t n = 0; n < j->N; ++n) {
         double v = j->alpha * (j->scale_a * j->scale_b * acc[n]);
         if (j->beta != 0.0) v += j->beta * load_elem(j->C, j->c_dtype, i * j->ldc + n);
-        if (j->relu && v < 0.0) v = 0.0; /* NaN propagates (NaN < 0 is false) */
+        if (j->bias) v += load_elem(j->bias, j->bias_dtype, n);
+        switch (j->act) {
+        case 1: if (v < 0.0) v = 0.0; break; /* NaN propagates (NaN < 0 is false) */
+        case 2: v = 1.0 / (1.0 + exp(-v)); break;
+        case 3: v = tanh(v); break;
+        default: break;
+        }
         out[n] = v;
     }
 }
@@ -246,7 +257,8 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
                 double* D_out, int64_t ldd,
                 int64_t M, int64_t N, int64_t K,
                 double alpha, double beta, double scale_a, double scale_b,
-                int relu, int absolute, int64_t row_begin, int64_t row_end,
+                int act, const void* bias, int bias_dtype,
+                int absolute, int64_t row_begin, int64_t row_end,
                 int nthreads) {
     if (M < 0 || N < 0 || K < 0 || row_begin < 0 || row_end > M || row_begin > row_end)
         return 1;
@@ -259,7 +271,8 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
     j.D = D_out; j.ldd = ldd;
     j.M = M; j.N = N; j.K = K;
     j.alpha = alpha; j.beta = beta; j.scale_a = scale_a; j.scale_b = scale_b;
-    j.relu = relu; j.absolute = absolute;
+    if (act < 0 || act > 3) return 1;
+    j.act = act; j.bias = bias; j.bias_dtype = bias_dtype; j.absolute = absolute;
     j.row_begin = row_begin; j.row_end = row_end; j.next_row = row_begin;
     /* Decode B once (the same exact values load_elem would produce); if the
      * copy does not fit in memory, decode element by element instead. */

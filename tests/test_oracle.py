@@ -262,6 +262,73 @@ def test_planted_mistakes_are_caught():
     assert not _agrees(wrong, exact, mag, p.K)
 
 
+# ---------------------------------------------------------------- bias and activations
+
+def _f16i(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def test_bias_relu_example_exact():
+    """kwkr.cn blog "CUTLASS Python接口" section 5.2: D = relu(A.B + bias), a bias
+    of N elements added to every row, alpha 1, beta 0, at that section's shape
+    M, N, K = 512, 1024, 768.  Small integer operands make every value exact;
+    the expected result is integer numpy arithmetic.  A bias added along rows,
+    or ReLU applied before the bias, would not match."""
+    g = np.random.default_rng(11)
+    M, N, K = 512, 1024, 768
+    A = g.integers(-2, 3, (M, K))
+    B = g.integers(-2, 3, (K, N))
+    bias = g.integers(-60, 61, N)
+    d = oracle.gemm(_f16i(A), "f16", _f16i(B), "f16", act="relu", bias=_f16i(bias))
+    lin = A @ B
+    assert np.array_equal(d, np.maximum(lin + bias[None, :], 0))
+    # the data tell the plausible mistakes apart
+    assert not np.array_equal(d, np.maximum(lin, 0) + bias[None, :])
+    assert not np.array_equal(d[:, :M], np.maximum(lin[:, :M] + bias[:M, None], 0))
+
+
+def test_bias_and_beta_c_are_both_added_before_the_activation():
+    g = np.random.default_rng(12)
+    A, B = g.integers(-3, 4, (7, 5)), g.integers(-3, 4, (5, 9))
+    C, bias = g.integers(-8, 9, (7, 9)), g.integers(-8, 9, 9)
+    d = oracle.gemm(_f16i(A), "f16", _f16i(B), "f16", _f16i(C), "f16", alpha=2.0, beta=-0.5,
+                    act="relu", bias=_f16i(bias))
+    assert np.array_equal(d, np.maximum(2.0 * (A @ B) - 0.5 * C + bias[None, :], 0))
+
+
+def test_sigmoid_and_tanh_of_zero():
+    """A zero product: sigmoid(0) = 1/2 and tanh(0) = 0 exactly."""
+    a = np.zeros((6, 4), np.uint16)
+    b = _rand_f16((4, 10), 13)
+    assert np.array_equal(oracle.gemm(a, "f16", b, "f16", act="sigmoid"), np.full((6, 10), 0.5))
+    assert np.array_equal(oracle.gemm(a, "f16", b, "f16", act="tanh"), np.zeros((6, 10)))
+
+
+def test_sigmoid_and_tanh_match_library_routines():
+    """Against scipy's logistic function and numpy's tanh applied to the
+    oracle's own linear combination (with bias)."""
+    from scipy.special import expit
+    p = inputs.random_problem(24, 40, 32, beta=0.5, lo=-2, hi=2, bias=True)
+    a, b, c, bv = (inputs.bits(t) for t in (p.A, p.B, p.C, p.bias))
+    lin = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=1.5, beta=0.5, bias=bv)
+    sig = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=1.5, beta=0.5, bias=bv, act="sigmoid")
+    th = oracle.gemm(a, "f16", b, "f16", c, "f16", alpha=1.5, beta=0.5, bias=bv, act="tanh")
+    assert np.allclose(sig, expit(lin), rtol=1e-14, atol=1e-15)
+    assert np.allclose(th, np.tanh(lin), rtol=1e-14, atol=1e-15)
+    assert np.all((sig >= 0) & (sig <= 1)) and np.all(np.abs(th) <= 1)
+
+
+def test_tanh_is_twice_sigmoid_of_twice_minus_one():
+    """tanh(x) = 2 sigmoid(2x) - 1 ties the two activations to each other:
+    the same product with alpha doubled."""
+    p = inputs.random_problem(16, 24, 20)
+    a, b = inputs.bits(p.A), inputs.bits(p.B)
+    th = oracle.gemm(a, "f16", b, "f16", alpha=0.75, act="tanh")
+    sig2 = oracle.gemm(a, "f16", b, "f16", alpha=1.5, act="sigmoid")
+    assert np.allclose(th, 2.0 * sig2 - 1.0, rtol=0, atol=1e-14)
+    assert np.allclose(th, -oracle.gemm(a, "f16", b, "f16", alpha=-0.75, act="tanh"), atol=0)
+
+
 # ---------------------------------------------------------------- cross-checks
 
 def test_numpy_float64_cross_check():
