@@ -41,6 +41,11 @@ def workloads():
         "fp16_1024_ones": lambda: [I.config1("a")],
         "fp16_grouped_32": lambda: I.config4(),
         "e4m3_8192": lambda: [I.config5b()],
+        # the bias + ReLU epilogue example of the kwkr.cn blog, section 5.2
+        "fp16_bias_relu_512x1024x768": lambda: [I.random_problem(512, 1024, 768, act="relu",
+                                                                 bias=True)],
+        # batch_count 16 of one shape, packed strides (kwkr.cn blog section 6.3)
+        BATCHED_WORKLOAD: lambda: [I.random_problem(1024, 1024, 1024, seed=b) for b in range(16)],
     }
     for layer in I.LLAMA70B_LAYERS:
         for m in I.LLAMA70B_TOKENS:
@@ -51,20 +56,26 @@ def workloads():
 
 
 DEFAULT_WORKLOAD = "fp16_4096x4096x4096_relu"
+BATCHED_WORKLOAD = "fp16_batched_16x1024x1024x1024"
 
 
 def custom_workload(name):
-    """custom_<f16|bf16|e4m3>_<M>x<N>x<K>[_b<beta>][_relu][_acol][_bcol]: seeded U[-1,1]
-    (N(0,1) for e4m3) operands of any shape, for sweeps and ablations."""
+    """custom_<f16|bf16|e4m3>_<M>x<N>x<K>[_b<beta>][_relu|_sigmoid|_tanh][_bias][_acol][_bcol]:
+    seeded U[-1,1] (N(0,1) for e4m3) operands of any shape, for sweeps and ablations."""
     from dense_gemm_15_gb300 import inputs as I
     parts = name.split("_")
     dtype = parts[1]
     M, N, K = (int(x) for x in parts[2].split("x"))
     beta = 0.0
-    relu = acol = bcol = False
+    relu = acol = bcol = bias = False
+    act = None
     for q in parts[3:]:
         if q == "relu":
             relu = True
+        elif q in ("sigmoid", "tanh"):
+            act = q
+        elif q == "bias":
+            bias = True
         elif q == "acol":
             acol = True
         elif q == "bcol":
@@ -72,7 +83,7 @@ def custom_workload(name):
         elif q.startswith("b"):
             beta = float(q[1:])
     p = I.random_problem(M, N, K, dtype=dtype, beta=beta, relu=relu, alpha=1.0,
-                         a_col_major=acol, b_col_major=bcol)
+                         a_col_major=acol, b_col_major=bcol, act=act, bias=bias)
     p.name = name
     return [p]
 
@@ -127,6 +138,8 @@ def algorithmic_bytes(probs):
         tot += p.M * p.K * ea + p.K * p.N * ea + p.M * p.N * 2
         if p.beta != 0.0:
             tot += p.M * p.N * 2
+        if getattr(p, "bias", None) is not None:
+            tot += p.N * 2
     return tot
 
 
@@ -198,12 +211,13 @@ def cpu_oracle_sample(probs, budget_s=10.0, max_rows=None):
     threads = oracle.default_threads()
     a, b = I.bits(p.A), I.bits(p.B)
     c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
+    bv = I.bits(p.bias) if p.bias is not None else None
 
     def run(rows):
         t0 = time.perf_counter()
         oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
-                    relu=p.relu, scale_a=p.scale_a, scale_b=p.scale_b,
-                    a_col_major=p.a_col_major, b_col_major=p.b_col_major,
+                    act=p.act, bias=bv, bias_dtype=p.d_dtype, scale_a=p.scale_a,
+                    scale_b=p.scale_b, a_col_major=p.a_col_major, b_col_major=p.b_col_major,
                     rows=(0, rows), threads=threads)
         return time.perf_counter() - t0
 
@@ -280,11 +294,12 @@ def run_reference(args):
     rows = int(desc.split("..")[1].split()[0])
     a, b = I.bits(p.A), I.bits(p.B)
     c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
+    bv = I.bits(p.bias) if p.bias is not None else None
 
     def step():
         oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
-                    relu=p.relu, scale_a=p.scale_a, scale_b=p.scale_b,
-                    a_col_major=p.a_col_major, b_col_major=p.b_col_major,
+                    act=p.act, bias=bv, bias_dtype=p.d_dtype, scale_a=p.scale_a,
+                    scale_b=p.scale_b, a_col_major=p.a_col_major, b_col_major=p.b_col_major,
                     rows=(0, rows), threads=cores)
 
     for _ in range(args.warmup):
@@ -320,11 +335,12 @@ def run_gpu(args):
     dist = maybe_init_dist(ws, "nccl")
     dev = torch.device("cuda", local)
     probs = get_workload(args.workload)
+    batched = args.workload == BATCHED_WORKLOAD
     grouped = len(probs) > 1
     p0 = probs[0]
     flops = sum(p.flops for p in probs)
 
-    plan = g.Plan(p0.a_dtype, p0.d_dtype, relu=p0.relu,
+    plan = g.Plan(p0.a_dtype, p0.d_dtype, epilogue=p0.act,
                   layout_a=g.COL_MAJOR if p0.a_col_major else g.ROW_MAJOR,
                   layout_b=g.COL_MAJOR if p0.b_col_major else g.ROW_MAJOR)
     for opt in args.opt or []:
@@ -336,6 +352,7 @@ def run_gpu(args):
         C = p.C.to(dev) if p.C is not None else None
         D = torch.empty(p.M, p.N, dtype=I.TORCH_DTYPE[p.d_dtype], device=dev)
         dv.append((A, B, C, D))
+    bias_dev = p0.bias.to(dev) if p0.bias is not None else None
     scales = None
     if p0.a_dtype == "e4m3":
         scales = (torch.tensor([p0.scale_a], device=dev), torch.tensor([p0.scale_b], device=dev))
@@ -351,15 +368,25 @@ def run_gpu(args):
             # leave the L2 holding clean lines: the written ones are evicted here
             torch.sum(flush_rd, dim=0, out=flush_sink)
     table = [dict(M=p.M, N=p.N, K=p.K, A=A, B=B, C=C, D=D) for p, (A, B, C, D) in zip(probs, dv)]
+    if batched:
+        # one buffer per operand, entries at packed strides
+        bA = torch.stack([A for A, _, _, _ in dv])
+        bB = torch.stack([B for _, B, _, _ in dv])
+        bD = torch.empty(len(probs), p0.M, p0.N, dtype=I.TORCH_DTYPE[p0.d_dtype], device=dev)
+        del dv[1:]
 
     def step():
-        if grouped:
+        if batched:
+            plan.batched(bA, bB, None, bD, p0.M, p0.N, p0.K, len(probs), p0.M * p0.K,
+                         p0.K * p0.N, 0, p0.M * p0.N, alpha=p0.alpha, beta=p0.beta,
+                         stream=stream)
+        elif grouped:
             plan.grouped(table, alpha=p0.alpha, beta=p0.beta, stream=stream)
         else:
             A, B, C, D = dv[0]
             plan.run(A, B, C, D, p0.M, p0.N, p0.K, alpha=p0.alpha, beta=p0.beta,
                      scale_a=scales[0] if scales else None,
-                     scale_b=scales[1] if scales else None, stream=stream)
+                     scale_b=scales[1] if scales else None, stream=stream, bias=bias_dev)
 
     for _ in range(args.warmup):
         l2_flush()
@@ -457,7 +484,8 @@ def run_gpu(args):
             "data": "synthetic",
             "config": {"workload": args.workload, "M": p0.M if not grouped else [p.M for p in probs],
                        "N": p0.N, "K": p0.K, "alpha": p0.alpha, "beta": p0.beta,
-                       "relu": p0.relu, "layout": "row-major A, B, C, D",
+                       "relu": p0.relu, "epilogue": p0.act,
+                       "bias": p0.bias is not None, "layout": "row-major A, B, C, D",
                        "l2": ("flushed between steps (256 MiB write%s, outside the step events)"
                               % (" then 256 MiB read" if args.flush == "write+read" else "")),
                        "parallelism": "replicas" if ws > 1 else "single",

@@ -17,7 +17,8 @@ from . import build as _build
 # enums mirrored from include/gemm15.h
 F16, BF16, F32, E4M3 = 0, 1, 2, 3
 ROW_MAJOR, COL_MAJOR = 0, 1
-EPI_LINEAR, EPI_RELU = 0, 1
+EPI_LINEAR, EPI_RELU, EPI_SIGMOID, EPI_TANH = 0, 1, 2, 3
+EPILOGUES = {"linear": EPI_LINEAR, "relu": EPI_RELU, "sigmoid": EPI_SIGMOID, "tanh": EPI_TANH}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, \
     ERR_DEVICE_FAULT, ERR_NO_DEVICE, ERR_BAD_PLAN = range(10)
 OPT_SCHEDULE, OPT_SPLITS, OPT_CTA_GROUP, OPT_TILE_N, OPT_RASTER, OPT_GRID, \
@@ -30,7 +31,7 @@ EXPORTED = (
     "gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
     "grouped_gemm_run", "gemm_plan_query_error", "gemm15_status_string",
     "gemm_plan_set_option", "gemm_plan_last_config", "gemm_run_splitk_noalloc",
-    "gemm_plan_trace",
+    "gemm_plan_trace", "gemm_run_batched", "gemm_run_args",
 )
 
 
@@ -39,6 +40,15 @@ class PlanDesc(ctypes.Structure):
                 ("d", ctypes.c_int), ("acc", ctypes.c_int), ("layout_a", ctypes.c_int),
                 ("layout_b", ctypes.c_int), ("layout_cd", ctypes.c_int),
                 ("epilogue", ctypes.c_int)]
+
+
+class Args(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("B", ctypes.c_void_p),
+                ("ldb", ctypes.c_int64), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("alpha", ctypes.c_float),
+                ("beta", ctypes.c_float), ("scale_a", ctypes.c_void_p),
+                ("scale_b", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
 
 
 class Problem(ctypes.Structure):
@@ -90,6 +100,9 @@ def load(build_if_missing: bool = True):
                                     f32, f32, vp, vp, vp]
         lib.gemm_run_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, f32, f32, f32, vp]
         lib.grouped_gemm_run.argtypes = [vp, ctypes.POINTER(Problem), i32, f32, f32, vp]
+        lib.gemm_run_args.argtypes = [vp, ctypes.POINTER(Args), vp]
+        lib.gemm_run_batched.argtypes = [vp, vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
+                                         i64, i64, i64, i64, i32, f32, f32, vp]
         lib.gemm_plan_query_error.argtypes = [vp]
         lib.gemm15_status_string.argtypes = [st]
         lib.gemm15_status_string.restype = ctypes.c_char_p
@@ -136,13 +149,18 @@ def _stream(stream):
 # ------------------------------------------------------------------ raw C calls
 
 def gemm_plan_create(a="f16", b=None, c=None, d=None, acc="f32", layout_a=ROW_MAJOR,
-                     layout_b=ROW_MAJOR, layout_cd=ROW_MAJOR, relu=False):
+                     layout_b=ROW_MAJOR, layout_cd=ROW_MAJOR, relu=False, epilogue=None):
+    """epilogue: "linear", "relu", "sigmoid", "tanh" (or its code); default from relu."""
     lib = load()
     b = b or a
     c = c or ("bf16" if a == "e4m3" else a)
     d = d or c
+    if epilogue is None:
+        epi = EPI_RELU if relu else EPI_LINEAR
+    else:
+        epi = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
     desc = PlanDesc(DTYPES[a], DTYPES[b], DTYPES[c], DTYPES[d], DTYPES[acc], layout_a,
-                    layout_b, layout_cd, EPI_RELU if relu else EPI_LINEAR)
+                    layout_b, layout_cd, epi)
     h = ctypes.c_void_p()
     _check(lib.gemm_plan_create(ctypes.byref(h), ctypes.byref(desc)), "gemm_plan_create")
     return h.value
@@ -182,6 +200,20 @@ def grouped_gemm_run(plan, problems, alpha=1.0, beta=0.0, stream=None):
                          _ptr(q["D"]), q.get("lda", 0), q.get("ldb", 0), q.get("ldc", 0),
                          q.get("ldd", 0))
     return load().grouped_gemm_run(plan, arr, len(problems), alpha, beta, _stream(stream))
+
+
+def gemm_run_args(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0, ldd=0,
+                  scale_a=None, scale_b=None, bias=None, stream=None):
+    args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
+                _ptr(scale_a), _ptr(scale_b), _ptr(bias))
+    return load().gemm_run_args(plan, ctypes.byref(args), _stream(stream))
+
+
+def gemm_run_batched(plan, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, D, ldd,
+                     stride_d, M, N, K, batch, alpha=1.0, beta=0.0, stream=None):
+    return load().gemm_run_batched(plan, _ptr(A), lda, stride_a, _ptr(B), ldb, stride_b,
+                                   _ptr(C), ldc, stride_c, _ptr(D), ldd, stride_d, M, N, K,
+                                   batch, alpha, beta, _stream(stream))
 
 
 def gemm_plan_query_error(plan):
@@ -232,12 +264,12 @@ class Plan:
     are fixed at construction, any shape may be run later."""
 
     def __init__(self, dtype="f16", out_dtype=None, relu=False, layout_a=ROW_MAJOR,
-                 layout_b=ROW_MAJOR, layout_cd=ROW_MAJOR):
+                 layout_b=ROW_MAJOR, layout_cd=ROW_MAJOR, epilogue=None):
         self.dtype = dtype
         self.out_dtype = out_dtype or ("bf16" if dtype == "e4m3" else dtype)
         self.layouts = (layout_a, layout_b, layout_cd)
         self.handle = gemm_plan_create(dtype, dtype, self.out_dtype, self.out_dtype, "f32",
-                                       layout_a, layout_b, layout_cd, relu)
+                                       layout_a, layout_b, layout_cd, relu, epilogue)
 
     def close(self):
         if self.handle:
@@ -255,7 +287,7 @@ class Plan:
         return self
 
     def run(self, A, B, C, D, M=None, N=None, K=None, alpha=1.0, beta=0.0, scale_a=None,
-            scale_b=None, stream=None, lda=None, ldb=None, ldc=None, ldd=None):
+            scale_b=None, stream=None, lda=None, ldb=None, ldc=None, ldd=None, bias=None):
         la, lb, lcd = self.layouts
         if M is None:
             M = A.shape[0] if la == ROW_MAJOR else A.shape[1]
@@ -265,13 +297,25 @@ class Plan:
         ldb = ldb or (N if lb == ROW_MAJOR else K)
         ldd = ldd or (N if lcd == ROW_MAJOR else M)
         ldc = ldc or ldd
-        st = gemm_run_ex(self.handle, A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta,
-                         scale_a, scale_b, stream)
+        if bias is not None:
+            st = gemm_run_args(self.handle, A, B, C, D, M, N, K, alpha, beta, lda, ldb, ldc, ldd,
+                               scale_a, scale_b, bias, stream)
+        else:
+            st = gemm_run_ex(self.handle, A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta,
+                             scale_a, scale_b, stream)
         _check(st, "gemm_run")
         return D
 
     def grouped(self, problems, alpha=1.0, beta=0.0, stream=None):
         _check(grouped_gemm_run(self.handle, problems, alpha, beta, stream), "grouped_gemm_run")
+
+    def batched(self, A, B, C, D, M, N, K, batch, stride_a, stride_b, stride_c, stride_d,
+                alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0, ldd=0, stream=None):
+        """Uniform-stride batch of one shape (strides in elements; 0 shares an operand)."""
+        _check(gemm_run_batched(self.handle, A, lda, stride_a, B, ldb, stride_b, C, ldc,
+                                stride_c, D, ldd, stride_d, M, N, K, batch, alpha, beta,
+                                stream), "gemm_run_batched")
+        return D
 
     def query_error(self):
         return gemm_plan_query_error(self.handle)

@@ -56,6 +56,14 @@ struct gemm15_plan {
     GroupEntry* h_groups = nullptr;  // pinned staging
     int groups_cap = 0;
     cudaEvent_t groups_done = nullptr;
+    // the problems the device table currently describes (a call with the same
+    // problems, C use and tile width reuses it without encoding or copying)
+    std::vector<gemm15_problem_t> groups_key;
+    bool groups_key_c = false;
+    int groups_key_bn = 0;
+    int groups_key_raster = 0;
+    int32_t groups_tiles = 0;
+    int groups_ng = 0;
     void* d_host_path[3] = {nullptr, nullptr, nullptr};  // A, B, C|D for gemm_run_host
     size_t host_path_cap[3] = {0, 0, 0};
     float* d_scales = nullptr;  // two floats for gemm_run_host
@@ -152,6 +160,8 @@ struct Prob {
     int64_t ldc;
     void* D;
     int64_t ldd;
+    const void* bias = nullptr;  // per output column of the user's D, or null
+    bool bias_rows = false;      // the bias runs along the computed rows (D^T)
 };
 
 // Column-major C/D: compute D^T = B^T . A^T, which is row-major N x M.
@@ -167,6 +177,7 @@ Prob normalise(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const v
         // A' = B^T (N x K): K contiguous iff B is column-major.
         // B' = A^T (K x M): K contiguous iff A is row-major.
         p = Prob{N, M, K, B, ldb, !b_row, A, lda, a_row, C, ldc, D, ldd};
+        p.bias_rows = true;  // the user's columns are the computed rows
     }
     return p;
 }
@@ -194,6 +205,7 @@ gemm15_status_t check_operands(const gemm15_plan* plan, const Prob& p, float bet
         if (p.ldc < p.N) return GEMM15_ERR_INVALID_ARG;
         if (!aligned16(p.C) || (p.ldc * eo) % 16) return GEMM15_ERR_ALIGNMENT;
     }
+    if (p.bias && !aligned16(p.bias)) return GEMM15_ERR_ALIGNMENT;
     return GEMM15_OK;
 }
 
@@ -456,7 +468,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         return GEMM15_OK;
     }
     const bool has_c = beta != 0.0f;
-    const bool relu = plan->desc.epilogue == GEMM15_EPI_RELU;
+    const int act = static_cast<int>(plan->desc.epilogue);
     if (p.K == 0) {
         ReduceParams rp{};
         rp.ws = nullptr;
@@ -471,8 +483,10 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.ldd = p.ldd;
         rp.alpha = alpha;
         rp.beta = beta;
-        rp.relu = relu;
+        rp.act = act;
         rp.has_c = has_c;
+        rp.bias = p.bias;
+        rp.bias_rows = p.bias_rows;
         if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
         Decision d;
         d.sched = SCHED_SPLIT;
@@ -510,7 +524,9 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.beta = beta;
     gp.scale_a = scale_a;
     gp.scale_b = scale_b;
-    gp.relu = relu;
+    gp.act = act;
+    gp.bias = d.sched == SCHED_SPLIT ? nullptr : p.bias;  // split-K: the reduction adds it
+    gp.bias_rows = p.bias_rows;
     fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.ws = plan->d_ws;
     gp.flags = plan->d_flags;
@@ -540,8 +556,10 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.beta = beta;
         rp.scale_a = scale_a;
         rp.scale_b = scale_b;
-        rp.relu = relu;
+        rp.act = act;
         rp.has_c = has_c;
+        rp.bias = p.bias;
+        rp.bias_rows = p.bias_rows;
         if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
         ++launches;
     }
@@ -579,7 +597,7 @@ gemm15_status_t gemm_plan_create(gemm15_plan_t* out, const gemm15_plan_desc_t* d
     auto valid_l = [](int l) { return l == GEMM15_ROW_MAJOR || l == GEMM15_COL_MAJOR; };
     if (!valid_t(d.a) || !valid_t(d.b) || !valid_t(d.c) || !valid_t(d.d) || !valid_t(d.acc) ||
         !valid_l(d.layout_a) || !valid_l(d.layout_b) || !valid_l(d.layout_cd) ||
-        (d.epilogue != GEMM15_EPI_LINEAR && d.epilogue != GEMM15_EPI_RELU))
+        (d.epilogue < GEMM15_EPI_LINEAR || d.epilogue > GEMM15_EPI_TANH))
         return GEMM15_ERR_INVALID_ARG;
     if (d.acc != GEMM15_F32 || d.a != d.b) return GEMM15_ERR_UNSUPPORTED;
     int elem, out_elem;
@@ -656,6 +674,25 @@ gemm15_status_t gemm_run_ex(gemm15_plan_t plan, const void* A, int64_t lda, cons
     if (!g.ok) return GEMM15_ERR_CUDA;
     Prob p = normalise(plan, M, N, K, A, lda, B, ldb, C, ldc, D, ldd);
     return run_dense(plan, p, alpha, beta, scale_a, scale_b, static_cast<cudaStream_t>(stream));
+}
+
+gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* a, void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (!a) return GEMM15_ERR_INVALID_ARG;
+    if ((a->scale_a || a->scale_b) && plan->elem != ELEM_E4M3) return GEMM15_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
+    const int64_t lda = a->lda ? a->lda : (a_row ? a->K : a->M);
+    const int64_t ldb = a->ldb ? a->ldb : (b_row ? a->N : a->K);
+    const int64_t ldc = a->ldc ? a->ldc : (cd_row ? a->N : a->M);
+    const int64_t ldd = a->ldd ? a->ldd : (cd_row ? a->N : a->M);
+    Prob p = normalise(plan, a->M, a->N, a->K, a->A, lda, a->B, ldb, a->C, ldc, a->D, ldd);
+    p.bias = a->bias;
+    return run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b,
+                     static_cast<cudaStream_t>(stream));
 }
 
 gemm15_status_t gemm_run(gemm15_plan_t plan, const void* A, const void* B, const void* C, void* D,
@@ -769,60 +806,79 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
         std::memset(&plan->last, 0, sizeof(plan->last));
         return GEMM15_OK;
     }
-    if (ng > plan->groups_cap) {
-        if (plan->groups_done) cudaEventSynchronize(plan->groups_done);
-        cudaFree(plan->d_groups);
-        if (plan->h_groups) cudaFreeHost(plan->h_groups);
-        plan->d_groups = nullptr;
-        plan->h_groups = nullptr;
-        plan->groups_cap = 0;
-        const int cap = std::max(ng, 64);
-        if (cudaMalloc(&plan->d_groups, cap * sizeof(GroupEntry)) != cudaSuccess ||
-            cudaMallocHost(&plan->h_groups, cap * sizeof(GroupEntry)) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM15_ERR_OOM;
-        }
-        plan->groups_cap = cap;
-    }
-    if (!plan->groups_done &&
-        cudaEventCreateWithFlags(&plan->groups_done, cudaEventDisableTiming) != cudaSuccess)
-        return GEMM15_ERR_CUDA;
-    // the previous grouped call's copy must have read the staging buffer
-    if (cudaEventSynchronize(plan->groups_done) != cudaSuccess) return GEMM15_ERR_CUDA;
-
     const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
     int32_t tiles = 0;
-    bool mixed_layout = false;
-    for (int i = 0; i < ng; ++i) {
-        const Prob& p = probs[i];
-        if (p.a_kmajor != probs[0].a_kmajor || p.b_kmajor != probs[0].b_kmajor) mixed_layout = true;
-        GroupEntry& e = plan->h_groups[i];
-        std::memset(&e, 0, sizeof(e));
-        if (!operand_maps(plan, p, bn, &e.tmA, &e.tmB)) return GEMM15_ERR_CUDA;
-        if (!output_maps(plan, p, has_c, &e.tmC, &e.tmD)) return GEMM15_ERR_CUDA;
-        e.M = static_cast<int32_t>(p.M);
-        e.N = static_cast<int32_t>(p.N);
-        e.K = static_cast<int32_t>(p.K);
-        e.k_blocks = static_cast<int32_t>(cdiv(p.K, bk));
-        e.m_blocks = static_cast<int32_t>(cdiv(p.M, TILE_M));
-        e.n_blocks = static_cast<int32_t>(cdiv(p.N, bn));
-        e.tile_start = tiles;
-        e.has_c = has_c;
-        e.D = p.D;
-        e.ldd = p.ldd;
-        e.C = has_c ? p.C : nullptr;
-        e.ldc = p.ldc;
-        e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
-                                        : std::min<int32_t>(e.m_blocks, 16);
-        const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;
-        if (tiles + t > (1ll << 30)) return GEMM15_ERR_INVALID_ARG;
-        tiles += static_cast<int32_t>(t);
+    const bool reuse = plan->d_groups && plan->groups_ng == ng && plan->groups_key_c == has_c &&
+                       plan->groups_key_bn == bn && plan->groups_key_raster == plan->opt.raster &&
+                       plan->groups_key.size() == static_cast<size_t>(count) &&
+                       std::memcmp(plan->groups_key.data(), problems,
+                                   sizeof(gemm15_problem_t) * static_cast<size_t>(count)) == 0;
+    if (reuse) {
+        tiles = plan->groups_tiles;
+        // the copy that wrote the table may have been enqueued on another stream
+        if (cudaStreamWaitEvent(s, plan->groups_done, 0) != cudaSuccess) return GEMM15_ERR_CUDA;
+    } else {
+        plan->groups_key.clear();  // the table is about to change
+        plan->groups_ng = 0;
+        if (ng > plan->groups_cap) {
+            if (plan->groups_done) cudaEventSynchronize(plan->groups_done);
+            cudaFree(plan->d_groups);
+            if (plan->h_groups) cudaFreeHost(plan->h_groups);
+            plan->d_groups = nullptr;
+            plan->h_groups = nullptr;
+            plan->groups_cap = 0;
+            const int cap = std::max(ng, 64);
+            if (cudaMalloc(&plan->d_groups, cap * sizeof(GroupEntry)) != cudaSuccess ||
+                cudaMallocHost(&plan->h_groups, cap * sizeof(GroupEntry)) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM15_ERR_OOM;
+            }
+            plan->groups_cap = cap;
+        }
+        if (!plan->groups_done &&
+            cudaEventCreateWithFlags(&plan->groups_done, cudaEventDisableTiming) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        // the previous grouped call's copy must have read the staging buffer
+        if (cudaEventSynchronize(plan->groups_done) != cudaSuccess) return GEMM15_ERR_CUDA;
+
+        bool mixed_layout = false;
+        for (int i = 0; i < ng; ++i) {
+            const Prob& p = probs[i];
+            if (p.a_kmajor != probs[0].a_kmajor || p.b_kmajor != probs[0].b_kmajor) mixed_layout = true;
+            GroupEntry& e = plan->h_groups[i];
+            std::memset(&e, 0, sizeof(e));
+            if (!operand_maps(plan, p, bn, &e.tmA, &e.tmB)) return GEMM15_ERR_CUDA;
+            if (!output_maps(plan, p, has_c, &e.tmC, &e.tmD)) return GEMM15_ERR_CUDA;
+            e.M = static_cast<int32_t>(p.M);
+            e.N = static_cast<int32_t>(p.N);
+            e.K = static_cast<int32_t>(p.K);
+            e.k_blocks = static_cast<int32_t>(cdiv(p.K, bk));
+            e.m_blocks = static_cast<int32_t>(cdiv(p.M, TILE_M));
+            e.n_blocks = static_cast<int32_t>(cdiv(p.N, bn));
+            e.tile_start = tiles;
+            e.has_c = has_c;
+            e.D = p.D;
+            e.ldd = p.ldd;
+            e.C = has_c ? p.C : nullptr;
+            e.ldc = p.ldc;
+            e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
+                                            : std::min<int32_t>(e.m_blocks, 16);
+            const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;
+            if (tiles + t > (1ll << 30)) return GEMM15_ERR_INVALID_ARG;
+            tiles += static_cast<int32_t>(t);
+        }
+        if (mixed_layout) return GEMM15_ERR_UNSUPPORTED;  // normalisation is per plan: cannot happen
+        if (cudaMemcpyAsync(plan->d_groups, plan->h_groups, ng * sizeof(GroupEntry),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaEventRecord(plan->groups_done, s) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        plan->groups_key.assign(problems, problems + count);
+        plan->groups_key_c = has_c;
+        plan->groups_key_bn = bn;
+        plan->groups_key_raster = plan->opt.raster;
+        plan->groups_tiles = tiles;
+        plan->groups_ng = ng;
     }
-    if (mixed_layout) return GEMM15_ERR_UNSUPPORTED;  // normalisation is per plan: cannot happen
-    if (cudaMemcpyAsync(plan->d_groups, plan->h_groups, ng * sizeof(GroupEntry),
-                        cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaEventRecord(plan->groups_done, s) != cudaSuccess)
-        return GEMM15_ERR_CUDA;
 
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
@@ -832,7 +888,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     gp.k_blocks = 0;
     gp.alpha = alpha;
     gp.beta = beta;
-    gp.relu = plan->desc.epilogue == GEMM15_EPI_RELU;
+    gp.act = static_cast<int>(plan->desc.epilogue);
     gp.has_c = has_c;
     fill_layout(plan, gp, probs[0].a_kmajor, probs[0].b_kmajor, bn);
     gp.ws = plan->d_ws;
@@ -858,6 +914,40 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     d.raster = 16;
     record_config(plan, d, 1);
     return GEMM15_OK;
+}
+
+gemm15_status_t gemm_run_batched(gemm15_plan_t plan, const void* A, int64_t lda, int64_t stride_a,
+                                 const void* B, int64_t ldb, int64_t stride_b, const void* C,
+                                 int64_t ldc, int64_t stride_c, void* D, int64_t ldd,
+                                 int64_t stride_d, int64_t M, int64_t N, int64_t K,
+                                 int32_t batch, float alpha, float beta, void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (batch < 0 || stride_a < 0 || stride_b < 0 || stride_c < 0 || stride_d < 0)
+        return GEMM15_ERR_INVALID_ARG;
+    if (batch == 0 || M == 0 || N == 0) {
+        std::memset(&plan->last, 0, sizeof(plan->last));
+        return (M < 0 || N < 0 || K < 0) ? GEMM15_ERR_INVALID_ARG : GEMM15_OK;
+    }
+    const int64_t ea = plan->elem == ELEM_E4M3 ? 1 : 2;
+    const int64_t ec = 2;  // C and D are 16-bit
+    if ((stride_a * ea) % 16 || (stride_b * ea) % 16 || (stride_c * ec) % 16 || (stride_d * ec) % 16)
+        return GEMM15_ERR_ALIGNMENT;
+    std::vector<gemm15_problem_t> probs(static_cast<size_t>(batch));
+    for (int32_t b = 0; b < batch; ++b) {
+        gemm15_problem_t& q = probs[b];
+        q.M = M;
+        q.N = N;
+        q.K = K;
+        q.A = static_cast<const uint8_t*>(A) + b * stride_a * ea;
+        q.B = static_cast<const uint8_t*>(B) + b * stride_b * ea;
+        q.C = C ? static_cast<const uint8_t*>(C) + b * stride_c * ec : nullptr;
+        q.D = static_cast<uint8_t*>(D) + b * stride_d * ec;
+        q.lda = lda;
+        q.ldb = ldb;
+        q.ldc = ldc;
+        q.ldd = ldd;
+    }
+    return grouped_gemm_run(plan, probs.data(), batch, alpha, beta, stream);
 }
 
 gemm15_status_t gemm_plan_query_error(gemm15_plan_t plan) {

@@ -137,7 +137,7 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
     }
     const auto is_layout = [](int l) { return l == GEMM15_ROW_MAJOR || l == GEMM15_COL_MAJOR; };
     if (!is_layout(d.layout_a) || !is_layout(d.layout_b) || !is_layout(d.layout_cd) ||
-        (d.epilogue != GEMM15_EPI_LINEAR && d.epilogue != GEMM15_EPI_RELU))
+        (d.epilogue < GEMM15_EPI_LINEAR || d.epilogue > GEMM15_EPI_TANH))
         return GEMM15_ERR_INVALID_ARG;
     if ((scale_a || scale_b) && elem != ELEM_E4M3) return GEMM15_ERR_INVALID_ARG;
     if (splits < 1 || M < 0 || N < 0 || K < 0) return GEMM15_ERR_INVALID_ARG;
@@ -195,7 +195,7 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
     int32_t* dev_status = status ? status : reinterpret_cast<int32_t*>(ds->scratch);
     if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return GEMM15_ERR_CUDA;
     float* partials = ds->scratch + STATUS_BYTES / sizeof(float);
-    const bool relu = d.epilogue == GEMM15_EPI_RELU;
+    const int act = static_cast<int>(d.epilogue);
 
     if (K > 0) {
         GemmParams gp;
@@ -224,7 +224,7 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
         gp.has_c = 0;  // the reduction reads C
         gp.alpha = alpha;
         gp.beta = beta;
-        gp.relu = relu;
+        gp.act = act;
         // shared-memory operand layouts (128-byte swizzle) and the MMA descriptor
         const uint32_t mn_box = static_cast<uint32_t>(128 * bk);
         const uint32_t umma_k = 32 / es;
@@ -271,7 +271,7 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
     rp.beta = beta;
     rp.scale_a = scale_a;
     rp.scale_b = scale_b;
-    rp.relu = relu;
+    rp.act = act;
     rp.has_c = has_c;
     const int64_t work = m * ((n + 7) / 8);
     const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, ds->num_sms * 8)));

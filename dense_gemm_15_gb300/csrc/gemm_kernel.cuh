@@ -117,11 +117,67 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     }
 }
 
+// One stored 16-bit output-type value as float.
+template <int ELEM>
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
+    if constexpr (ELEM == ELEM_F16) return __half2float(__ushort_as_half(h));
+    else return __bfloat162float(__ushort_as_bfloat16(h));
+}
+
 // max(x, 0) that keeps NaN (one max.NaN instruction).
 __device__ __forceinline__ float relu_nan(float x) {
     float r;
     asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(x));
     return r;
+}
+
+// Logistic sigmoid 1 / (1 + e^-x) from the exponential and fast-division
+// intrinsics (its definition; x -> -inf gives 0, +inf gives 1, NaN stays NaN).
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// tanh by the hardware approximation (PTX tanh.approx.f32, relative error
+// below 2^-10.9, the order of one 16-bit output rounding).
+__device__ __forceinline__ float tanh_f(float x) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// The epilogue activation of one value (Activation).
+__device__ __forceinline__ float activate(float x, int act) {
+    switch (act) {
+        case ACT_RELU: return relu_nan(x);
+        case ACT_SIGMOID: return sigmoid_f(x);
+        case ACT_TANH: return tanh_f(x);
+        default: return x;
+    }
+}
+
+// Applies the activation to n values held in registers: one uniform branch,
+// then straight-line code.
+template <int NV>
+__device__ __forceinline__ void activate_all(float (&v)[NV], int act) {
+    if (act == ACT_RELU) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = relu_nan(v[i]);
+    } else if (act == ACT_SIGMOID) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = sigmoid_f(v[i]);
+    } else if (act == ACT_TANH) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = tanh_f(v[i]);
+    }
+}
+
+// Eight consecutive bias elements starting at column c (16-bit, zero past n),
+// packed in pairs.
+__device__ __forceinline__ uint4 load_bias8(const void* bias, int64_t c, int64_t n) {
+    const uint16_t* b = static_cast<const uint16_t*>(bias);
+    if (c + 8 <= n) return __ldg(reinterpret_cast<const uint4*>(b + c));
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int t = 0; t < 8; ++t)
+        if (c + t < n) w[t >> 1] |= static_cast<uint32_t>(__ldg(b + c + t)) << (16 * (t & 1));
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ------------------------------------------------------------------ errors
@@ -621,7 +677,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (p.scale_a) alpha *= __ldg(p.scale_a);
         if (p.scale_b) alpha *= __ldg(p.scale_b);
         const float beta = p.beta;
-        const bool relu = p.relu != 0;
+        const int act = p.act;
+        const bool has_bias = p.bias != nullptr;
         // C, D and the peers' partial tiles are each touched once here: let L2
         // evict them before the A and B tiles that other CTAs still read
         const uint64_t pol_once = l2_policy_evict_first();
@@ -698,6 +755,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool to_ws = (w.kind == WK_PEER || w.kind == WK_SPLIT);
             const bool stage_c = has_c && !to_ws && rows_live;
             const int nch = min(NCH, (N - n0 + EPI_COLS - 1) / EPI_COLS);
+            // bias of this thread's row (bias indexed by output row)
+            float bias_row = 0.0f;
+            if (has_bias && p.bias_rows && !to_ws && row0 + lane < M)
+                bias_row = half_bits_to_float<ELEM>(__ldg(static_cast<const uint16_t*>(p.bias) + row0 + lane));
 
             // C is fetched while the mainloop still runs: the whole tile when
             // every chunk has its own box, else the first chunk, with the rest
@@ -751,25 +812,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int32_t pb0 = w.kind == WK_OWNER ? next_peer(w, w.h0) : -1;
             const bool preload = pb0 >= 0 && sched_sk_last(st) && ok;
             if (preload && rows_live) {
-                // two chunks of the first peer in flight: chunk c + 1 is requested
-                // before chunk c is summed and written to TMEM
-                float4 ps[2][16];
-                auto request = [&](float4 (&dst)[16], int c) {
-                    const float4* src0 = peer_src(w, pb0, c * EPI_COLS);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[i] = ld_global_cg_hint(src0 + 32 * i, pol_once);
-                };
-                auto finish = [&](float4 (&cur)[16], int c) {
+                for (int c = 0; c < nch; ++c) {
                     const int32_t col0 = c * EPI_COLS;
+                    // the whole chunk of the first peer in flight at once (16 loads)
+                    float4 ps[16];
+                    const float4* src0 = peer_src(w, pb0, col0);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ps[i] = ld_global_cg_hint(src0 + 32 * i, pol_once);
                     for (int32_t pb = next_peer(w, pb0 + 1); pb >= 0; pb = next_peer(w, pb + 1)) {
                         const float4* src = peer_src(w, pb, col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
-                            cur[i].x += t.x;
-                            cur[i].y += t.y;
-                            cur[i].z += t.z;
-                            cur[i].w += t.w;
+                            ps[i].x += t.x;
+                            ps[i].y += t.y;
+                            ps[i].z += t.z;
+                            ps[i].w += t.w;
                         }
                     }
 #pragma unroll
@@ -777,21 +835,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         uint32_t r[32];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            r[4 * i + 0] = __float_as_uint(cur[8 * h + i].x);
-                            r[4 * i + 1] = __float_as_uint(cur[8 * h + i].y);
-                            r[4 * i + 2] = __float_as_uint(cur[8 * h + i].z);
-                            r[4 * i + 3] = __float_as_uint(cur[8 * h + i].w);
+                            r[4 * i + 0] = __float_as_uint(ps[8 * h + i].x);
+                            r[4 * i + 1] = __float_as_uint(ps[8 * h + i].y);
+                            r[4 * i + 2] = __float_as_uint(ps[8 * h + i].z);
+                            r[4 * i + 3] = __float_as_uint(ps[8 * h + i].w);
                         }
                         tmem_st32(tmem_base + lane_base + (ab ^ 1u) * BN + col0 + h * 32, r);
-                    }
-                };
-                request(ps[0], 0);
-                for (int c = 0; c < nch; c += 2) {
-                    if (c + 1 < nch) request(ps[1], c + 1);
-                    finish(ps[0], c);
-                    if (c + 1 < nch) {
-                        if (c + 2 < nch) request(ps[0], c + 2);
-                        finish(ps[1], c + 1);
                     }
                 }
                 tmem_st_wait();
@@ -816,6 +865,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int32_t col0 = c * EPI_COLS;
                 const uint32_t b = WHOLE ? static_cast<uint32_t>(c) : (n_chunk & 1u);
                 const uint32_t buf = ebuf0 + b * EPI_BUF_BYTES;
+                // bias by output column: lane j < 8 fetches columns 8j..8j+7 of the chunk
+                uint4 bias8 = make_uint4(0u, 0u, 0u, 0u);
+                if (has_bias && !p.bias_rows && !to_ws)
+                    bias8 = load_bias8(p.bias, static_cast<int64_t>(n0) + col0 + 8 * (lane & 7), N);
                 if (WHOLE) {
                     // nothing to wait for: the boxes were freed when the tile started
                 } else if (stage_c) {
@@ -903,45 +956,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 OutT* drow = Dptr + static_cast<int64_t>(my_row) * ldd + n0 + col0;
                 // 128-byte swizzle: 16-byte chunk j of row `lane` sits at j ^ (lane % 8)
                 auto slot_of = [&](int j) { return buf + lane * 128 + ((j ^ (lane & 7)) << 4); };
-                // alpha * acc (+ beta * C) (ReLU) -> 16-bit pairs; the C and ReLU
-                // variants are separate straight-line code (no branch between the
-                // eight groups), and all eight C loads come before any store
-                uint32_t pk[8][4];
-                auto convert = [&](auto has_c, auto has_relu) {
+                // alpha * acc (+ beta * C), then the bias, then the activation, then
+                // 16-bit pairs: each phase is straight-line code chosen by one
+                // uniform branch, and all eight C loads come before any store
+                if (stage_c) {
                     uint4 cvs[8];
-                    if constexpr (decltype(has_c)::value) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) cvs[j] = ld_shared_v4(slot_of(j));
-                    }
+                    for (int j = 0; j < 8; ++j) cvs[j] = ld_shared_v4(slot_of(j));
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        float o[8];
+                        const uint32_t cw[4] = {cvs[j].x, cvs[j].y, cvs[j].z, cvs[j].w};
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) o[t] = alpha * v[8 * j + t];
-                        if constexpr (decltype(has_c)::value) {
-                            const uint32_t cw[4] = {cvs[j].x, cvs[j].y, cvs[j].z, cvs[j].w};
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f = unpack2<ELEM>(cw[t]);
+                            v[8 * j + 2 * t] = fmaf(beta, f.x, alpha * v[8 * j + 2 * t]);
+                            v[8 * j + 2 * t + 1] = fmaf(beta, f.y, alpha * v[8 * j + 2 * t + 1]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] *= alpha;
+                }
+                if (has_bias) {
+                    if (p.bias_rows) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) v[i] += bias_row;
+                    } else {
+                        // lane j (< 8) holds columns 8j..8j+7 of this chunk
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t bw[4] = {__shfl_sync(0xffffffffu, bias8.x, j),
+                                                    __shfl_sync(0xffffffffu, bias8.y, j),
+                                                    __shfl_sync(0xffffffffu, bias8.z, j),
+                                                    __shfl_sync(0xffffffffu, bias8.w, j)};
 #pragma unroll
                             for (int t = 0; t < 4; ++t) {
-                                const float2 f = unpack2<ELEM>(cw[t]);
-                                o[2 * t] = fmaf(beta, f.x, o[2 * t]);
-                                o[2 * t + 1] = fmaf(beta, f.y, o[2 * t + 1]);
+                                const float2 f = unpack2<ELEM>(bw[t]);
+                                v[8 * j + 2 * t] += f.x;
+                                v[8 * j + 2 * t + 1] += f.y;
                             }
                         }
-                        if constexpr (decltype(has_relu)::value) {
-#pragma unroll
-                            for (int t = 0; t < 8; ++t) o[t] = relu_nan(o[t]);
-                        }
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) pk[j][t] = pack2<ELEM>(o[2 * t], o[2 * t + 1]);
                     }
-                };
-                if (stage_c) {
-                    if (relu) convert(std::true_type{}, std::true_type{});
-                    else convert(std::true_type{}, std::false_type{});
-                } else {
-                    if (relu) convert(std::false_type{}, std::true_type{});
-                    else convert(std::false_type{}, std::false_type{});
                 }
+                activate_all(v, act);
+                uint32_t pk[8][4];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) pk[j][t] = pack2<ELEM>(v[8 * j + 2 * t], v[8 * j + 2 * t + 1]);
                 if (!ragged) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) st_shared_v4(slot_of(j), pk[j][0], pk[j][1], pk[j][2], pk[j][3]);
@@ -1025,9 +1087,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------------ split-K reduction
 
-// D = act(alpha * sum_s partial_s + beta * C) for split-K runs (splits >= 1),
-// or D = act(beta * C) when K == 0 (splits == 0).  Each thread owns 8
-// consecutive columns of one row; partial tiles are summed in split order.
+// D = act(alpha * sum_s partial_s + beta * C + bias) for split-K runs (splits
+// >= 1), or D = act(beta * C + bias) when K == 0 (splits == 0).  Each thread
+// owns 8 consecutive columns of one row; partial tiles are summed in split order.
 template <int ELEM>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     using OutT = typename OutType<ELEM>::T;
@@ -1058,6 +1120,26 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
             }
         }
         const int nvalid = min(8, p.N - n);
+        float bias[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) bias[t] = 0.0f;
+        if (p.bias) {
+            const uint16_t* bv = static_cast<const uint16_t*>(p.bias);
+            if (p.bias_rows) {
+                const float b = half_bits_to_float<ELEM>(__ldg(bv + m));
+#pragma unroll
+                for (int t = 0; t < 8; ++t) bias[t] = b;
+            } else {
+                const uint4 b8 = load_bias8(p.bias, n, p.N);
+                const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = unpack2<ELEM>(bw[t]);
+                    bias[2 * t] = f.x;
+                    bias[2 * t + 1] = f.y;
+                }
+            }
+        }
         const OutT* crow = reinterpret_cast<const OutT*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
         OutT* drow = reinterpret_cast<OutT*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
         float o[8];
@@ -1070,8 +1152,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
                 else cv = __bfloat162float(crow[t]);
                 x = fmaf(p.beta, cv, x);
             }
-            if (p.relu) x = relu_nan(x);
-            o[t] = x;
+            o[t] = activate(x + bias[t], p.act);
         }
         if (nvalid == 8) {
             *reinterpret_cast<uint4*>(drow) =

@@ -9,6 +9,8 @@ namespace g15 {
 enum ElemKind : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_E4M3 = 2 };
 enum Schedule : int { SCHED_DP = 1, SCHED_SK = 2, SCHED_SPLIT = 3 };
 enum DeviceError : int { DEV_ERR_TIMEOUT = 5, DEV_ERR_FAULT = 7 };
+// epilogue activation (values of gemm15_epilogue_t)
+enum Activation : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SIGMOID = 2, ACT_TANH = 3 };
 
 constexpr int TILE_M = 128;         // rows of A per CTA (UMMA M for one SM)
 constexpr int EPI_WARPS = 4;        // epilogue warps (one per 32-lane TMEM quarter)
@@ -46,7 +48,9 @@ struct GemmParams {
     float alpha, beta;
     const float* scale_a;             // fp8 per-tensor scales (device), or null
     const float* scale_b;
-    int32_t relu;
+    int32_t act;                      // Activation
+    int32_t bias_rows;                // bias indexed by output row (1) or column (0)
+    const void* bias;                 // 16-bit bias vector (device), or null
     // operand layouts in shared memory (bytes) and the MMA instruction descriptor
     uint32_t a_kmajor, b_kmajor;
     uint32_t a_lbo, a_sbo, a_kstep;
@@ -88,7 +92,9 @@ struct ReduceParams {
     float alpha, beta;
     const float* scale_a;
     const float* scale_b;
-    int32_t relu, has_c;
+    int32_t act, has_c;
+    const void* bias;                 // as in GemmParams
+    int32_t bias_rows;
 };
 
 }  // namespace g15

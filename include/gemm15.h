@@ -56,10 +56,21 @@ typedef enum {
 
 typedef enum { GEMM15_ROW_MAJOR = 0, GEMM15_COL_MAJOR = 1 } gemm15_layout_t;
 
-/* Epilogue activation, applied after alpha*(A.B) + beta*C ("CUTLASS Python
- * 接口全解析" section 2.3; kwkr.cn blog section 5.2 applies ReLU after the
- * linear combination). */
-typedef enum { GEMM15_EPI_LINEAR = 0, GEMM15_EPI_RELU = 1 } gemm15_epilogue_t;
+/* Epilogue activation, applied last, to alpha*(A.B) + beta*C (+ bias)
+ * ("CUTLASS Python 接口全解析" section 2.3 fuses an activation into the
+ * epilogue; the kwkr.cn blog "CUTLASS Python接口" section 5.2 applies ReLU to
+ * alpha*(A.B) + beta*C + bias; "Generating State-of-the-Art GEMMs with
+ * TorchInductor's CuteDSL backend", roadmap section, lists ReLU, Sigmoid and
+ * Tanh as epilogue activations).  NaN propagates through every activation.
+ *   SIGMOID: 1 / (1 + exp(-x)), with the fast exponential and division;
+ *   TANH:    the hardware approximation (relative error below 2^-10.9, the
+ *            order of one fp16 rounding). */
+typedef enum {
+    GEMM15_EPI_LINEAR = 0,
+    GEMM15_EPI_RELU = 1,
+    GEMM15_EPI_SIGMOID = 2,
+    GEMM15_EPI_TANH = 3
+} gemm15_epilogue_t;
 
 typedef enum {
     GEMM15_OK = 0,
@@ -121,6 +132,32 @@ gemm15_status_t gemm_run_ex(gemm15_plan_t plan, const void* A, int64_t lda, cons
                             int64_t M, int64_t N, int64_t K, float alpha, float beta,
                             const float* scale_a, const float* scale_b, void* stream);
 
+/* Per-run arguments of gemm_run_args (leading dimensions 0 = packed, as in
+ * gemm_run). */
+typedef struct {
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    const void* C;
+    int64_t ldc;
+    void* D;
+    int64_t ldd;
+    int64_t M, N, K;
+    float alpha, beta;
+    const float* scale_a; /* E4M3 plans: DEVICE float, NULL = 1 (as gemm_run_ex) */
+    const float* scale_b;
+    const void* bias;     /* DEVICE vector of N elements of D's type, or NULL */
+} gemm15_args_t;
+
+/* D = act(alpha * s_a * s_b * (A . B) + beta * C + bias), bias[j] added to
+ * every element of column j of D -- the LinearCombinationBiasReLU epilogue of
+ * the kwkr.cn blog "CUTLASS Python接口", section 5.2 (bias vector of length N in
+ * the output type, fp32 arithmetic, activation last).  Everything else as
+ * gemm_run_ex; the bias pointer must be 16-byte aligned (ALIGNMENT otherwise).
+ * With K == 0, D = act(beta * C + bias). */
+gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* args, void* stream);
+
 /* End-to-end variant for callers holding HOST buffers (packed layouts as in
  * gemm_run; pinned memory recommended).  Copies A, B (and C when beta != 0)
  * into plan-owned device buffers, runs the GEMM and copies D back, all on
@@ -152,6 +189,24 @@ typedef struct {
  * alignment rules as gemm_run_ex. */
 gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* problems,
                                  int32_t count, float alpha, float beta, void* stream);
+
+/* Batched GEMM: `batch` independent problems of one shape, problem b reading
+ * A + b*stride_a, B + b*stride_b, C + b*stride_c and writing D + b*stride_d
+ * (strides in elements), D_b = act(alpha * (A_b . B_b) + beta * C_b) -- the
+ * batch_count / batch_stride arguments of the kwkr.cn blog "CUTLASS
+ * Python接口", section 6.3, where the strides of packed batches are M*K, K*N
+ * and M*N.  A stride of 0 shares that operand across the batch (one weight
+ * matrix for every batch entry); the D matrices must not overlap.  Leading
+ * dimensions as in gemm_run_ex (0 = packed).  Every stride * element size must
+ * be a multiple of 16 bytes (ALIGNMENT otherwise).  Runs as one grouped launch
+ * (same device table and rules as grouped_gemm_run: K == 0 is UNSUPPORTED);
+ * batch == 0, M == 0 or N == 0 do nothing.  INVALID_ARG for batch < 0 or
+ * negative strides. */
+gemm15_status_t gemm_run_batched(gemm15_plan_t plan, const void* A, int64_t lda, int64_t stride_a,
+                                 const void* B, int64_t ldb, int64_t stride_b, const void* C,
+                                 int64_t ldc, int64_t stride_c, void* D, int64_t ldd,
+                                 int64_t stride_d, int64_t M, int64_t N, int64_t K,
+                                 int32_t batch, float alpha, float beta, void* stream);
 
 /* Reads and clears the plan's device status word (GEMM15_OK if no device-side
  * error was recorded).  Synchronises the plan's device; call it after the

@@ -71,6 +71,8 @@ def dtype_code(dt) -> int:
 
 
 def _leading(arr: np.ndarray, code: int) -> int:
+    if arr.ndim == 2 and arr.size == 0:
+        return max(1, arr.shape[1])  # an empty operand (K == 0) is never read
     if arr.ndim != 2 or arr.strides[1] != _ITEMSIZE[code]:
         raise ValueError("operand storage must be 2-D with unit inner stride")
     if arr.strides[0] % _ITEMSIZE[code]:
