@@ -388,6 +388,13 @@ def run_gpu(args):
                      scale_a=scales[0] if scales else None,
                      scale_b=scales[1] if scales else None, stream=stream, bias=bias_dev)
 
+    tuned = None
+    if args.autotune and not grouped:
+        A, B, C, D = dv[0]
+        res = plan.autotune(A, B, C, D, p0.M, p0.N, p0.K, alpha=p0.alpha, beta=p0.beta,
+                            bias=bias_dev, scale_a=scales[0] if scales else None,
+                            scale_b=scales[1] if scales else None, iterations=5, stream=stream)
+        tuned = {"candidates": len(res), "best_us": res[0]["us"], "worst_us": res[-1]["us"]}
     for _ in range(args.warmup):
         l2_flush()
         step()
@@ -489,7 +496,7 @@ def run_gpu(args):
                        "l2": ("flushed between steps (256 MiB write%s, outside the step events)"
                               % (" then 256 MiB read" if args.flush == "write+read" else "")),
                        "parallelism": "replicas" if ws > 1 else "single",
-                       "kernel": cfg},
+                       "kernel": cfg, "autotuned": tuned},
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -516,6 +523,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--list", action="store_true")
+    ap.add_argument("--autotune", action="store_true",
+                    help="time every kernel configuration first and keep the fastest")
     ap.add_argument("--trace", help="after timing, save one step's per-CTA timeline (.npy)")
     ap.add_argument("--flush", choices=["write", "write+read"], default="write",
                     help="L2 flush between timed steps")

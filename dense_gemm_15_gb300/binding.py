@@ -31,7 +31,8 @@ EXPORTED = (
     "gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
     "grouped_gemm_run", "gemm_plan_query_error", "gemm15_status_string",
     "gemm_plan_set_option", "gemm_plan_last_config", "gemm_run_splitk_noalloc",
-    "gemm_plan_trace", "gemm_run_batched", "gemm_run_args",
+    "gemm_plan_trace", "gemm_run_batched", "gemm_run_args", "gemm_plan_autotune",
+    "gemm_plan_forget_tuning",
 )
 
 
@@ -65,6 +66,15 @@ class Config(ctypes.Structure):
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class TuneResult(ctypes.Structure):
+    _fields_ = [("config", Config), ("sk_dp_waves", ctypes.c_int32), ("us", ctypes.c_float),
+                ("status", ctypes.c_int)]
+
+    def as_dict(self):
+        return {"config": self.config.as_dict(), "sk_dp_waves": self.sk_dp_waves,
+                "us": self.us, "status": self.status}
 
 
 class Gemm15Error(RuntimeError):
@@ -101,6 +111,10 @@ def load(build_if_missing: bool = True):
         lib.gemm_run_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, f32, f32, f32, vp]
         lib.grouped_gemm_run.argtypes = [vp, ctypes.POINTER(Problem), i32, f32, f32, vp]
         lib.gemm_run_args.argtypes = [vp, ctypes.POINTER(Args), vp]
+        lib.gemm_plan_autotune.argtypes = [vp, ctypes.POINTER(Args), i32,
+                                           ctypes.POINTER(TuneResult), i32,
+                                           ctypes.POINTER(i32), vp]
+        lib.gemm_plan_forget_tuning.argtypes = [vp]
         lib.gemm_run_batched.argtypes = [vp, vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
                                          i64, i64, i64, i64, i32, f32, f32, vp]
         lib.gemm_plan_query_error.argtypes = [vp]
@@ -207,6 +221,24 @@ def gemm_run_args(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ldb=0, 
     args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
                 _ptr(scale_a), _ptr(scale_b), _ptr(bias))
     return load().gemm_run_args(plan, ctypes.byref(args), _stream(stream))
+
+
+def gemm_plan_autotune(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0,
+                       ldd=0, scale_a=None, scale_b=None, bias=None, iterations=10,
+                       stream=None):
+    """Returns (status, [result dicts, fastest first])."""
+    args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
+                _ptr(scale_a), _ptr(scale_b), _ptr(bias))
+    cap = 64
+    out = (TuneResult * cap)()
+    n = ctypes.c_int32()
+    st = load().gemm_plan_autotune(plan, ctypes.byref(args), int(iterations), out, cap,
+                                   ctypes.byref(n), _stream(stream))
+    return st, [out[i].as_dict() for i in range(min(n.value, cap))]
+
+
+def gemm_plan_forget_tuning(plan):
+    return load().gemm_plan_forget_tuning(plan)
 
 
 def gemm_run_batched(plan, A, lda, stride_a, B, ldb, stride_b, C, ldc, stride_c, D, ldd,
@@ -316,6 +348,17 @@ class Plan:
                                 stride_c, D, ldd, stride_d, M, N, K, batch, alpha, beta,
                                 stream), "gemm_run_batched")
         return D
+
+    def autotune(self, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, bias=None, scale_a=None,
+                 scale_b=None, iterations=10, stream=None, **ld):
+        """Times every candidate kernel configuration for this shape and keeps the
+        fastest for later runs of the same (M, N, K); returns the results."""
+        st, res = gemm_plan_autotune(self.handle, A, B, C, D, M, N, K, alpha, beta,
+                                     ld.get("lda", 0), ld.get("ldb", 0), ld.get("ldc", 0),
+                                     ld.get("ldd", 0), scale_a, scale_b, bias, iterations,
+                                     stream)
+        _check(st, "gemm_plan_autotune")
+        return res
 
     def query_error(self):
         return gemm_plan_query_error(self.handle)

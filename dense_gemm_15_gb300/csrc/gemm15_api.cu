@@ -12,6 +12,8 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <map>
+#include <tuple>
 #include <vector>
 
 #include "../../include/gemm15.h"
@@ -36,6 +38,11 @@ struct Options {
     int fault_skip_flag = -1;
     int sk_dp_waves = -1;
     int trace_items = 0;
+};
+
+// Kernel choice fixed by gemm_plan_autotune for one problem shape.
+struct Tuned {
+    int schedule, cta_group, tile_n, sk_dp_waves, splits;
 };
 
 }  // namespace
@@ -74,6 +81,8 @@ struct gemm15_plan {
     int trace_ctas = 0;
     Options opt;
     gemm15_config_t last{};
+    // autotuned choices per computed problem shape (M, N, K after normalisation)
+    std::map<std::tuple<int64_t, int64_t, int64_t>, Tuned> tuned;
 };
 
 namespace {
@@ -241,11 +250,30 @@ int pair_clusters(gemm15_plan* plan) {
 //     operands at the same time, lose more to L2 misses than the tail wave
 //     costs); stream-K over the tail waves otherwise;
 //   - less than one wave: split-K with a separate reduction when at least two
-//     splits per tile fit (stream-K otherwise), unless K is short (fewer than
-//     32 k-blocks), where data-parallel 128 x 128 tiles win.
+//     splits per tile fit (stream-K otherwise), on SM-pair tiles when M >= 512
+//     and on 128-wide tiles when more than 16 splits per tile fit; unless K
+//     is short (fewer than 32 k-blocks), where data-parallel 128 x 128 tiles
+//     win.
+// The plan's options with an autotuned choice for this shape filled in where
+// the option is left automatic.
+Options effective_options(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
+    Options o = plan->opt;
+    const auto it = plan->tuned.find(std::make_tuple(M, N, K));
+    if (it == plan->tuned.end()) return o;
+    const Tuned& t = it->second;
+    if (o.schedule == 0) {
+        o.schedule = t.schedule;
+        if (o.sk_dp_waves < 0) o.sk_dp_waves = t.sk_dp_waves;
+        if (o.splits == 0) o.splits = t.splits;
+    }
+    if (o.cta_group == 0) o.cta_group = t.cta_group;
+    if (o.tile_n == 0) o.tile_n = t.tile_n;
+    return o;
+}
+
 Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     Decision d;
-    const Options& o = plan->opt;
+    const Options o = effective_options(plan, M, N, K);
     d.bk = plan->elem == ELEM_E4M3 ? 128 : 64;
     d.bn = o.tile_n ? o.tile_n : (N <= 128 ? 128 : 256);
     const int G1 = o.grid > 0 ? std::min(o.grid, plan->num_sms) : plan->num_sms;
@@ -253,13 +281,12 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     // SM-pair tiles 256 x 128 exist for 16-bit operands only (an fp8 half-tile
     // of B would be narrower than one 128-byte swizzle row)
     const bool pair_ok = d.bn == 256 || plan->elem != ELEM_E4M3;
+    const int clusters = std::min(pair_clusters(plan), G1 / 2);
     if (pair_ok && o.cta_group != 1) {
-        const int clusters = std::min(pair_clusters(plan), G1 / 2);
         const int64_t tiles2 = cdiv(M, 2 * TILE_M) * cdiv(N, 256);
         if (clusters > 0 && (o.cta_group == 2 || (d.bn == 256 && M >= 512 && tiles2 >= clusters))) cg = 2;
     }
-    d.cg = cg;
-    const int G = cg == 2 ? std::min(pair_clusters(plan), G1 / 2) : G1;  // scheduling units
+    int G = cg == 2 ? clusters : G1;  // scheduling units
     d.k_blocks = static_cast<int32_t>(cdiv(K, d.bk));
     auto set_tiles = [&]() {
         d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M * cg));
@@ -285,8 +312,22 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
             }
         } else {
             sched = (G / d.tiles >= 2) ? SCHED_SPLIT : SCHED_SK;
+            if (sched == SCHED_SPLIT && o.cta_group == 0 && cg == 1 && pair_ok && d.bn == 256 &&
+                M >= 512 && clusters > 0) {
+                // pair tiles share each B tile across the pair at the same
+                // number of split units
+                cg = 2;
+                G = clusters;
+                set_tiles();
+            }
+            if (sched == SCHED_SPLIT && !o.tile_n && cg == 1 && d.bn == 256 && G / d.tiles > 16) {
+                // many splits: half-width tiles halve the fp32 partial traffic
+                d.bn = 128;
+                set_tiles();
+            }
         }
     }
+    d.cg = cg;
     d.sched = sched;
     d.raster = o.raster > 0 ? std::min<int32_t>(o.raster, d.m_blocks)
                             : std::min<int32_t>(d.m_blocks, cg == 2 ? 8 : 16);
@@ -693,6 +734,128 @@ gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* a, void* 
     p.bias = a->bias;
     return run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b,
                      static_cast<cudaStream_t>(stream));
+}
+
+gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, int32_t iterations,
+                                   gemm15_tune_result_t* results, int32_t capacity, int32_t* count,
+                                   void* stream) {
+    if (count) *count = 0;
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (!a || iterations < 1 || capacity < 0 || (capacity > 0 && !results))
+        return GEMM15_ERR_INVALID_ARG;
+    if ((a->scale_a || a->scale_b) && plan->elem != ELEM_E4M3) return GEMM15_ERR_INVALID_ARG;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
+    Prob p = normalise(plan, a->M, a->N, a->K, a->A, a->lda ? a->lda : (a_row ? a->K : a->M), a->B,
+                       a->ldb ? a->ldb : (b_row ? a->N : a->K), a->C,
+                       a->ldc ? a->ldc : (cd_row ? a->N : a->M), a->D,
+                       a->ldd ? a->ldd : (cd_row ? a->N : a->M));
+    p.bias = a->bias;
+    gemm15_status_t st = check_operands(plan, p, a->beta);
+    if (st != GEMM15_OK) return st;
+    if (p.M == 0 || p.N == 0 || p.K == 0) return GEMM15_OK;  // one fixed path: nothing to choose
+    const auto key = std::make_tuple(p.M, p.N, p.K);
+    plan->tuned.erase(key);
+
+    // candidates: every schedule on each tile shape, stream-K with and without
+    // its data-parallel waves
+    std::vector<Tuned> cands;
+    for (int sched : {SCHED_DP, SCHED_SK, SCHED_SPLIT})
+        for (int cg : {1, 2})
+            for (int bn : {128, 256}) {
+                if (cg == 2 && bn == 128 && plan->elem == ELEM_E4M3) continue;
+                if (sched == SCHED_SK) {
+                    for (int w : {-1, 0}) cands.push_back(Tuned{sched, cg, bn, w, 0});
+                } else {
+                    cands.push_back(Tuned{sched, cg, bn, -1, 0});
+                }
+            }
+    const Options saved = plan->opt;
+    // every timed run starts from an L2 that holds none of the operands (a
+    // write of twice the L2 size), as when they do not stay in L2 between uses
+    int l2_bytes = 0;
+    cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, plan->device);
+    const size_t flush_bytes = std::max<size_t>(2 * static_cast<size_t>(l2_bytes), 64u << 20);
+    void* flush = nullptr;
+    if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM15_ERR_OOM;
+    }
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        cudaFree(flush);
+        return GEMM15_ERR_CUDA;
+    }
+    std::vector<gemm15_tune_result_t> res;
+    int best = -1;
+    for (size_t i = 0; i < cands.size(); ++i) {
+        const Tuned& c = cands[i];
+        plan->opt = saved;
+        plan->opt.schedule = c.schedule;
+        plan->opt.cta_group = c.cta_group;
+        plan->opt.tile_n = c.tile_n;
+        plan->opt.sk_dp_waves = c.sk_dp_waves;
+        plan->opt.splits = c.splits;
+        gemm15_tune_result_t r{};
+        r.sk_dp_waves = c.sk_dp_waves;
+        r.us = -1.0f;
+        r.status = run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b, s);  // warm-up
+        r.config = plan->last;
+        float total_ms = 0.0f;
+        for (int it = 0; it < iterations && r.status == GEMM15_OK; ++it) {
+            float ms = 0.0f;
+            if (cudaMemsetAsync(flush, it & 0xff, flush_bytes, s) != cudaSuccess ||
+                cudaEventRecord(e0, s) != cudaSuccess) {
+                r.status = GEMM15_ERR_CUDA;
+                break;
+            }
+            r.status = run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b, s);
+            if (r.status != GEMM15_OK) break;
+            if (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+                r.status = GEMM15_ERR_CUDA;
+                break;
+            }
+            total_ms += ms;
+        }
+        if (r.status == GEMM15_OK) {
+            r.us = 1000.0f * total_ms / iterations;
+            const gemm15_status_t dev = gemm_plan_query_error(plan);
+            if (dev != GEMM15_OK) r.status = dev;
+        }
+        if (r.status == GEMM15_OK && (best < 0 || r.us < res[best].us)) best = static_cast<int>(res.size());
+        res.push_back(r);
+    }
+    plan->opt = saved;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamSynchronize(s);
+    cudaFree(flush);
+    if (best < 0) return GEMM15_ERR_CUDA;
+    plan->tuned[key] = cands[best];
+    // leave D holding the chosen configuration's result (and plan->last its config)
+    st = run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b, s);
+    if (st != GEMM15_OK) return st;
+    std::stable_sort(res.begin(), res.end(), [](const gemm15_tune_result_t& x, const gemm15_tune_result_t& y) {
+        const bool xo = x.status == GEMM15_OK, yo = y.status == GEMM15_OK;
+        if (xo != yo) return xo;
+        return xo && x.us < y.us;
+    });
+    const int32_t n = static_cast<int32_t>(res.size());
+    for (int32_t i = 0; i < std::min(n, capacity); ++i) results[i] = res[i];
+    if (count) *count = n;
+    return GEMM15_OK;
+}
+
+gemm15_status_t gemm_plan_forget_tuning(gemm15_plan_t plan) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    plan->tuned.clear();
+    return GEMM15_OK;
 }
 
 gemm15_status_t gemm_run(gemm15_plan_t plan, const void* A, const void* B, const void* C, void* D,

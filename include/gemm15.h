@@ -254,6 +254,39 @@ typedef struct {
 
 gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out);
 
+/* One candidate measured by gemm_plan_autotune. */
+typedef struct {
+    gemm15_config_t config;  /* what the candidate launched */
+    int32_t sk_dp_waves;     /* stream-K option the candidate forced (-1 = automatic) */
+    float us;                /* mean time per run in microseconds (-1 if it failed) */
+    gemm15_status_t status;  /* GEMM15_OK, or why the candidate could not run */
+} gemm15_tune_result_t;
+
+/* Autotuning: "profile every kernel configuration for the problem size and
+ * data types, then fix the fastest" (kwkr.cn blog "CUTLASS Python接口",
+ * section 6.2, GemmProfiler; autotuning over candidate configurations in
+ * "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL backend",
+ * section 6.2).  Runs each candidate the library can launch for this problem
+ * -- data-parallel, stream-K (with and without its data-parallel waves) and
+ * split-K schedules on single-SM and SM-pair tiles 128 and 256 wide -- once to
+ * warm up and then `iterations` times, each timed with CUDA events on
+ * `stream` after the L2 cache has been cleared (a write of twice its size to
+ * a scratch buffer the call allocates and frees), as when the operands do not
+ * stay in L2 between uses; the call synchronises the stream.  The fastest is kept in the plan for
+ * this (M, N, K): later gemm_run / gemm_run_ex / gemm_run_args calls of that
+ * shape use it wherever the corresponding plan options are left automatic.
+ * The operands are used as in gemm_run_args (D is written many times; it ends
+ * holding the chosen configuration's result).  The first min(count,
+ * capacity) results, fastest first (failed candidates last), go to the HOST
+ * array `results`; *count receives the number of candidates.  M, N or K == 0:
+ * nothing to choose, OK.  Argument errors as gemm_run_args. */
+gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* args,
+                                   int32_t iterations, gemm15_tune_result_t* results,
+                                   int32_t capacity, int32_t* count, void* stream);
+
+/* Drops every autotuned choice of the plan. */
+gemm15_status_t gemm_plan_forget_tuning(gemm15_plan_t plan);
+
 /* Copies the timeline of the plan's last traced GEMM-kernel launch (see
  * GEMM15_OPT_TRACE_ITEMS) into the HOST buffer `out` of `capacity` bytes, after
  * synchronising the plan's device.  Layout: for each of *ctas CTAs, one header
