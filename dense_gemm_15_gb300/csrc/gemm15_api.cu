@@ -69,6 +69,7 @@ struct gemm15_plan {
     bool groups_key_c = false;
     int groups_key_bn = 0;
     int groups_key_raster = 0;
+    int groups_key_cg = 0;
     int32_t groups_tiles = 0;
     int groups_ng = 0;
     void* d_host_path[3] = {nullptr, nullptr, nullptr};  // A, B, C|D for gemm_run_host
@@ -969,10 +970,28 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
         std::memset(&plan->last, 0, sizeof(plan->last));
         return GEMM15_OK;
     }
-    const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
+    const int G1 = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
+    // SM-pair tiles when the groups fill a wave of them and rounding each group's
+    // rows up to 256 instead of 128 adds at most ~15% rows
+    int cg = 1;
+    const int clusters = std::min(pair_clusters(plan), G1 / 2);
+    const bool pair_ok = bn == 256 || plan->elem != ELEM_E4M3;
+    if (clusters > 0 && pair_ok && plan->opt.cta_group != 1) {
+        int64_t tiles2 = 0, rows1 = 0, rows2 = 0;
+        for (const Prob& p : probs) {
+            tiles2 += cdiv(p.M, 2 * TILE_M) * cdiv(p.N, bn);
+            rows1 += cdiv(p.M, TILE_M) * TILE_M;
+            rows2 += cdiv(p.M, 2 * TILE_M) * 2 * TILE_M;
+        }
+        if (plan->opt.cta_group == 2 ||
+            (bn == 256 && tiles2 >= clusters && rows2 * 100 <= rows1 * 115))
+            cg = 2;
+    }
+    const int G = cg == 2 ? clusters : G1;  // scheduling units
     int32_t tiles = 0;
     const bool reuse = plan->d_groups && plan->groups_ng == ng && plan->groups_key_c == has_c &&
                        plan->groups_key_bn == bn && plan->groups_key_raster == plan->opt.raster &&
+                       plan->groups_key_cg == cg &&
                        plan->groups_key.size() == static_cast<size_t>(count) &&
                        std::memcmp(plan->groups_key.data(), problems,
                                    sizeof(gemm15_problem_t) * static_cast<size_t>(count)) == 0;
@@ -1010,13 +1029,13 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
             if (p.a_kmajor != probs[0].a_kmajor || p.b_kmajor != probs[0].b_kmajor) mixed_layout = true;
             GroupEntry& e = plan->h_groups[i];
             std::memset(&e, 0, sizeof(e));
-            if (!operand_maps(plan, p, bn, &e.tmA, &e.tmB)) return GEMM15_ERR_CUDA;
+            if (!operand_maps(plan, p, bn / cg, &e.tmA, &e.tmB)) return GEMM15_ERR_CUDA;
             if (!output_maps(plan, p, has_c, &e.tmC, &e.tmD)) return GEMM15_ERR_CUDA;
             e.M = static_cast<int32_t>(p.M);
             e.N = static_cast<int32_t>(p.N);
             e.K = static_cast<int32_t>(p.K);
             e.k_blocks = static_cast<int32_t>(cdiv(p.K, bk));
-            e.m_blocks = static_cast<int32_t>(cdiv(p.M, TILE_M));
+            e.m_blocks = static_cast<int32_t>(cdiv(p.M, TILE_M * cg));
             e.n_blocks = static_cast<int32_t>(cdiv(p.N, bn));
             e.tile_start = tiles;
             e.has_c = has_c;
@@ -1025,7 +1044,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
             e.C = has_c ? p.C : nullptr;
             e.ldc = p.ldc;
             e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
-                                            : std::min<int32_t>(e.m_blocks, 16);
+                                            : std::min<int32_t>(e.m_blocks, cg == 2 ? 8 : 16);
             const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;
             if (tiles + t > (1ll << 30)) return GEMM15_ERR_INVALID_ARG;
             tiles += static_cast<int32_t>(t);
@@ -1039,6 +1058,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
         plan->groups_key_c = has_c;
         plan->groups_key_bn = bn;
         plan->groups_key_raster = plan->opt.raster;
+        plan->groups_key_cg = cg;
         plan->groups_tiles = tiles;
         plan->groups_ng = ng;
     }
@@ -1053,7 +1073,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     gp.beta = beta;
     gp.act = static_cast<int>(plan->desc.epilogue);
     gp.has_c = has_c;
-    fill_layout(plan, gp, probs[0].a_kmajor, probs[0].b_kmajor, bn);
+    fill_layout(plan, gp, probs[0].a_kmajor, probs[0].b_kmajor, bn, cg);
     gp.ws = plan->d_ws;
     gp.flags = plan->d_flags;
     gp.status = plan->d_status;
@@ -1062,19 +1082,20 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     gp.fault_skip_flag = -1;
     gp.groups = plan->d_groups;
     gp.num_groups = ng;
-    const int grid = std::min(G, tiles);
+    const int grid = std::min(G, tiles) * cg;
     {
         gemm15_status_t tst = attach_trace(plan, gp, grid, s);
         if (tst != GEMM15_OK) return tst;
     }
-    if (launch_kernel(plan->elem, bn, 1, gp, grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    if (launch_kernel(plan->elem, bn, cg, gp, grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
     Decision d;
     d.bn = bn;
     d.bk = bk;
+    d.cg = cg;
     d.sched = SCHED_DP;
     d.grid = grid;
     d.tiles = tiles;
-    d.raster = 16;
+    d.raster = cg == 2 ? 8 : 16;
     record_config(plan, d, 1);
     return GEMM15_OK;
 }

@@ -54,6 +54,26 @@ def test_batched_matches_oracle_per_entry(dtype, a_col, b_col, share_b, pad):
             assert torch.isnan(Dh[b * sd + M * N:(b + 1) * sd]).all(), "wrote between entries"
 
 
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_batched_tile_shapes(cta_group):
+    """The same batch on single-SM and on SM-pair tiles."""
+    batch, M, N, K = 6, 392, 520, 264
+    probs = [inputs.random_problem(M, N, K, dtype="bf16", beta=1.0, act="tanh", seed=b)
+             for b in range(batch)]
+    A = torch.stack([p.A for p in probs]).cuda()
+    B = torch.stack([p.B for p in probs]).cuda()
+    C = torch.stack([p.C for p in probs]).cuda()
+    D = torch.empty(batch, M, N, dtype=torch.bfloat16, device="cuda")
+    plan = g.Plan("bf16", epilogue="tanh").set(g.OPT_CTA_GROUP, cta_group)
+    plan.batched(A, B, C, D, M, N, K, batch, M * K, K * N, M * N, M * N, beta=1.0)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    assert plan.last_config()["cta_group"] == cta_group
+    Dh = D.cpu()
+    for b, p in enumerate(probs):
+        assert_matches_oracle(p, inputs.bits(Dh[b]))
+
+
 def test_batched_argument_errors():
     M, N, K = 64, 128, 64
     p = inputs.random_problem(M, N, K, beta=1.0)

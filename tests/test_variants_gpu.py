@@ -174,11 +174,31 @@ def test_grouped_config4_full():
     plan = g.Plan("f16")
     outs = _run_grouped(probs, plan)
     cfg = plan.last_config()
-    assert cfg["tiles"] == sum(((p.M + 127) // 128) * 16 for p in probs)
+    rows = 128 * cfg["cta_group"]
+    assert cfg["tiles"] == sum(((p.M + rows - 1) // rows) * 16 for p in probs)
     for i in (0, 7, 19, 31):
         p = probs[i]
         for rows in sample_rows(p.M, count=2, span=32, seed=i):
             assert_matches_oracle(p, outs[i], rows=rows)
+
+
+@pytest.mark.parametrize("dtype,a_col,b_col", [("f16", False, False), ("bf16", True, False),
+                                               ("f16", False, True), ("e4m3", False, False)])
+def test_grouped_on_sm_pair_tiles(dtype, a_col, b_col):
+    """Groups of ragged M (down to 1 row) on 256 x 256 SM-pair tiles.  N and K
+    are multiples of 16 (fp8 rows), M of 8 where A is column-major."""
+    ms = [64, 200, 8, 392, 520] if a_col else [64, 200, 1, 385, 520]
+    sizes = list(zip(ms, [256, 272, 16, 512, 1040], [128, 400, 128, 144, 528]))
+    probs = [inputs.random_problem(M, N, K, dtype=dtype, beta=0.0 if dtype == "e4m3" else 0.5,
+                                   alpha=1.5, relu=True, a_col_major=a_col, b_col_major=b_col,
+                                   seed=i) for i, (M, N, K) in enumerate(sizes)]
+    plan = plan_for(probs[0], cta_group=2)
+    outs = _run_grouped(probs, plan)
+    cfg = plan.last_config()
+    assert cfg["cta_group"] == 2 and cfg["tile_m"] == 256
+    assert cfg["tiles"] == sum(((M + 255) // 256) * ((N + 255) // 256) for M, N, _ in sizes)
+    for p, d in zip(probs, outs):
+        assert_matches_oracle(p, d)
 
 
 def test_grouped_skips_empty_groups_and_rejects_k_zero():
