@@ -399,8 +399,9 @@ cudaError_t launch_kernel(int elem, int bn, int cg, const GemmParams& gp, int gr
 }
 
 cudaError_t launch_reduce_kernel(int out_elem, const ReduceParams& rp, cudaStream_t s, int num_sms) {
-    const int64_t work = static_cast<int64_t>(rp.M) * ((rp.N + 7) / 8);
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(work, 256), num_sms * 8)));
+    const int64_t work = static_cast<int64_t>(rp.M) * cdiv(rp.N, REDUCE_COLS);
+    const int grid = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(cdiv(work, REDUCE_THREADS), num_sms * 16)));
     return out_elem == ELEM_F16 ? launch_reduce<ELEM_F16>(rp, grid, s) : launch_reduce<ELEM_BF16>(rp, grid, s);
 }
 

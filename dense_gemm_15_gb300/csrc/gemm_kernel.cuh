@@ -1089,11 +1089,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // D = act(alpha * sum_s partial_s + beta * C + bias) for split-K runs (splits
 // >= 1), or D = act(beta * C + bias) when K == 0 (splits == 0).  Each thread
-// owns 8 consecutive columns of one row; partial tiles are summed in split order.
+// owns REDUCE_COLS consecutive columns of one row; partial tiles are summed in
+// split order, eight splits' loads in flight at a time.
 template <int ELEM>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     using OutT = typename OutType<ELEM>::T;
-    const int64_t nv = (p.N + 7) / 8;
+    constexpr int V = REDUCE_COLS;
+    const int64_t nv = (p.N + V - 1) / V;
     const int64_t total = static_cast<int64_t>(p.M) * nv;
     float alpha = p.alpha;
     if (p.scale_a) alpha *= __ldg(p.scale_a);
@@ -1101,50 +1103,51 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int32_t m = static_cast<int32_t>(idx / nv);
-        const int32_t n = static_cast<int32_t>(idx - static_cast<int64_t>(m) * nv) * 8;
-        float acc[8];
+        const int32_t n = static_cast<int32_t>(idx - static_cast<int64_t>(m) * nv) * V;
+        float acc[V];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
+        for (int t = 0; t < V; ++t) acc[t] = 0.0f;
         if (p.splits > 0) {
             const int32_t mb = m / TILE_M, r = m - mb * TILE_M;
             const int32_t nb = n / p.tile_n, cc = n - nb * p.tile_n;
             const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;
             const float* src = p.ws + static_cast<size_t>(mb * p.n_blocks + nb) * p.splits * tile_elems +
                                static_cast<size_t>(r) * p.tile_n + cc;
-            for (int32_t s = 0; s < p.splits; ++s) {
+            constexpr int U = 8;
+            int32_t s = 0;
+            for (; s + U <= p.splits; s += U) {
+                float4 a[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) a[u] = __ldcg(reinterpret_cast<const float4*>(src + u * tile_elems));
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    acc[0] += a[u].x; acc[1] += a[u].y; acc[2] += a[u].z; acc[3] += a[u].w;
+                }
+                src += U * tile_elems;
+            }
+            for (; s < p.splits; ++s) {
                 const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-                const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 1);
                 acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
                 src += tile_elems;
             }
         }
-        const int nvalid = min(8, p.N - n);
-        float bias[8];
+        const int nvalid = min(V, p.N - n);
+        float bias[V];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) bias[t] = 0.0f;
+        for (int t = 0; t < V; ++t) bias[t] = 0.0f;
         if (p.bias) {
             const uint16_t* bv = static_cast<const uint16_t*>(p.bias);
-            if (p.bias_rows) {
-                const float b = half_bits_to_float<ELEM>(__ldg(bv + m));
 #pragma unroll
-                for (int t = 0; t < 8; ++t) bias[t] = b;
-            } else {
-                const uint4 b8 = load_bias8(p.bias, n, p.N);
-                const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 f = unpack2<ELEM>(bw[t]);
-                    bias[2 * t] = f.x;
-                    bias[2 * t + 1] = f.y;
-                }
+            for (int t = 0; t < V; ++t) {
+                if (p.bias_rows) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + m));
+                else if (t < nvalid) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + n + t));
             }
         }
         const OutT* crow = reinterpret_cast<const OutT*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
         OutT* drow = reinterpret_cast<OutT*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
-        float o[8];
+        float o[V];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < V; ++t) {
             float x = alpha * acc[t];
             if (p.has_c && t < nvalid) {
                 float cv;
@@ -1154,10 +1157,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
             }
             o[t] = activate(x + bias[t], p.act);
         }
-        if (nvalid == 8) {
-            *reinterpret_cast<uint4*>(drow) =
-                make_uint4(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]),
-                           pack2<ELEM>(o[4], o[5]), pack2<ELEM>(o[6], o[7]));
+        if (nvalid == V) {
+            *reinterpret_cast<uint2*>(drow) = make_uint2(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]));
         } else {
             for (int t = 0; t < nvalid; ++t) {
                 if constexpr (ELEM == ELEM_F16) drow[t] = __float2half_rn(o[t]);

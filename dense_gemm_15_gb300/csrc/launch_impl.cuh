@@ -69,7 +69,7 @@ int max_pair_clusters() {
 
 template <int ELEM>
 cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream) {
-    splitk_reduce_kernel<ELEM><<<grid, 256, 0, stream>>>(p);
+    splitk_reduce_kernel<ELEM><<<grid, REDUCE_THREADS, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
