@@ -85,7 +85,7 @@ class Problem:
     def __init__(self, name, A, B, C, M, N, K, alpha=1.0, beta=0.0, relu=False,
                  a_dtype="f16", b_dtype="f16", c_dtype="f16", d_dtype="f16",
                  a_col_major=False, b_col_major=False, scale_a=1.0, scale_b=1.0,
-                 act=None, bias=None):
+                 act=None, bias=None, aux=None, aux_op=None):
         self.name = name
         self.A, self.B, self.C = A, B, C
         self.M, self.N, self.K = M, N, K
@@ -94,6 +94,9 @@ class Problem:
         # optional per-column bias vector (N elements of the output type)
         self.act = act or ("relu" if relu else "linear")
         self.bias = bias
+        # optional auxiliary M x N tensor entering the activated value by
+        # aux_op ("add", "sub", "mul", "div")
+        self.aux, self.aux_op = aux, aux_op
         self.a_dtype, self.b_dtype = a_dtype, b_dtype
         self.c_dtype, self.d_dtype = c_dtype, d_dtype
         self.a_col_major, self.b_col_major = a_col_major, b_col_major
@@ -187,9 +190,12 @@ def config5b(M=8192, N=8192, K=8192, scale_a=1.0, scale_b=1.0, seed=0) -> Proble
 
 def random_problem(M, N, K, dtype="f16", out_dtype=None, alpha=1.0, beta=0.0, relu=False,
                    a_col_major=False, b_col_major=False, seed=0, lo=-1.0, hi=1.0,
-                   scale_a=1.0, scale_b=1.0, wid=9, act=None, bias=False) -> Problem:
+                   scale_a=1.0, scale_b=1.0, wid=9, act=None, bias=False,
+                   aux_op=None) -> Problem:
     """A small seeded problem of any shape, layout and dtype, for edge-case tests
-    (``bias=True`` adds a U[lo, hi] bias vector of N output-type elements)."""
+    (``bias=True`` adds a U[lo, hi] bias vector of N output-type elements;
+    ``aux_op`` adds an M x N auxiliary tensor, U[0.5, 2] for "div" so that no
+    divisor is near zero, U[lo, hi] otherwise)."""
     out_dtype = out_dtype or ("bf16" if dtype == "e4m3" else dtype)
     key = (M * 1_000_003 + N * 10_007 + K * 101 + int(a_col_major) * 2 + int(b_col_major)) % (2**31)
     sa, sb = _mk((M, K), (K, N), a_col_major, b_col_major)
@@ -201,7 +207,11 @@ def random_problem(M, N, K, dtype="f16", out_dtype=None, alpha=1.0, beta=0.0, re
         B = uniform(sb, lo, hi, dtype, wid, key + 1, seed)
     C = uniform((M, N), lo, hi, out_dtype, wid, key + 2, seed) if beta != 0.0 else None
     bv = uniform((N,), lo, hi, out_dtype, wid, key + 3, seed) if bias else None
+    zv = None
+    if aux_op:
+        zlo, zhi = (0.5, 2.0) if aux_op == "div" else (lo, hi)
+        zv = uniform((M, N), zlo, zhi, out_dtype, wid, key + 4, seed)
     return Problem("random_%dx%dx%d" % (M, N, K), A, B, C, M, N, K, alpha=alpha, beta=beta,
                    relu=relu, a_dtype=dtype, b_dtype=dtype, c_dtype=out_dtype,
                    d_dtype=out_dtype, a_col_major=a_col_major, b_col_major=b_col_major,
-                   scale_a=scale_a, scale_b=scale_b, act=act, bias=bv)
+                   scale_a=scale_a, scale_b=scale_b, act=act, bias=bv, aux=zv, aux_op=aux_op)

@@ -24,6 +24,7 @@ import numpy as np
 
 F16, BF16, F32, E4M3, F64 = 0, 1, 2, 3, 4
 ACTS = {"linear": 0, "relu": 1, "sigmoid": 2, "tanh": 3}
+AUX_OPS = {None: 0, "add": 1, "sub": 2, "mul": 3, "div": 4}
 _NAMES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3, "f64": F64}
 _ITEMSIZE = {F16: 2, BF16: 2, F32: 4, E4M3: 1, F64: 8}
 
@@ -58,7 +59,7 @@ def _load():
             lib.oracle_gemm.restype = i32
             lib.oracle_gemm.argtypes = [vp, i32, i64, i32, vp, i32, i64, i32, vp, i32, i64,
                                         vp, i64, i64, i64, i64, dbl, dbl, dbl, dbl,
-                                        i32, vp, i32, i32, i64, i64, i32]
+                                        i32, vp, i32, vp, i32, i64, i32, i32, i64, i64, i32]
             lib.oracle_round_f16_array.argtypes = [vp, vp, i64]
             lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
             lib.oracle_decode_array.argtypes = [vp, i32, vp, i64]
@@ -87,13 +88,15 @@ def default_threads() -> int:
 def gemm(a, a_dtype, b, b_dtype, c=None, c_dtype="f16", *, alpha=1.0, beta=0.0,
          relu=False, scale_a=1.0, scale_b=1.0, a_col_major=False, b_col_major=False,
          rows=None, threads=None, absolute=False, act=None, bias=None,
-         bias_dtype=None) -> np.ndarray:
+         bias_dtype=None, aux=None, aux_dtype=None, aux_op=None) -> np.ndarray:
     """D = act(alpha * s_a * s_b * (A @ B) + beta * C + bias) in float64, for
     rows ``rows = (begin, end)`` of D (all rows by default).
 
     ``act`` is "linear", "relu", "sigmoid" or "tanh" (default: "relu" if
     ``relu`` else "linear"); ``bias`` is the stored bits of an N-vector of type
-    ``bias_dtype`` (default ``c_dtype``), added to every row.
+    ``bias_dtype`` (default ``c_dtype``), added to every row; ``aux`` (M x N
+    row-major storage of type ``aux_dtype``, default ``c_dtype``) enters the
+    activated value by ``aux_op`` in "add", "sub", "mul", "div".
 
     ``absolute=True`` returns sum_k |A[i,k]| |B[k,j]| instead (the matrix the
     error bound of the checker is built from); alpha/beta/C are then unused.
@@ -132,13 +135,21 @@ def gemm(a, a_dtype, b, b_dtype, c=None, c_dtype="f16", *, alpha=1.0, beta=0.0,
             raise ValueError("bias must hold N elements")
         bcode = dtype_code(bias_dtype or c_dtype)
         bptr = bias.ctypes.data
+    zptr, zcode, ldz, op = None, 0, 0, AUX_OPS[aux_op]
+    if op:
+        aux = np.asarray(aux)
+        if aux.shape != (M, N):
+            raise ValueError("aux must be M x N row-major storage")
+        zcode = dtype_code(aux_dtype or c_dtype)
+        ldz = _leading(aux, zcode)
+        zptr = aux.ctypes.data
     r0, r1 = (0, M) if rows is None else rows
     out = np.empty((r1 - r0, N), dtype=np.float64)
     rc = lib.oracle_gemm(a.ctypes.data, ac, lda, int(a_col_major),
                          b.ctypes.data, bc, ldb, int(b_col_major),
                          cptr, cc, ldc, out.ctypes.data, N, M, N, K,
                          float(alpha), float(beta), float(scale_a), float(scale_b),
-                         act_code, bptr, bcode, int(bool(absolute)), r0, r1,
+                         act_code, bptr, bcode, zptr, zcode, ldz, op, int(bool(absolute)), r0, r1,
                          int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle_gemm failed with code %d" % rc)

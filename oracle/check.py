@@ -6,6 +6,11 @@ Tolerance for fp16 / bf16 output (element by element):
                    + u * (|beta * C_ij| + |bias_j|)
                    [+ u * |D_ref_ij| for sigmoid and tanh]
 
+and, with an auxiliary tensor Z entering after the activation, that bound E
+becomes E + u*(|Z| + |D_ref|) for add / sub, E*|Z| + u*|D_ref| for mul and
+E/|Z| + u*|D_ref| for div (the error of the activated value carried through
+the operation, plus one rounding of the result).
+
 with u = 2^-10 for fp16 and 2^-7 for bf16 output.  The first two terms are the
 stated bound of the method's accuracy target; |alpha| and s_a*s_b scale it
 with the product term it bounds (for alpha = s = 1 it is the literal bound),
@@ -48,9 +53,12 @@ def reference(prob, bits_of, rows=None, threads=None):
     a, b = bits_of(prob.A), bits_of(prob.B)
     c = bits_of(prob.C) if prob.C is not None else None
     bias = getattr(prob, "bias", None)
+    aux_op = getattr(prob, "aux_op", None)
+    aux = bits_of(prob.aux) if aux_op else None
     d_ref = gemm(a, prob.a_dtype, b, prob.b_dtype, c if prob.beta != 0.0 else None,
                  prob.c_dtype, alpha=prob.alpha, beta=prob.beta, act=_act(prob),
                  bias=bits_of(bias) if bias is not None else None, bias_dtype=prob.d_dtype,
+                 aux=aux, aux_dtype=prob.d_dtype, aux_op=aux_op,
                  scale_a=prob.scale_a, scale_b=prob.scale_b,
                  a_col_major=prob.a_col_major, b_col_major=prob.b_col_major,
                  rows=rows, threads=threads)
@@ -78,6 +86,20 @@ def compare(d_bits: np.ndarray, out_dtype: str, d_ref, absab, c64, prob):
                     out_dtype) if bias is not None else None
     tol = bound(absab, prob.alpha, prob.beta, c64, out_dtype, prob.scale_a * prob.scale_b,
                 bias64=bias64, d_ref=d_ref if _act(prob) in ("sigmoid", "tanh") else None)
+    aux_op = getattr(prob, "aux_op", None)
+    if aux_op:
+        z = _bits16(prob.aux)
+        if d_ref.shape[0] != prob.M:
+            raise ValueError("aux checks compare whole results")
+        z64 = np.abs(decode(z, out_dtype))
+        u = ROUND_UNIT[out_dtype]
+        dr = u * np.abs(np.nan_to_num(d_ref))
+        if aux_op in ("add", "sub"):
+            tol = tol + u * z64 + dr
+        elif aux_op == "mul":
+            tol = tol * z64 + dr
+        else:
+            tol = tol / z64 + dr
     err = np.abs(d - d_ref)
     ratio = np.where(np.isfinite(err), err / tol, np.inf)
     # NaN where the reference is NaN too counts as agreement.

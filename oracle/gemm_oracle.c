@@ -8,7 +8,7 @@
  * What it computes (plain definition, no blocking, no reordering of the sum):
  *
  *     D[i,j] = act( alpha * s_a * s_b * sum_{k=0..K-1} x(A[i,k]) * x(B[k,j])
- *                   + beta * x(C[i,j]) + x(bias[j]) )
+ *                   + beta * x(C[i,j]) + x(bias[j]) )  [op x(Z[i,j])]
  *
  *   - "D = A*B + C" for a RowMajor fp16 plan is the worked example of
  *     "Python packages associated with CUTLASS" (CUTLASS python/README.md),
@@ -24,6 +24,10 @@
  *     CuteDSL backend", roadmap section, names ReLU, Sigmoid and Tanh as
  *     epilogue activations).  sigmoid(v) = 1 / (1 + e^-v); tanh is the C
  *     library's.  The bias is optional (absent = 0).
+ *   - op is an optional elementwise operation with an auxiliary M x N tensor Z
+ *     (add, subtract, multiply, divide), applied to the activated value: the
+ *     EFC epilogue operations listed in the roadmap section of the CuteDSL page
+ *     (auxiliary tensor loads, elementwise add / mul / sub / div, activations).
  *   - s_a, s_b are per-tensor dequantisation scales of fp8 operands (real value
  *     = s * stored value); they are 1 for 16-bit operands.  FP8 mm support is
  *     listed in "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL
@@ -179,6 +183,8 @@ typedef struct {
     double alpha, beta, scale_a, scale_b;
     int act;                     /* 0 identity, 1 ReLU, 2 sigmoid, 3 tanh */
     const void* bias; int bias_dtype;  /* N elements, or NULL */
+    const void* aux; int aux_dtype; int64_t ldaux; int aux_op;  /* Z, row-major; op 0 none,
+                                                                   1 add, 2 sub, 3 mul, 4 div */
     int absolute;                /* 1: compute sum |a||b| (error bound), no epilogue */
     int64_t row_begin, row_end;
     const double* Bd;            /* B decoded to double, K x N row-major, or NULL */
@@ -229,6 +235,16 @@ static void oracle_row(const oracle_job* j, int64_t i, double* acc) {
         case 3: v = tanh(v); break;
         default: break;
         }
+        if (j->aux_op) {
+            const double z = load_elem(j->aux, j->aux_dtype, i * j->ldaux + n);
+            switch (j->aux_op) {
+            case 1: v = v + z; break;
+            case 2: v = v - z; break;
+            case 3: v = v * z; break;
+            case 4: v = v / z; break;
+            default: break;
+            }
+        }
         out[n] = v;
     }
 }
@@ -258,6 +274,7 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
                 int64_t M, int64_t N, int64_t K,
                 double alpha, double beta, double scale_a, double scale_b,
                 int act, const void* bias, int bias_dtype,
+                const void* aux, int aux_dtype, int64_t ldaux, int aux_op,
                 int absolute, int64_t row_begin, int64_t row_end,
                 int nthreads) {
     if (M < 0 || N < 0 || K < 0 || row_begin < 0 || row_end > M || row_begin > row_end)
@@ -271,8 +288,9 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
     j.D = D_out; j.ldd = ldd;
     j.M = M; j.N = N; j.K = K;
     j.alpha = alpha; j.beta = beta; j.scale_a = scale_a; j.scale_b = scale_b;
-    if (act < 0 || act > 3) return 1;
+    if (act < 0 || act > 3 || aux_op < 0 || aux_op > 4 || (aux_op && !aux)) return 1;
     j.act = act; j.bias = bias; j.bias_dtype = bias_dtype; j.absolute = absolute;
+    j.aux = aux; j.aux_dtype = aux_dtype; j.ldaux = ldaux; j.aux_op = aux_op;
     j.row_begin = row_begin; j.row_end = row_end; j.next_row = row_begin;
     /* Decode B once (the same exact values load_elem would produce); if the
      * copy does not fit in memory, decode element by element instead. */

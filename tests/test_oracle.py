@@ -329,6 +329,43 @@ def test_tanh_is_twice_sigmoid_of_twice_minus_one():
     assert np.allclose(th, -oracle.gemm(a, "f16", b, "f16", alpha=-0.75, act="tanh"), atol=0)
 
 
+@pytest.mark.parametrize("op", ["add", "sub", "mul", "div"])
+def test_aux_tensor_ops_exact(op):
+    """An auxiliary M x N tensor Z entering the activated value (the EFC
+    operations of the CuteDSL page's roadmap section): small integer operands
+    and power-of-two divisors keep every value exact; applying the operation
+    before the activation would not match."""
+    g = np.random.default_rng(21)
+    A, B = g.integers(-3, 4, (9, 6)), g.integers(-3, 4, (6, 11))
+    bias = g.integers(-5, 6, 11)
+    Z = g.choice([-4.0, -2.0, -1.0, 1.0, 2.0, 4.0], (9, 11))
+    d = oracle.gemm(_f16i(A), "f16", _f16i(B), "f16", act="relu", bias=_f16i(bias),
+                    aux=_f16i(Z), aux_op=op)
+    r = np.maximum(A @ B + bias[None, :], 0).astype(np.float64)
+    want = {"add": r + Z, "sub": r - Z, "mul": r * Z, "div": r / Z}[op]
+    assert np.array_equal(d, want)
+    pre = (A @ B + bias[None, :]).astype(np.float64)
+    wrong = np.maximum({"add": pre + Z, "sub": pre - Z, "mul": pre * Z, "div": pre / Z}[op], 0)
+    assert not np.array_equal(d, wrong)
+
+
+def test_aux_ops_invert_each_other():
+    """(X * Z) / Z and (X / Z) * Z give X back exactly for Z = 2, and X - Z
+    plus Z within the rounding of X - Z, with X the oracle's own result
+    without Z."""
+    p = inputs.random_problem(12, 20, 16, act="tanh", bias=True)
+    a, b, bv = inputs.bits(p.A), inputs.bits(p.B), inputs.bits(p.bias)
+    x = oracle.gemm(a, "f16", b, "f16", act="tanh", bias=bv)
+    z = np.full((12, 20), 0x4000, np.uint16)  # 2.0
+    assert np.array_equal(oracle.gemm(a, "f16", b, "f16", act="tanh", bias=bv, aux=z,
+                                      aux_op="mul") / 2.0, x)
+    assert np.array_equal(oracle.gemm(a, "f16", b, "f16", act="tanh", bias=bv, aux=z,
+                                      aux_op="div") * 2.0, x)
+    # x - 2 rounds to the spacing of numbers near 2: equal within that spacing
+    assert np.allclose(oracle.gemm(a, "f16", b, "f16", act="tanh", bias=bv, aux=z,
+                                   aux_op="sub") + 2.0, x, rtol=0, atol=2.0 ** -50)
+
+
 # ---------------------------------------------------------------- cross-checks
 
 def test_numpy_float64_cross_check():
