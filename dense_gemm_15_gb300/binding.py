@@ -19,6 +19,7 @@ F16, BF16, F32, E4M3 = 0, 1, 2, 3
 ROW_MAJOR, COL_MAJOR = 0, 1
 EPI_LINEAR, EPI_RELU, EPI_SIGMOID, EPI_TANH = 0, 1, 2, 3
 EPILOGUES = {"linear": EPI_LINEAR, "relu": EPI_RELU, "sigmoid": EPI_SIGMOID, "tanh": EPI_TANH}
+AUX_OPS = {None: 0, "add": 1, "sub": 2, "mul": 3, "div": 4}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_OOM, \
     ERR_DEVICE_FAULT, ERR_NO_DEVICE, ERR_BAD_PLAN = range(10)
 OPT_SCHEDULE, OPT_SPLITS, OPT_CTA_GROUP, OPT_TILE_N, OPT_RASTER, OPT_GRID, \
@@ -49,7 +50,8 @@ class Args(ctypes.Structure):
                 ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64), ("M", ctypes.c_int64),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("alpha", ctypes.c_float),
                 ("beta", ctypes.c_float), ("scale_a", ctypes.c_void_p),
-                ("scale_b", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+                ("scale_b", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("aux", ctypes.c_void_p), ("ldaux", ctypes.c_int64), ("aux_op", ctypes.c_int32)]
 
 
 class Problem(ctypes.Structure):
@@ -217,9 +219,12 @@ def grouped_gemm_run(plan, problems, alpha=1.0, beta=0.0, stream=None):
 
 
 def gemm_run_args(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0, ldd=0,
-                  scale_a=None, scale_b=None, bias=None, stream=None):
+                  scale_a=None, scale_b=None, bias=None, aux=None, ldaux=0, aux_op=None,
+                  stream=None):
+    """aux_op: None, "add", "sub", "mul", "div" (or its code)."""
+    op = AUX_OPS[aux_op] if aux_op is None or isinstance(aux_op, str) else int(aux_op)
     args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
-                _ptr(scale_a), _ptr(scale_b), _ptr(bias))
+                _ptr(scale_a), _ptr(scale_b), _ptr(bias), _ptr(aux), ldaux, op)
     return load().gemm_run_args(plan, ctypes.byref(args), _stream(stream))
 
 
@@ -228,7 +233,7 @@ def gemm_plan_autotune(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ld
                        stream=None):
     """Returns (status, [result dicts, fastest first])."""
     args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
-                _ptr(scale_a), _ptr(scale_b), _ptr(bias))
+                _ptr(scale_a), _ptr(scale_b), _ptr(bias), None, 0, 0)
     cap = 64
     out = (TuneResult * cap)()
     n = ctypes.c_int32()
@@ -319,7 +324,8 @@ class Plan:
         return self
 
     def run(self, A, B, C, D, M=None, N=None, K=None, alpha=1.0, beta=0.0, scale_a=None,
-            scale_b=None, stream=None, lda=None, ldb=None, ldc=None, ldd=None, bias=None):
+            scale_b=None, stream=None, lda=None, ldb=None, ldc=None, ldd=None, bias=None,
+            aux=None, aux_op=None, ldaux=0):
         la, lb, lcd = self.layouts
         if M is None:
             M = A.shape[0] if la == ROW_MAJOR else A.shape[1]
@@ -329,9 +335,9 @@ class Plan:
         ldb = ldb or (N if lb == ROW_MAJOR else K)
         ldd = ldd or (N if lcd == ROW_MAJOR else M)
         ldc = ldc or ldd
-        if bias is not None:
+        if bias is not None or aux_op is not None:
             st = gemm_run_args(self.handle, A, B, C, D, M, N, K, alpha, beta, lda, ldb, ldc, ldd,
-                               scale_a, scale_b, bias, stream)
+                               scale_a, scale_b, bias, aux, ldaux, aux_op, stream)
         else:
             st = gemm_run_ex(self.handle, A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta,
                              scale_a, scale_b, stream)

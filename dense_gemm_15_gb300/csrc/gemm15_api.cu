@@ -172,6 +172,9 @@ struct Prob {
     int64_t ldd;
     const void* bias = nullptr;  // per output column of the user's D, or null
     bool bias_rows = false;      // the bias runs along the computed rows (D^T)
+    const void* aux = nullptr;   // auxiliary tensor Z (layout of C / D), or null
+    int64_t ldaux = 0;
+    int aux_op = 0;
 };
 
 // Column-major C/D: compute D^T = B^T . A^T, which is row-major N x M.
@@ -216,6 +219,11 @@ gemm15_status_t check_operands(const gemm15_plan* plan, const Prob& p, float bet
         if (!aligned16(p.C) || (p.ldc * eo) % 16) return GEMM15_ERR_ALIGNMENT;
     }
     if (p.bias && !aligned16(p.bias)) return GEMM15_ERR_ALIGNMENT;
+    if (p.aux_op < 0 || p.aux_op > 4) return GEMM15_ERR_INVALID_ARG;
+    if (p.aux_op) {
+        if (!p.aux || p.ldaux < p.N) return GEMM15_ERR_INVALID_ARG;
+        if (!aligned16(p.aux) || (p.ldaux * eo) % 16) return GEMM15_ERR_ALIGNMENT;
+    }
     return GEMM15_OK;
 }
 
@@ -530,6 +538,9 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.has_c = has_c;
         rp.bias = p.bias;
         rp.bias_rows = p.bias_rows;
+        rp.aux = p.aux;
+        rp.ldaux = p.ldaux;
+        rp.aux_op = p.aux_op;
         if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
         Decision d;
         d.sched = SCHED_SPLIT;
@@ -570,6 +581,9 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.act = act;
     gp.bias = d.sched == SCHED_SPLIT ? nullptr : p.bias;  // split-K: the reduction adds it
     gp.bias_rows = p.bias_rows;
+    gp.aux = p.aux;
+    gp.ldaux = p.ldaux;
+    gp.aux_op = d.sched == SCHED_SPLIT ? 0 : p.aux_op;
     fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.ws = plan->d_ws;
     gp.flags = plan->d_flags;
@@ -603,6 +617,9 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.has_c = has_c;
         rp.bias = p.bias;
         rp.bias_rows = p.bias_rows;
+        rp.aux = p.aux;
+        rp.ldaux = p.ldaux;
+        rp.aux_op = p.aux_op;
         if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
         ++launches;
     }
@@ -734,6 +751,9 @@ gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* a, void* 
     const int64_t ldd = a->ldd ? a->ldd : (cd_row ? a->N : a->M);
     Prob p = normalise(plan, a->M, a->N, a->K, a->A, lda, a->B, ldb, a->C, ldc, a->D, ldd);
     p.bias = a->bias;
+    p.aux_op = a->aux_op;
+    p.aux = a->aux_op ? a->aux : nullptr;
+    p.ldaux = a->ldaux ? a->ldaux : (cd_row ? a->N : a->M);
     return run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b,
                      static_cast<cudaStream_t>(stream));
 }
@@ -757,6 +777,9 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
                        a->ldc ? a->ldc : (cd_row ? a->N : a->M), a->D,
                        a->ldd ? a->ldd : (cd_row ? a->N : a->M));
     p.bias = a->bias;
+    p.aux_op = a->aux_op;
+    p.aux = a->aux_op ? a->aux : nullptr;
+    p.ldaux = a->ldaux ? a->ldaux : (cd_row ? a->N : a->M);
     gemm15_status_t st = check_operands(plan, p, a->beta);
     if (st != GEMM15_OK) return st;
     if (p.M == 0 || p.N == 0 || p.K == 0) return GEMM15_OK;  // one fixed path: nothing to choose

@@ -153,6 +153,17 @@ __device__ __forceinline__ float activate(float x, int act) {
     }
 }
 
+// v op z for the auxiliary-tensor operation (1 add, 2 sub, 3 mul, 4 div).
+__device__ __forceinline__ float aux_apply(float v, float z, int op) {
+    switch (op) {
+        case 1: return v + z;
+        case 2: return v - z;
+        case 3: return v * z;
+        case 4: return v / z;
+        default: return v;
+    }
+}
+
 // Applies the activation to n values held in registers: one uniform branch,
 // then straight-line code.
 template <int NV>
@@ -999,6 +1010,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 activate_all(v, act);
+                if (p.aux_op && my_row < M) {
+                    // the auxiliary tensor's 64 columns of this row, 16 bytes at a time
+                    const uint16_t* zrow = static_cast<const uint16_t*>(p.aux) +
+                                           static_cast<int64_t>(my_row) * p.ldaux + n0 + col0;
+                    uint4 zv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) zv[j] = load_bias8(zrow + 8 * j, 0, left - 8 * j);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t zw[4] = {zv[j].x, zv[j].y, zv[j].z, zv[j].w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f = unpack2<ELEM>(zw[t]);
+                            v[8 * j + 2 * t] = aux_apply(v[8 * j + 2 * t], f.x, p.aux_op);
+                            v[8 * j + 2 * t + 1] = aux_apply(v[8 * j + 2 * t + 1], f.y, p.aux_op);
+                        }
+                    }
+                }
                 uint32_t pk[8][4];
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -1156,6 +1185,10 @@ __global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __g
                 x = fmaf(p.beta, cv, x);
             }
             o[t] = activate(x + bias[t], p.act);
+            if (p.aux_op && t < nvalid) {
+                const uint16_t z = static_cast<const uint16_t*>(p.aux)[static_cast<int64_t>(m) * p.ldaux + n + t];
+                o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);
+            }
         }
         if (nvalid == V) {
             *reinterpret_cast<uint2*>(drow) = make_uint2(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]));

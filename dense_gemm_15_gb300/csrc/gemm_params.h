@@ -53,6 +53,9 @@ struct GemmParams {
     int32_t act;                      // Activation
     int32_t bias_rows;                // bias indexed by output row (1) or column (0)
     const void* bias;                 // 16-bit bias vector (device), or null
+    const void* aux;                  // auxiliary tensor Z (output type, row-major), or null
+    int64_t ldaux;
+    int32_t aux_op;                   // 0 none, 1 add, 2 sub, 3 mul, 4 div
     // operand layouts in shared memory (bytes) and the MMA instruction descriptor
     uint32_t a_kmajor, b_kmajor;
     uint32_t a_lbo, a_sbo, a_kstep;
@@ -97,6 +100,9 @@ struct ReduceParams {
     int32_t act, has_c;
     const void* bias;                 // as in GemmParams
     int32_t bias_rows;
+    const void* aux;
+    int64_t ldaux;
+    int32_t aux_op;
 };
 
 }  // namespace g15

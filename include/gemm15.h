@@ -132,6 +132,18 @@ gemm15_status_t gemm_run_ex(gemm15_plan_t plan, const void* A, int64_t lda, cons
                             int64_t M, int64_t N, int64_t K, float alpha, float beta,
                             const float* scale_a, const float* scale_b, void* stream);
 
+/* Elementwise operation of an auxiliary tensor Z with the activated value
+ * (the EFC epilogue operations -- auxiliary tensor loads, elementwise add /
+ * sub / mul / div -- of the roadmap section of "Generating State-of-the-Art
+ * GEMMs with TorchInductor's CuteDSL backend"). */
+typedef enum {
+    GEMM15_AUX_NONE = 0,
+    GEMM15_AUX_ADD = 1, /* D = act(...) + Z */
+    GEMM15_AUX_SUB = 2, /* D = act(...) - Z */
+    GEMM15_AUX_MUL = 3, /* D = act(...) * Z */
+    GEMM15_AUX_DIV = 4  /* D = act(...) / Z (IEEE division) */
+} gemm15_aux_op_t;
+
 /* Per-run arguments of gemm_run_args (leading dimensions 0 = packed, as in
  * gemm_run). */
 typedef struct {
@@ -148,14 +160,19 @@ typedef struct {
     const float* scale_a; /* E4M3 plans: DEVICE float, NULL = 1 (as gemm_run_ex) */
     const float* scale_b;
     const void* bias;     /* DEVICE vector of N elements of D's type, or NULL */
+    const void* aux;      /* DEVICE M x N tensor Z of D's type and layout, or NULL */
+    int64_t ldaux;        /* its leading dimension (0 = packed) */
+    int32_t aux_op;       /* gemm15_aux_op_t; GEMM15_AUX_NONE ignores aux */
 } gemm15_args_t;
 
-/* D = act(alpha * s_a * s_b * (A . B) + beta * C + bias), bias[j] added to
- * every element of column j of D -- the LinearCombinationBiasReLU epilogue of
- * the kwkr.cn blog "CUTLASS Python接口", section 5.2 (bias vector of length N in
- * the output type, fp32 arithmetic, activation last).  Everything else as
- * gemm_run_ex; the bias pointer must be 16-byte aligned (ALIGNMENT otherwise).
- * With K == 0, D = act(beta * C + bias). */
+/* D = act(alpha * s_a * s_b * (A . B) + beta * C + bias) [op Z], bias[j]
+ * added to every element of column j of D -- the LinearCombinationBiasReLU
+ * epilogue of the kwkr.cn blog "CUTLASS Python接口", section 5.2 (bias vector of
+ * length N in the output type, fp32 arithmetic, activation last) -- and an
+ * optional auxiliary tensor Z entering the activated value by aux_op.
+ * Everything else as gemm_run_ex; the bias and aux pointers and ldaux * 2 must
+ * be 16-byte aligned (ALIGNMENT otherwise), ldaux >= the contiguous extent
+ * (INVALID_ARG otherwise).  With K == 0, D = act(beta * C + bias) [op Z]. */
 gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* args, void* stream);
 
 /* End-to-end variant for callers holding HOST buffers (packed layouts as in

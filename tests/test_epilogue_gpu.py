@@ -121,3 +121,69 @@ def test_misaligned_bias_is_rejected():
     bias = torch.zeros(136, dtype=torch.float16, device="cuda")[4:]  # 8-byte offset
     st = g.gemm_run_args(plan.handle, A, B, None, D, 64, 128, 64, 1.0, 0.0, bias=bias)
     assert st == g.ERR_ALIGNMENT
+
+
+def _run_aux(plan, prob, col_major_cd=False):
+    A, B = prob.A.cuda(), prob.B.cuda()
+    C = prob.C.cuda() if prob.C is not None else None
+    Z = prob.aux.cuda()
+    bias = prob.bias.cuda() if prob.bias is not None else None
+    dt = inputs.TORCH_DTYPE[prob.d_dtype]
+    if col_major_cd:
+        C = C.t().contiguous() if C is not None else None
+        Z = Z.t().contiguous()
+        D = torch.full((prob.N, prob.M), float("nan"), dtype=dt, device="cuda")
+    else:
+        D = torch.full((prob.M, prob.N), float("nan"), dtype=dt, device="cuda")
+    st = g.gemm_run_args(plan.handle, A, B, C, D, prob.M, prob.N, prob.K, prob.alpha,
+                         prob.beta, bias=bias, aux=Z, aux_op=prob.aux_op)
+    assert st == g.OK, g.status_string(st)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    Dh = D.cpu()
+    return inputs.bits(Dh.t().contiguous() if col_major_cd else Dh)
+
+
+@pytest.mark.parametrize("op", ["add", "sub", "mul", "div"])
+@pytest.mark.parametrize("act", ["relu", "sigmoid"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_aux_tensor_ops(op, act, dtype):
+    """D = act(alpha*A.B + beta*C + bias) op Z (EFC epilogue operations)."""
+    prob = inputs.random_problem(392, 520, 712, dtype=dtype, alpha=0.5, beta=0.5, act=act,
+                                 bias=True, aux_op=op)
+    assert_matches_oracle(prob, _run_aux(_plan(prob), prob))
+
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("col_major_cd", [False, True])
+def test_aux_under_every_schedule_and_output_layout(sched, col_major_cd):
+    prob = inputs.random_problem(296, 264, 2048, dtype="bf16", beta=1.0, act="tanh",
+                                 aux_op="mul")
+    plan = _plan(prob, layout_cd=LAYOUT[col_major_cd], schedule=sched)
+    d = _run_aux(plan, prob, col_major_cd=col_major_cd)
+    assert plan.last_config()["schedule"] == sched
+    assert_matches_oracle(prob, d)
+
+
+def test_aux_with_ragged_n_and_k_zero():
+    prob = inputs.random_problem(75, 136, 200, beta=1.0, act="relu", aux_op="sub")
+    assert_matches_oracle(prob, _run_aux(_plan(prob), prob))
+    # N = 136 ends inside the last 64-column chunk; K = 0 runs the reduction kernel alone
+    prob0 = inputs.random_problem(40, 72, 0, beta=0.75, act="sigmoid", aux_op="div")
+    prob0.A = torch.empty(40, 0, dtype=torch.float16)
+    prob0.B = torch.empty(0, 72, dtype=torch.float16)
+    assert_matches_oracle(prob0, _run_aux(_plan(prob0), prob0))
+
+
+def test_aux_argument_errors():
+    prob = inputs.random_problem(64, 128, 64, aux_op="add")
+    plan = _plan(prob)
+    A, B = prob.A.cuda(), prob.B.cuda()
+    D = torch.empty(64, 128, dtype=torch.float16, device="cuda")
+    Z = prob.aux.cuda()
+    run = lambda **kw: g.gemm_run_args(plan.handle, A, B, None, D, 64, 128, 64, 1.0, 0.0, **kw)
+    assert run(aux=None, aux_op="add") == g.ERR_INVALID_ARG
+    assert run(aux=Z, aux_op=7) == g.ERR_INVALID_ARG
+    assert run(aux=Z, aux_op="add", ldaux=100) == g.ERR_INVALID_ARG   # < N
+    assert run(aux=Z, aux_op="add", ldaux=132) == g.ERR_ALIGNMENT     # 264 bytes
+    assert run(aux=Z, aux_op="add") == g.OK
