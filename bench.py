@@ -288,7 +288,7 @@ def run_reference(args):
     import oracle
     from dense_gemm_15_gb300 import inputs as I
     probs = get_workload(args.workload)
-    per_step = min(10.0, 120.0 / max(1, args.steps + args.warmup))
+    per_step = min(args.cpu_budget, 120.0 / max(1, args.steps + args.warmup))
     _, cores, desc, _ = cpu_oracle_sample(probs, budget_s=per_step)
     p = max(probs, key=lambda q: q.flops)
     rows = int(desc.split("..")[1].split()[0])
