@@ -238,6 +238,7 @@ struct Decision {
     int32_t m_blocks = 0, n_blocks = 0, tiles = 0, k_blocks = 0;
     int32_t dp_tiles = 0, splits = 1, raster = 1;
     int64_t sk_units = 0;
+    bool balanced = false;  // split-K over a stream-K partition of all units
     size_t ws_bytes = 0;
     int flags = 0;
 };
@@ -338,6 +339,12 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
     }
     d.cg = cg;
     d.sched = sched;
+    // balanced split-K (option splits = -1): the k iterations of all tiles cut
+    // evenly over every unit (pieces may straddle two tiles); the reduction
+    // kernel finds each tile's pieces from the partition.  Measured slower than
+    // whole splits per tile on the GB300 decode shapes (each unit leaves up to
+    // two partial tiles), so it is never chosen automatically.
+    d.balanced = sched == SCHED_SPLIT && cg == 1 && o.splits == -1 && d.tiles < G;
     d.raster = o.raster > 0 ? std::min<int32_t>(o.raster, d.m_blocks)
                             : std::min<int32_t>(d.m_blocks, cg == 2 ? 8 : 16);
     const size_t half_tile = static_cast<size_t>(TILE_M) * d.bn * sizeof(float);
@@ -355,6 +362,11 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
         // per unit and CTA: a tail piece and a head piece may each leave a partial tile
         d.ws_bytes = static_cast<size_t>(2 * units) * cg * half_tile;
         d.flags = 2 * units * cg;
+    } else if (d.balanced) {
+        d.sk_units = static_cast<int64_t>(d.tiles) * d.k_blocks;
+        units = static_cast<int>(std::min<int64_t>(G, d.sk_units));
+        d.splits = 0;
+        d.ws_bytes = static_cast<size_t>(2 * units) * half_tile;  // a tail and a head piece per unit
     } else {
         int splits = o.splits > 0 ? o.splits : std::max(1, G / std::max<int32_t>(d.tiles, 1));
         splits = static_cast<int>(std::min<int64_t>(splits, d.k_blocks));
@@ -569,7 +581,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.n_blocks = d.n_blocks;
     gp.tiles = d.tiles;
     gp.raster = d.raster;
-    gp.sched = d.sched;
+    gp.sched = d.balanced ? SCHED_SK : d.sched;
+    gp.sk_partials_only = d.balanced ? 1 : 0;
     gp.dp_tiles = d.dp_tiles;
     gp.splits = d.splits;
     gp.has_c = has_c && d.sched != SCHED_SPLIT;
@@ -620,6 +633,13 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.aux = p.aux;
         rp.ldaux = p.ldaux;
         rp.aux_op = p.aux_op;
+        if (d.balanced) {
+            rp.units = d.grid;
+            rp.sk_units = d.sk_units;
+            rp.k_blocks = d.k_blocks;
+            rp.m_blocks = d.m_blocks;
+            rp.raster = d.raster;
+        }
         if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
         ++launches;
     }
@@ -1181,7 +1201,7 @@ gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option,
             o.schedule = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_SPLITS:
-            if (v < 0 || v > 4096) return GEMM15_ERR_INVALID_ARG;
+            if (v < -1 || v > 4096) return GEMM15_ERR_INVALID_ARG;
             o.splits = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_CTA_GROUP:

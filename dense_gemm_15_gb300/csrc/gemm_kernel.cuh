@@ -302,6 +302,15 @@ __device__ __forceinline__ int32_t sk_slot(const Unit& un, int32_t v, bool head)
     return (2 * v + (head ? 1 : 0)) * un.cg + un.rank;
 }
 
+// Linear tile index of block (mb, nb) in the raster order of raster_coords.
+__device__ __forceinline__ int32_t raster_tile(int32_t mb, int32_t nb, int32_t m_blocks,
+                                               int32_t n_blocks, int32_t raster) {
+    const int32_t band = mb / raster;
+    const int32_t first_m = band * raster;
+    const int32_t rows = min(raster, m_blocks - first_m);
+    return band * raster * n_blocks + nb * rows + (mb - first_m);
+}
+
 __device__ __forceinline__ void raster_coords(int32_t tile, int32_t m_blocks, int32_t n_blocks,
                                               int32_t raster, int32_t& mb, int32_t& nb) {
     const int32_t band_tiles = raster * n_blocks;
@@ -434,6 +443,8 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
             }
             w.kind = owner == un.id ? WK_OWNER : WK_PEER;
         }
+        // balanced split-K: every piece goes to the workspace, the reduction adds them
+        if (p.sk_partials_only) w.kind = WK_SPLIT;
         return true;
     }
     return false;
@@ -1136,7 +1147,42 @@ __global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __g
         float acc[V];
 #pragma unroll
         for (int t = 0; t < V; ++t) acc[t] = 0.0f;
-        if (p.splits > 0) {
+        if (p.units > 0) {
+            // balanced split-K: tile t's pieces are held by units h0..h1 of the
+            // stream-K partition; h0's piece (the tile's head) sits in slot
+            // 2*h0 + 1, the others' in slot 2*v; summed in unit order
+            const int32_t mb = m / TILE_M, r = m - mb * TILE_M;
+            const int32_t nb = n / p.tile_n, cc = n - nb * p.tile_n;
+            const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;
+            const int64_t t0 = static_cast<int64_t>(raster_tile(mb, nb, p.m_blocks, p.n_blocks, p.raster)) * p.k_blocks;
+            auto begin = [&](int64_t u) { return (p.sk_units * u) / p.units; };
+            auto unit_of = [&](int64_t x) {
+                int64_t u = (x * p.units) / p.sk_units;
+                while (u > 0 && begin(u) > x) --u;
+                while (u + 1 < p.units && begin(u + 1) <= x) ++u;
+                return u;
+            };
+            const int64_t h0 = unit_of(t0), h1 = unit_of(t0 + p.k_blocks - 1);
+            const float* base = p.ws + static_cast<size_t>(r) * p.tile_n + cc;
+            const float4 a0 = __ldcg(reinterpret_cast<const float4*>(base + (2 * h0 + 1) * tile_elems));
+            acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
+            constexpr int U = 8;
+            int64_t v = h0 + 1;
+            for (; v + U - 1 <= h1; v += U) {
+                float4 a[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    a[u] = __ldcg(reinterpret_cast<const float4*>(base + 2 * (v + u) * tile_elems));
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    acc[0] += a[u].x; acc[1] += a[u].y; acc[2] += a[u].z; acc[3] += a[u].w;
+                }
+            }
+            for (; v <= h1; ++v) {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(base + 2 * v * tile_elems));
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            }
+        } else if (p.splits > 0) {
             const int32_t mb = m / TILE_M, r = m - mb * TILE_M;
             const int32_t nb = n / p.tile_n, cc = n - nb * p.tile_n;
             const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;

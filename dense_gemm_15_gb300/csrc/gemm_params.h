@@ -47,6 +47,8 @@ struct GemmParams {
     int32_t splits;                   // SPLIT: k-splits per tile
     int32_t has_c;                    // beta != 0 (C is read)
     int64_t sk_units;                 // SK: (tiles - dp_tiles) * k_blocks
+    int32_t sk_partials_only;         // SK partition whose every piece leaves a partial tile
+                                      // for the reduction kernel (balanced split-K)
     float alpha, beta;
     const float* scale_a;             // fp8 per-tensor scales (device), or null
     const float* scale_b;
@@ -103,6 +105,11 @@ struct ReduceParams {
     const void* aux;
     int64_t ldaux;
     int32_t aux_op;
+    // balanced split-K: the partials come from a stream-K partition of
+    // sk_units iterations over units units (0 = classic split-K layout)
+    int32_t units;
+    int64_t sk_units;
+    int32_t k_blocks, m_blocks, raster;
 };
 
 }  // namespace g15

@@ -237,7 +237,9 @@ const char* gemm15_status_string(gemm15_status_t status);
 /* Tuning / test options (defaults are the library's own choices). */
 typedef enum {
     GEMM15_OPT_SCHEDULE = 0,     /* 0 auto, 1 data-parallel, 2 stream-K, 3 split-K + reduce */
-    GEMM15_OPT_SPLITS = 1,       /* split-K: splits per tile (0 = auto) */
+    GEMM15_OPT_SPLITS = 1,       /* split-K: splits per tile (0 = auto; -1 = balanced:
+                                    the k iterations of all tiles cut evenly over
+                                    every SM, single-SM tiles only) */
     GEMM15_OPT_CTA_GROUP = 2,    /* 0 auto, 1 one-SM tiles, 2 SM-pair tiles */
     GEMM15_OPT_TILE_N = 3,       /* 0 auto, 128 or 256 */
     GEMM15_OPT_RASTER = 4,       /* 0 auto, else M-blocks per raster band */
@@ -263,7 +265,10 @@ typedef struct {
     int32_t schedule;    /* 1 data-parallel, 2 stream-K, 3 split-K + reduce */
     int32_t grid;        /* CTAs launched by the GEMM kernel */
     int32_t tiles;       /* output tiles */
-    int32_t splits;      /* split-K splits per tile (1 otherwise) */
+    int32_t splits;      /* split-K splits per tile (1 otherwise; 0 for balanced split-K:
+                            the k iterations of all tiles cut evenly over every SM, a
+                            piece may straddle two tiles, the reduction kernel finds
+                            each tile's pieces) */
     int32_t raster;      /* M-blocks per raster band */
     int32_t launches;    /* kernels launched by the run */
     int32_t swap_ab;     /* 1 if the run computed D^T = B^T . A^T */

@@ -11,7 +11,7 @@ LAYOUT = {False: g.ROW_MAJOR, True: g.COL_MAJOR}
 
 
 def plan_for(prob, **opts):
-    plan = g.Plan(prob.a_dtype, prob.d_dtype, relu=prob.relu,
+    plan = g.Plan(prob.a_dtype, prob.d_dtype, epilogue=prob.act,
                   layout_a=LAYOUT[prob.a_col_major], layout_b=LAYOUT[prob.b_col_major])
     for k, v in opts.items():
         plan.set(getattr(g, "OPT_" + k.upper()), v)

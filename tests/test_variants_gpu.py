@@ -389,6 +389,33 @@ def _sk_items(tr, cta, k_blocks):
     return pos, kinds
 
 
+@pytest.mark.parametrize("M,N,K,act", [(16, 8192, 2048, "linear"), (300, 1040, 4096, "relu"),
+                                       (128, 768, 16384, "tanh")])
+def test_balanced_split_k(M, N, K, act):
+    """Balanced split-K (splits = -1) cuts the k iterations of all tiles evenly
+    over every SM (32, 15 and 3 tiles; in the last case each tile's pieces come
+    from about 50 units) and the reduction kernel finds each tile's pieces from
+    the partition."""
+    prob = inputs.random_problem(M, N, K, dtype="bf16", beta=0.5, act=act, bias=True)
+    plan = plan_for(prob, schedule=g.SCHED_SPLIT, splits=-1)
+    A, B, C = prob.A.cuda(), prob.B.cuda(), prob.C.cuda()
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    assert g.gemm_run_args(plan.handle, A, B, C, D, M, N, K, prob.alpha, prob.beta,
+                           bias=prob.bias.cuda()) == g.OK
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    cfg = plan.last_config()
+    assert cfg["schedule"] == g.SCHED_SPLIT and cfg["splits"] == 0 and cfg["launches"] == 2
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert cfg["grid"] == n_sms
+    assert_matches_oracle(prob, inputs.bits(D.cpu()))
+    D2 = torch.empty_like(D)
+    g.gemm_run_args(plan.handle, A, B, C, D2, M, N, K, prob.alpha, prob.beta,
+                    bias=prob.bias.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(D, D2), "balanced split-K is not deterministic"
+
+
 @pytest.mark.parametrize("cg,grid", [(1, 4), (2, 8)])
 def test_stream_k_takes_tail_then_head_then_whole_tiles(cg, grid):
     """Four units over six tiles of 64 k-blocks: 96 k-blocks each, so every
