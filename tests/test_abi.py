@@ -4,6 +4,7 @@ here reaches a kernel."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -75,3 +76,32 @@ def test_binding_names_match_c_entry_points():
         if name == "gemm15_status_string":
             continue
         assert callable(getattr(g, name)), name
+
+
+def test_ctypes_structs_match_the_header_layout(tmp_path):
+    """Compile a probe against include/gemm15.h with the host C compiler and
+    compare every struct's size and field offsets with the ctypes mirrors."""
+    mirrors = {"gemm15_plan_desc_t": g.PlanDesc, "gemm15_problem_t": g.Problem,
+               "gemm15_config_t": g.Config, "gemm15_args_t": g.Args,
+               "gemm15_tune_result_t": g.TuneResult}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "gemm15.h"', "int main(void) {"]
+    for cname, cls in mirrors.items():
+        lines.append('printf("%s size %%zu\\n", sizeof(%s));' % (cname, cname))
+        for field, _ in cls._fields_:
+            lines.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (cname, field, cname, field))
+    lines += ["return 0;", "}"]
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for line in out:
+        if line:
+            parts = line.split()
+            got[(parts[0], parts[1])] = int(parts[2])
+    for cname, cls in mirrors.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for field, _ in cls._fields_:
+            assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
