@@ -111,3 +111,27 @@ def test_config2_full_size_sampled_rows():
     strong = inputs.config2(strong=True)
     d = run_gpu(plan_for(strong), strong)
     assert_matches_oracle(strong, d, rows=(4096 - 64, 4096))
+
+
+def test_alpha_zero_gives_rounded_beta_c():
+    """alpha = 0: the product term vanishes, D = rne(beta * C) bit-exactly."""
+    prob = inputs.random_problem(200, 264, 136, alpha=0.0, beta=0.5)
+    want = (prob.C.to(torch.float64) * 0.5).to(torch.float16)
+    assert np.array_equal(run_gpu(plan_for(prob), prob), inputs.bits(want))
+
+
+@pytest.mark.parametrize("K", [1, 7, 63, 64, 65, 127, 129])
+def test_k_around_one_k_block(K):
+    """K from 1 to just past two k-blocks of 64, with A and B padded to a
+    16-byte leading dimension (the K tail is zero-filled by the TMA)."""
+    M, N = 130, 264
+    prob = inputs.random_problem(M, N, K, beta=1.0, relu=True)
+    lda = (K + 7) // 8 * 8
+    A = torch.zeros(M, lda, dtype=torch.float16)
+    A[:, :K] = prob.A
+    plan = plan_for(prob)
+    D = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    plan.run(A.cuda(), prob.B.cuda(), prob.C.cuda(), D, M, N, K, alpha=1.0, beta=1.0, lda=lda)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    assert_matches_oracle(prob, inputs.bits(D.cpu()))
