@@ -22,11 +22,12 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32, E4M3, F64 = 0, 1, 2, 3, 4
+F16, BF16, F32, E4M3, F64, E5M2, E2M1, UE8M0 = 0, 1, 2, 3, 4, 5, 6, 7
 ACTS = {"linear": 0, "relu": 1, "sigmoid": 2, "tanh": 3}
 AUX_OPS = {None: 0, "add": 1, "sub": 2, "mul": 3, "div": 4}
-_NAMES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3, "f64": F64}
-_ITEMSIZE = {F16: 2, BF16: 2, F32: 4, E4M3: 1, F64: 8}
+_NAMES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3, "f64": F64, "e5m2": E5M2,
+          "e2m1": E2M1, "ue8m0": UE8M0}
+_ITEMSIZE = {F16: 2, BF16: 2, F32: 4, E4M3: 1, F64: 8, E5M2: 1, E2M1: 1, UE8M0: 1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
@@ -59,7 +60,8 @@ def _load():
             lib.oracle_gemm.restype = i32
             lib.oracle_gemm.argtypes = [vp, i32, i64, i32, vp, i32, i64, i32, vp, i32, i64,
                                         vp, i64, i64, i64, i64, dbl, dbl, dbl, dbl,
-                                        i32, vp, i32, vp, i32, i64, i32, i32, i64, i64, i32]
+                                        i32, vp, i32, vp, i32, i64, i32, vp, vp, i32, i64,
+                                        i32, i64, i64, i32]
             lib.oracle_round_f16_array.argtypes = [vp, vp, i64]
             lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
             lib.oracle_decode_array.argtypes = [vp, i32, vp, i64]
@@ -88,7 +90,7 @@ def default_threads() -> int:
 def gemm(a, a_dtype, b, b_dtype, c=None, c_dtype="f16", *, alpha=1.0, beta=0.0,
          relu=False, scale_a=1.0, scale_b=1.0, a_col_major=False, b_col_major=False,
          rows=None, threads=None, absolute=False, act=None, bias=None,
-         bias_dtype=None, aux=None, aux_dtype=None, aux_op=None) -> np.ndarray:
+         bias_dtype=None, aux=None, aux_dtype=None, aux_op=None, scales=None) -> np.ndarray:
     """D = act(alpha * s_a * s_b * (A @ B) + beta * C + bias) in float64, for
     rows ``rows = (begin, end)`` of D (all rows by default).
 
@@ -96,7 +98,9 @@ def gemm(a, a_dtype, b, b_dtype, c=None, c_dtype="f16", *, alpha=1.0, beta=0.0,
     ``relu`` else "linear"); ``bias`` is the stored bits of an N-vector of type
     ``bias_dtype`` (default ``c_dtype``), added to every row; ``aux`` (M x N
     row-major storage of type ``aux_dtype``, default ``c_dtype``) enters the
-    activated value by ``aux_op`` in "add", "sub", "mul", "div".
+    activated value by ``aux_op`` in "add", "sub", "mul", "div".  ``scales`` =
+    (SA, SB, scale_dtype, block) makes A and B block-scaled: SA is M x
+    ceil(K/block), SB ceil(K/block) x N, both row-major stored bits.
 
     ``absolute=True`` returns sum_k |A[i,k]| |B[k,j]| instead (the matrix the
     error bound of the checker is built from); alpha/beta/C are then unused.
@@ -143,13 +147,24 @@ def gemm(a, a_dtype, b, b_dtype, c=None, c_dtype="f16", *, alpha=1.0, beta=0.0,
         zcode = dtype_code(aux_dtype or c_dtype)
         ldz = _leading(aux, zcode)
         zptr = aux.ctypes.data
+    sa_ptr = sb_ptr = None
+    s_code, block = 0, 0
+    if scales is not None:
+        sa, sb, s_dt, block = scales
+        kb = -(-K // block)
+        sa, sb = np.ascontiguousarray(sa), np.ascontiguousarray(sb)
+        if sa.shape != (M, kb) or sb.shape != (kb, N):
+            raise ValueError("block scales must be M x ceil(K/block) and ceil(K/block) x N")
+        s_code = dtype_code(s_dt)
+        sa_ptr, sb_ptr = sa.ctypes.data, sb.ctypes.data
     r0, r1 = (0, M) if rows is None else rows
     out = np.empty((r1 - r0, N), dtype=np.float64)
     rc = lib.oracle_gemm(a.ctypes.data, ac, lda, int(a_col_major),
                          b.ctypes.data, bc, ldb, int(b_col_major),
                          cptr, cc, ldc, out.ctypes.data, N, M, N, K,
                          float(alpha), float(beta), float(scale_a), float(scale_b),
-                         act_code, bptr, bcode, zptr, zcode, ldz, op, int(bool(absolute)), r0, r1,
+                         act_code, bptr, bcode, zptr, zcode, ldz, op, sa_ptr, sb_ptr, s_code,
+                         int(block), int(bool(absolute)), r0, r1,
                          int(threads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle_gemm failed with code %d" % rc)
@@ -176,7 +191,7 @@ def decode(bits: np.ndarray, dtype) -> np.ndarray:
     lib = _load()
     code = dtype_code(dtype)
     want = {F16: np.uint16, BF16: np.uint16, E4M3: np.uint8, F32: np.float32,
-            F64: np.float64}[code]
+            F64: np.float64, E5M2: np.uint8, E2M1: np.uint8, UE8M0: np.uint8}[code]
     bits = np.ascontiguousarray(bits, dtype=want)
     out = np.empty(bits.shape, dtype=np.float64)
     lib.oracle_decode_array(bits.ctypes.data, code, out.ctypes.data, bits.size)

@@ -34,6 +34,13 @@
  *     backend", section "CuteDSL 后端支持的功能 / 功能清单".
  *   - element types of A, B, C are bound separately ("CUTLASS Python 接口全解析"
  *     section 2.1); each stored value is decoded exactly to double by x().
+ *   - block-scaled operands (the _scaled_mm formats MXFP8 / MXFP4 / NVFP4 of the
+ *     CuteDSL page's "功能清单", whose scale types and block sizes that page
+ *     leaves to the formats' definitions): every element is multiplied by the
+ *     decoded scale of its block of `block` consecutive K indices before the
+ *     product -- x(A[i,k]) * x(SA[i, k/block]) and x(B[k,j]) * x(SB[k/block, j]).
+ *     MX formats: E4M3 / E5M2 / E2M1 elements, E8M0 scales, block 32; NVFP4:
+ *     E2M1 elements, E4M3 scales, block 16 (a per-tensor scale is alpha).
  *
  * The sum runs in double precision in increasing k.  Threads split the rows
  * of D; each row is computed by exactly one thread with the same arithmetic,
@@ -48,7 +55,8 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_E4M3 = 3, OR_F64 = 4 };
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_E4M3 = 3, OR_F64 = 4,
+       OR_E5M2 = 5, OR_E2M1 = 6, OR_UE8M0 = 7 };
 
 /* ---- decoding stored element bits to double, from the format definitions */
 
@@ -98,12 +106,38 @@ double oracle_decode_e4m3(uint8_t q) {
     return sign ? -v : v;
 }
 
+/* OCP 8-bit E5M2: 1 sign, 5 exponent (bias 15), 2 fraction bits, with
+ * infinities and NaN as in binary16 (it is binary16's top byte). */
+double oracle_decode_e5m2(uint8_t q) {
+    return oracle_decode_f16((uint16_t)((uint16_t)q << 8));
+}
+
+/* OCP 4-bit E2M1 (the element type of MXFP4 / NVFP4), stored one per byte in
+ * the low nibble: 1 sign, 2 exponent (bias 1), 1 fraction bit, no infinity or
+ * NaN; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_decode_e2m1(uint8_t q) {
+    int sign = (q >> 3) & 1;
+    int e = (q >> 1) & 0x3;
+    int f = q & 0x1;
+    double v = e == 0 ? 0.5 * f : ldexp(1.0 + 0.5 * f, e - 1);
+    return sign ? -v : v;
+}
+
+/* OCP E8M0 block scale (UE8M0): 8 exponent bits, no sign or fraction; value
+ * 2^(e - 127), 0xFF is NaN. */
+double oracle_decode_ue8m0(uint8_t q) {
+    return q == 0xFF ? NAN : ldexp(1.0, (int)q - 127);
+}
+
 static double load_elem(const void* p, int dtype, int64_t idx) {
     switch (dtype) {
     case OR_F16: return oracle_decode_f16(((const uint16_t*)p)[idx]);
     case OR_BF16: return oracle_decode_bf16(((const uint16_t*)p)[idx]);
     case OR_E4M3: return oracle_decode_e4m3(((const uint8_t*)p)[idx]);
     case OR_F32: return (double)((const float*)p)[idx];
+    case OR_E5M2: return oracle_decode_e5m2(((const uint8_t*)p)[idx]);
+    case OR_E2M1: return oracle_decode_e2m1(((const uint8_t*)p)[idx]);
+    case OR_UE8M0: return oracle_decode_ue8m0(((const uint8_t*)p)[idx]);
     default: return ((const double*)p)[idx];
     }
 }
@@ -185,6 +219,9 @@ typedef struct {
     const void* bias; int bias_dtype;  /* N elements, or NULL */
     const void* aux; int aux_dtype; int64_t ldaux; int aux_op;  /* Z, row-major; op 0 none,
                                                                    1 add, 2 sub, 3 mul, 4 div */
+    /* block scales: A[i,k] is scaled by SA[i, k / block] (M x ceil(K/block),
+     * row-major), B[k,j] by SB[k / block, j] (ceil(K/block) x N, row-major) */
+    const void* sa; const void* sb; int s_dtype; int64_t block;
     int absolute;                /* 1: compute sum |a||b| (error bound), no epilogue */
     int64_t row_begin, row_end;
     const double* Bd;            /* B decoded to double, K x N row-major, or NULL */
@@ -203,8 +240,10 @@ static int64_t b_index(const oracle_job* j, int64_t k, int64_t n) {
  * (i, j) the terms are still added in increasing k. */
 static void oracle_row(const oracle_job* j, int64_t i, double* acc) {
     for (int64_t n = 0; n < j->N; ++n) acc[n] = 0.0;
+    const int64_t kblocks = j->block > 0 ? (j->K + j->block - 1) / j->block : 0;
     for (int64_t k = 0; k < j->K; ++k) {
         double a = load_elem(j->A, j->a_dtype, a_index(j, i, k));
+        if (j->sa) a *= load_elem(j->sa, j->s_dtype, i * kblocks + k / j->block);
         if (j->absolute) a = fabs(a);
         if (j->Bd) {
             const double* brow = j->Bd + k * j->N;
@@ -215,6 +254,7 @@ static void oracle_row(const oracle_job* j, int64_t i, double* acc) {
         } else {
             for (int64_t n = 0; n < j->N; ++n) {
                 double b = load_elem(j->B, j->b_dtype, b_index(j, k, n));
+                if (j->sb) b *= load_elem(j->sb, j->s_dtype, (k / j->block) * j->N + n);
                 if (j->absolute) b = fabs(b);
                 acc[n] += a * b;
             }
@@ -275,6 +315,7 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
                 double alpha, double beta, double scale_a, double scale_b,
                 int act, const void* bias, int bias_dtype,
                 const void* aux, int aux_dtype, int64_t ldaux, int aux_op,
+                const void* sa, const void* sb, int s_dtype, int64_t block,
                 int absolute, int64_t row_begin, int64_t row_end,
                 int nthreads) {
     if (M < 0 || N < 0 || K < 0 || row_begin < 0 || row_end > M || row_begin > row_end)
@@ -291,6 +332,8 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
     if (act < 0 || act > 3 || aux_op < 0 || aux_op > 4 || (aux_op && !aux)) return 1;
     j.act = act; j.bias = bias; j.bias_dtype = bias_dtype; j.absolute = absolute;
     j.aux = aux; j.aux_dtype = aux_dtype; j.ldaux = ldaux; j.aux_op = aux_op;
+    if ((sa || sb) && block < 1) return 1;
+    j.sa = sa; j.sb = sb; j.s_dtype = s_dtype; j.block = block;
     j.row_begin = row_begin; j.row_end = row_end; j.next_row = row_begin;
     /* Decode B once (the same exact values load_elem would produce); if the
      * copy does not fit in memory, decode element by element instead. */
@@ -299,8 +342,11 @@ int oracle_gemm(const void* A, int a_dtype, int64_t lda, int a_col_major,
         bd = (double*)malloc(sizeof(double) * (size_t)K * (size_t)N);
         if (bd)
             for (int64_t k = 0; k < K; ++k)
-                for (int64_t n = 0; n < N; ++n)
-                    bd[k * N + n] = load_elem(B, b_dtype, b_index(&j, k, n));
+                for (int64_t n = 0; n < N; ++n) {
+                    double b = load_elem(B, b_dtype, b_index(&j, k, n));
+                    if (j.sb) b *= load_elem(j.sb, j.s_dtype, (k / j.block) * N + n);
+                    bd[k * N + n] = b;
+                }
     }
     j.Bd = bd;
     pthread_mutex_init(&j.lock, NULL);

@@ -366,6 +366,106 @@ def test_aux_ops_invert_each_other():
                                    aux_op="sub") + 2.0, x, rtol=0, atol=2.0 ** -50)
 
 
+# ---------------------------------------------------------------- block-scaled formats
+
+def test_decode_e5m2_and_ue8m0_all_patterns_match_torch():
+    bits = np.arange(256, dtype=np.uint8)
+    for name, tdt in (("e5m2", torch.float8_e5m2), ("ue8m0", torch.float8_e8m0fnu)):
+        ours = oracle.decode(bits, name)
+        ref = torch.from_numpy(bits).view(tdt).to(torch.float64).numpy()
+        assert np.array_equal(np.isnan(ours), np.isnan(ref)), name
+        m = ~np.isnan(ref)
+        assert np.array_equal(ours[m], ref[m]), name
+
+
+def test_decode_e2m1_matches_the_format_table():
+    """The 16 E2M1 codes: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (OCP MX)."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    ours = oracle.decode(np.arange(16, dtype=np.uint8), "e2m1")
+    assert list(ours[:8]) == mags and list(-ours[8:]) == mags
+    assert np.all(np.signbit(ours[8:]))
+
+
+def _mx_case(seed, M, N, K, block, elem):
+    g = np.random.default_rng(seed)
+    kb = -(-K // block)
+    if elem == "e2m1":
+        a = g.integers(0, 16, (M, K), dtype=np.uint8)
+        b = g.integers(0, 16, (K, N), dtype=np.uint8)
+    else:
+        a = g.integers(0, 256, (M, K), dtype=np.uint8)
+        b = g.integers(0, 256, (K, N), dtype=np.uint8)
+        a[(a & 0x7F) == 0x7F] = 0x3C  # no NaN (e4m3) / keep finite
+        b[(b & 0x7F) == 0x7F] = 0x3C
+        if elem == "e5m2":
+            a[(a & 0x7C) == 0x7C] = 0x3C  # no inf / NaN
+            b[(b & 0x7C) == 0x7C] = 0x3C
+    sa = g.integers(120, 135, (M, kb), dtype=np.uint8)
+    sb = g.integers(120, 135, (kb, N), dtype=np.uint8)
+    return a, b, sa, sb
+
+
+@pytest.mark.parametrize("elem,block,K", [("e4m3", 32, 96), ("e5m2", 32, 80), ("e2m1", 32, 64),
+                                          ("e2m1", 16, 40)])
+def test_block_scaled_brute_force_exact(elem, block, K):
+    """Block-scaled GEMM (MXFP8 / MXFP4 / NVFP4-style blocks) against exact
+    rational arithmetic on values decoded by torch (e4m3, e5m2, E8M0) or the
+    format table (e2m1); a scale indexed by k mod block instead of k / block
+    fails."""
+    M, N = 5, 7
+    a, b, sa, sb = _mx_case(7, M, N, K, block, elem)
+    tdt = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    if elem == "e2m1":
+        table = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6])
+        av, bv = table[a], table[b]
+    else:
+        av = torch.from_numpy(a).view(tdt[elem]).to(torch.float64).numpy()
+        bv = torch.from_numpy(b).view(tdt[elem]).to(torch.float64).numpy()
+    sav = torch.from_numpy(sa).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    sbv = torch.from_numpy(sb).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    exact = np.zeros((M, N))
+    wrong = np.zeros((M, N))
+    for i in range(M):
+        for j in range(N):
+            acc = Fraction(0)
+            bad = Fraction(0)
+            for k in range(K):
+                acc += Fraction(av[i, k]) * Fraction(sav[i, k // block]) * Fraction(bv[k, j]) * Fraction(sbv[k // block, j])
+                kk = k % block if k % block < sav.shape[1] else 0
+                bad += Fraction(av[i, k]) * Fraction(sav[i, kk]) * Fraction(bv[k, j]) * Fraction(sbv[kk, j])
+            exact[i, j] = float(acc)
+            wrong[i, j] = float(bad)
+    d = oracle.gemm(a, elem, b, elem, scales=(sa, sb, "ue8m0", block))
+    assert np.allclose(d, exact, rtol=1e-14, atol=0)
+    assert not np.allclose(wrong, exact, rtol=1e-6, atol=0)
+
+
+def test_unit_scales_equal_the_unscaled_product():
+    """All E8M0 scales 127 (= 1): the block-scaled result is the plain one."""
+    M, N, K = 8, 12, 64
+    a, b, _, _ = _mx_case(3, M, N, K, 32, "e4m3")
+    ones_a = np.full((M, 2), 127, np.uint8)
+    ones_b = np.full((2, N), 127, np.uint8)
+    assert np.array_equal(oracle.gemm(a, "e4m3", b, "e4m3", scales=(ones_a, ones_b, "ue8m0", 32)),
+                          oracle.gemm(a, "e4m3", b, "e4m3"))
+
+
+def test_nvfp4_blocks_with_e4m3_scales_and_tensor_scale():
+    """NVFP4-style: E2M1 elements, E4M3 block scales per 16, a per-tensor scale
+    as alpha; equals the plain product of operands pre-multiplied in float64."""
+    M, N, K, block = 6, 10, 48, 16
+    g = np.random.default_rng(5)
+    a = g.integers(0, 16, (M, K), dtype=np.uint8)
+    b = g.integers(0, 16, (K, N), dtype=np.uint8)
+    sa = g.integers(0x30, 0x48, (M, K // block), dtype=np.uint8)  # positive finite e4m3
+    sb = g.integers(0x30, 0x48, (K // block, N), dtype=np.uint8)
+    d = oracle.gemm(a, "e2m1", b, "e2m1", alpha=0.25, scales=(sa, sb, "e4m3", block))
+    av = oracle.decode(a, "e2m1") * np.repeat(oracle.decode(sa, "e4m3"), block, axis=1)
+    bv = oracle.decode(b, "e2m1") * np.repeat(oracle.decode(sb, "e4m3"), block, axis=0)
+    plain = oracle.gemm(np.ascontiguousarray(av), "f64", np.ascontiguousarray(bv), "f64", alpha=0.25)
+    assert np.array_equal(d, plain)
+
+
 # ---------------------------------------------------------------- cross-checks
 
 def test_numpy_float64_cross_check():
