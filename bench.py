@@ -140,7 +140,30 @@ def algorithmic_bytes(probs):
             tot += p.M * p.N * 2
         if getattr(p, "bias", None) is not None:
             tot += p.N * 2
+        if getattr(p, "aux", None) is not None:
+            tot += p.M * p.N * 2
     return tot
+
+
+def roofline_entry(flops, abytes, ms, dtype, pk, pk_kind, traffic):
+    """The roofline object of the JSON line for one launch of `flops` FLOPs
+    and `abytes` algorithmic bytes taking `ms` milliseconds.  The bound is the
+    roof the shape's arithmetic intensity meets first: HBM below the ridge
+    point (peak FLOP/s / HBM bytes/s), the tensor pipe above it."""
+    peak = tensor_peak(dtype, pk)
+    achieved = flops / (ms * 1e-3) / 1e12
+    achieved_gbs = abytes / (ms * 1e-3) / 1e9
+    ridge = peak * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if flops / abytes < ridge:
+        return {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"], "traffic": traffic,
+                "peak_source": "%s HBM copy" % pk_kind, "algorithmic_bytes": abytes,
+                "achieved_tflops": achieved, "intensity_flop_per_byte": flops / abytes}
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": "%s bf16 burst%s" % (pk_kind, " x2 (fp8)" if dtype == "e4m3" else ""),
+            "algorithmic_bytes": abytes, "achieved_gbs": achieved_gbs,
+            "intensity_flop_per_byte": flops / abytes}
 
 
 # ------------------------------------------------------------------ clocks
@@ -470,23 +493,8 @@ def run_gpu(args):
     pk, pk_kind = peaks()
     peak = tensor_peak(p0.a_dtype, pk)
     achieved = flops / (ms_step * 1e-3) / 1e12
-    abytes = algorithmic_bytes(probs)
-    achieved_gbs = abytes / (ms_step * 1e-3) / 1e9
-    # the bound is the roof the shape's arithmetic intensity meets first:
-    # HBM below the ridge point (peak FLOP/s / HBM bytes/s), tensor above it
-    ridge = peak * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if flops / abytes < ridge:
-        roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
-                    "traffic": recorded_traffic(args.workload),
-                    "peak_source": "%s HBM copy" % pk_kind, "algorithmic_bytes": abytes,
-                    "achieved_tflops": achieved, "intensity_flop_per_byte": flops / abytes}
-    else:
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
-                    "peak_source": "%s bf16 burst%s" % (pk_kind, " x2 (fp8)" if p0.a_dtype == "e4m3" else ""),
-                    "algorithmic_bytes": abytes, "achieved_gbs": achieved_gbs,
-                    "intensity_flop_per_byte": flops / abytes}
+    roofline = roofline_entry(flops, algorithmic_bytes(probs), ms_step, p0.a_dtype, pk, pk_kind,
+                              recorded_traffic(args.workload))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
