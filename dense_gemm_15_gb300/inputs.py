@@ -19,6 +19,10 @@ Workload ids (the ``workload_id`` seed component):
   3  bf16 Llama-3.3-70B linear layers        (W ~ N(0, 0.02), X ~ N(0, 1), beta 0)
   4  fp16 grouped, 32 groups, N 4096, K 2048 (M_g ~ U{64..4096}, U[-1,1])
   5  fp16 stream-K shapes (U[-1,1]) and e4m3 8192^3 (N(0,1) clamped to +-448)
+  11 block-scaled operands (MX / NVFP4 storage of N(0,1) float32 values with a
+     per-block spread of 2^U{-8..8}); the quantisation to codes and block
+     scales is storage preparation, like the fp8 cast above: the GEMM takes
+     the codes and scales as they are.
 """
 from __future__ import annotations
 
@@ -186,6 +190,99 @@ def config5b(M=8192, N=8192, K=8192, scale_a=1.0, scale_b=1.0, seed=0) -> Proble
     return Problem("e4m3_%dx%dx%d" % (M, N, K), A, B, None, M, N, K, alpha=1.0, beta=0.0,
                    a_dtype="e4m3", b_dtype="e4m3", c_dtype="bf16", d_dtype="bf16",
                    scale_a=scale_a, scale_b=scale_b)
+
+
+# ---------------------------------------------------------------- block-scaled storage
+#
+# Element formats of the block-scaled GEMMs (MXFP8 / MXFP4 / NVFP4): the largest
+# finite magnitude and the exponent of its leading bit (OCP MX element types).
+MX_ELEMS = {"e4m3": (448.0, 8), "e5m2": (57344.0, 15), "e2m1": (6.0, 2)}
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_codes(x: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 code of each float64 value, ties to the even code,
+    saturating at +-6; one code per byte, sign in bit 3 (negative zero kept)."""
+    mag = np.minimum(np.abs(x), 6.0)
+    lo = np.clip(np.searchsorted(E2M1_VALUES, mag, side="right") - 1, 0, 7)
+    hi = np.minimum(lo + 1, 7)
+    dlo, dhi = mag - E2M1_VALUES[lo], E2M1_VALUES[hi] - mag
+    up = (dhi < dlo) | ((dhi == dlo) & (lo % 2 == 1))
+    code = np.where(up, hi, lo).astype(np.uint8)
+    return code | (np.signbit(x).astype(np.uint8) << 3)
+
+
+def _elem_codes(x: np.ndarray, elem: str) -> np.ndarray:
+    if elem == "e2m1":
+        return e2m1_codes(x)
+    mx = MX_ELEMS[elem][0]
+    tdt = torch.float8_e4m3fn if elem == "e4m3" else torch.float8_e5m2
+    # x is a float32 value times a power of two here: one rounding, saturating
+    t = torch.from_numpy(np.clip(x, -mx, mx).astype(np.float32)).to(tdt)
+    return t.view(torch.uint8).numpy()
+
+
+def quantize_blocks(x: np.ndarray, elem: str, block: int, scale: str = "ue8m0", axis: int = 1):
+    """Block-scaled storage of ``x`` (float32-representable values) with one
+    scale per ``block`` consecutive entries along ``axis`` (the K axis: 1 for
+    A [M, K], 0 for B [K, N]); a ragged last block is shorter.
+
+    ``scale="ue8m0"`` (OCP MX): the block's scale is 2^X with
+    X = floor(log2(amax)) - emax(elem), stored as the E8M0 code X + 127 (0 for
+    an all-zero block); elements are x / 2^X rounded to nearest even in
+    ``elem``, saturating.  ``scale="e4m3"`` (NVFP4 style): the scale is
+    amax / max(elem) rounded to e4m3 (1 for an all-zero block) and the
+    elements are x / scale rounded in ``elem``.
+
+    Returns (element codes, same shape as x, uint8; scale codes, uint8, shape
+    with ceil(K / block) along ``axis``)."""
+    if scale == "e4m3" and elem != "e2m1":
+        raise ValueError("e4m3 block scales go with e2m1 elements (NVFP4)")
+    xt = np.moveaxis(np.asarray(x, dtype=np.float64), axis, -1)
+    K = xt.shape[-1]
+    kb = -(-K // block)
+    pad = np.zeros(xt.shape[:-1] + (kb * block - K,))
+    blocks = np.concatenate([xt, pad], axis=-1).reshape(xt.shape[:-1] + (kb, block))
+    amax = np.abs(blocks).max(axis=-1)
+    mx, emax = MX_ELEMS[elem]
+    if scale == "ue8m0":
+        with np.errstate(divide="ignore"):
+            X = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - emax, -127)
+        X = np.clip(X, -127, 127).astype(np.int64)
+        s_codes = (X + 127).astype(np.uint8)
+        s_val = np.ldexp(1.0, X)
+    elif scale == "e4m3":
+        s32 = torch.from_numpy(np.clip(amax / mx, 0, 448.0).astype(np.float32))
+        s_codes = s32.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+        s_codes[s_codes == 0] = 0x38  # 1.0 for all-zero (or vanishing) blocks
+        s_val = torch.from_numpy(s_codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    else:
+        raise ValueError("scale must be 'ue8m0' or 'e4m3'")
+    scaled = blocks / s_val[..., None]
+    codes = _elem_codes(scaled, elem).reshape(blocks.shape[:-2] + (kb * block,))[..., :K]
+    return np.moveaxis(codes, -1, axis).copy(), np.moveaxis(s_codes, -1, axis).copy()
+
+
+def block_scaled_problem(M, N, K, elem="e4m3", block=32, scale="ue8m0", alpha=1.0, seed=0,
+                         wid=11) -> Problem:
+    """A seeded block-scaled GEMM: A [M, K] and B [K, N] drawn N(0, 1) (float32
+    values) with a per-block magnitude spread of 2^U{-8..8}, quantised by
+    ``quantize_blocks`` along K; row-major codes, bf16 output, beta 0.  The
+    scale codes ride on the problem as ``block_scales = (SA, SB, scale, block)``."""
+    key = (M * 1_000_003 + N * 10_007 + K * 101 + block) % (2 ** 31)
+    g = rng(wid, key, seed)
+    kb = -(-K // block)
+    spread_a = np.repeat(np.ldexp(1.0, g.integers(-8, 9, size=(M, kb))), block, axis=1)[:, :K]
+    spread_b = np.repeat(np.ldexp(1.0, g.integers(-8, 9, size=(kb, N))), block, axis=0)[:K]
+    a = g.normal(0.0, 1.0, size=(M, K)).astype(np.float32).astype(np.float64) * spread_a
+    b = g.normal(0.0, 1.0, size=(K, N)).astype(np.float32).astype(np.float64) * spread_b
+    qa, sa = quantize_blocks(a, elem, block, scale, axis=1)
+    qb, sb = quantize_blocks(b, elem, block, scale, axis=0)
+    p = Problem("%s_%s_block%d_%dx%dx%d" % (elem, scale, block, M, N, K), torch.from_numpy(qa),
+                torch.from_numpy(qb), None, M, N, K, alpha=alpha, beta=0.0, a_dtype=elem,
+                b_dtype=elem, c_dtype="bf16", d_dtype="bf16")
+    p.block_scales = (torch.from_numpy(sa), torch.from_numpy(sb), scale, block)
+    return p
 
 
 def random_problem(M, N, K, dtype="f16", out_dtype=None, alpha=1.0, beta=0.0, relu=False,

@@ -52,6 +52,9 @@ def reference(prob, bits_of, rows=None, threads=None):
     ``bits``), so this module needs nothing from the CUDA path."""
     a, b = bits_of(prob.A), bits_of(prob.B)
     c = bits_of(prob.C) if prob.C is not None else None
+    scales = getattr(prob, "block_scales", None)
+    if scales is not None:
+        scales = (bits_of(scales[0]), bits_of(scales[1]), scales[2], scales[3])
     bias = getattr(prob, "bias", None)
     aux_op = getattr(prob, "aux_op", None)
     aux = bits_of(prob.aux) if aux_op else None
@@ -61,10 +64,10 @@ def reference(prob, bits_of, rows=None, threads=None):
                  aux=aux, aux_dtype=prob.d_dtype, aux_op=aux_op,
                  scale_a=prob.scale_a, scale_b=prob.scale_b,
                  a_col_major=prob.a_col_major, b_col_major=prob.b_col_major,
-                 rows=rows, threads=threads)
+                 rows=rows, threads=threads, scales=scales)
     absab = gemm(a, prob.a_dtype, b, prob.b_dtype, absolute=True,
                  a_col_major=prob.a_col_major, b_col_major=prob.b_col_major,
-                 rows=rows, threads=threads)
+                 rows=rows, threads=threads, scales=scales)
     c64 = None
     if c is not None and prob.beta != 0.0:
         r0, r1 = (0, prob.M) if rows is None else rows
