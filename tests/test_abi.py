@@ -105,3 +105,28 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for field, _ in cls._fields_:
             assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
+
+
+def test_noalloc_argument_checks_precede_any_device_call():
+    """gemm_run_splitk_noalloc validates its descriptor, sizes and split count
+    before it touches the device, so these answers need no GPU."""
+    lib = g.load()
+
+    def call(desc, M=64, N=64, K=64, splits=2, scale=None):
+        d = ctypes.byref(desc) if desc is not None else None
+        return lib.gemm_run_splitk_noalloc(d, None, K, None, N, None, N, None, N, M, N, K, 1.0,
+                                           0.0, scale, None, splits, None, None)
+
+    ok = g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F32, 0, 0, 0, 0)
+    assert call(None) == g.ERR_INVALID_ARG
+    assert call(g.PlanDesc(g.F16, g.BF16, g.F16, g.F16, g.F32, 0, 0, 0, 0)) == g.ERR_UNSUPPORTED
+    assert call(g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F16, 0, 0, 0, 0)) == g.ERR_UNSUPPORTED
+    assert call(g.PlanDesc(g.E4M3, g.E4M3, g.F16, g.F16, g.F32, 0, 0, 0, 0)) == g.ERR_UNSUPPORTED
+    assert call(g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F32, 2, 0, 0, 0)) == g.ERR_INVALID_ARG
+    assert call(g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F32, 0, 0, 0, 9)) == g.ERR_INVALID_ARG
+    scale = ctypes.c_float(1.0)
+    assert call(ok, scale=ctypes.addressof(scale)) == g.ERR_INVALID_ARG  # scales are fp8-only
+    assert call(ok, splits=0) == g.ERR_INVALID_ARG
+    assert call(ok, M=-1) == g.ERR_INVALID_ARG
+    assert call(ok, K=1 << 31) == g.ERR_INVALID_ARG
+    assert call(ok, M=0) == g.OK and call(ok, N=0) == g.OK  # nothing to do
