@@ -15,6 +15,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -109,11 +110,40 @@ def tensor_peak(dtype, pk, sustained=False):
     return bf16 * (2.0 if dtype == "e4m3" else 1.0)
 
 
+def code_only(src: str) -> str:
+    """C / C++ source without its comments, whitespace runs collapsed to one
+    space: what the compiler sees, so that the hash below follows the code
+    and not the comments (string and character literals are kept whole)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_hash():
+    """Identity of the kernel sources' code (comments excluded), which a
+    recorded DRAM traffic figure is tied to."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "dense_gemm_15_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "dense_gemm_15_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
+            h.update(b"\0")
     return h.hexdigest()[:16]
 
 

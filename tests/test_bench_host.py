@@ -115,3 +115,22 @@ def test_committed_traffic_entries_are_well_formed():
         assert name in bench.workloads() or name.startswith("custom_"), name
         assert e["dram_bytes_per_launch"] == e["dram_read_bytes"] + e["dram_write_bytes"]
         assert len(e["kernel_hash"]) == 16
+
+
+def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
+    src = 'x = 1; // one\n/* block\n comment */ asm("max.NaN.f32 %0, %1; // kept");\n'
+    assert bench.code_only(src) == 'x = 1; asm("max.NaN.f32 %0, %1; // kept");'
+    assert bench.code_only("a  /* c */b\n\n'/'") == "a b '/'"
+    import shutil
+    csrc = tmp_path / "dense_gemm_15_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES:
+        shutil.copy(bench.os.path.join(bench.ROOT, "dense_gemm_15_gb300", "csrc", f), csrc / f)
+    real = bench.kernel_hash()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_hash() == real
+    k = csrc / "gemm_kernel.cuh"
+    k.write_text("// a new comment line\n" + k.read_text(encoding="utf-8"), encoding="utf-8")
+    assert bench.kernel_hash() == real
+    k.write_text(k.read_text(encoding="utf-8") + "\nint one_more_line;\n", encoding="utf-8")
+    assert bench.kernel_hash() != real
