@@ -1,11 +1,15 @@
 // Persistent warp-specialised tcgen05 GEMM for sm_103a.
 //
-//   D = act(alpha * s_a * s_b * (A . B) + beta * C),  act in {identity, ReLU}
+//   D = act(alpha * s_a * s_b * (A . B) + beta * C + bias) [op Z],
+//   act in {identity, ReLU, sigmoid, tanh}, op in {+, -, *, /}
 //
 // The operation is the plan/run GEMM of the CUTLASS Python interface
 // ("Python packages associated with CUTLASS", section "CUTLASS Python
 // Interface"; alpha/beta as in the kwkr.cn blog "CUTLASS Python接口" section
-// 3.3; ReLU fused in the epilogue as in "CUTLASS Python 接口全解析" section 2.3).
+// 3.3; ReLU fused in the epilogue as in "CUTLASS Python 接口全解析" section 2.3;
+// the bias of that blog's section 5.2; sigmoid, tanh and the auxiliary tensor Z
+// from the roadmap section of "Generating State-of-the-Art GEMMs with
+// TorchInductor's CuteDSL backend").
 // Stream-K and grouped scheduling are the variants listed under "Current
 // functionality" of the CUTLASS README; this kernel is our own design for
 // Blackwell (tcgen05 / TMEM / TMA), not the pre-SM90 kernels the pages use.
@@ -13,7 +17,7 @@
 // One CTA per SM (CG = 1) or one SM pair per tile (CG = 2), 192 threads:
 //   warp 0      TMA producer: A and B tiles into a STAGES-deep shared ring
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2..5  epilogue: TMEM -> registers -> alpha/beta/C/ReLU -> 16-bit ->
+//   warps 2..5  epilogue: TMEM -> registers -> alpha/beta/C/bias/act/Z -> 16-bit ->
 //               swizzled shared staging -> TMA store (one 32-row quarter each)
 // The fp32 accumulator lives in TMEM, double-buffered (2 x TILE_N columns),
 // so the epilogue of tile i overlaps the mainloop of tile i+1.
