@@ -65,7 +65,7 @@ struct GemmParams {
     uint32_t idesc;
     // workspace and status
     float* ws;                        // fp32 partial tiles
-    uint32_t* flags;                  // SK partial-ready flags, one per CTA
+    uint32_t* flags;                  // SK partial-ready flags, two per CTA (tail, head piece)
     int32_t* status;                  // device status word (0 = ok)
     uint32_t epoch;                   // launch sequence number (flag value)
     uint64_t timeout_ns;              // bound of every wait
