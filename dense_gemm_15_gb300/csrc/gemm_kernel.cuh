@@ -1131,8 +1131,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------------ split-K reduction
 
-// D = act(alpha * sum_s partial_s + beta * C + bias) for split-K runs (splits
-// >= 1), or D = act(beta * C + bias) when K == 0 (splits == 0).  Each thread
+// D = act(alpha * sum_s partial_s + beta * C + bias) [op Z] for split-K runs
+// (splits >= 1), or D = act(beta * C + bias) [op Z] when K == 0 (splits == 0).  Each thread
 // owns REDUCE_COLS consecutive columns of one row; partial tiles are summed in
 // split order, eight splits' loads in flight at a time.
 template <int ELEM>
