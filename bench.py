@@ -1,10 +1,13 @@
 """GEMM throughput on one GB300 (or N replicas), one JSON line on rank 0.
 
 A step is one call of the hot path: gemm_run (or grouped_gemm_run) on the
-workload's resident device inputs.  Default workload: fp16 4096^3 with
-alpha 1.5, beta 0.5 and a fused ReLU (the second configuration of the target
-list).  The metric is TFLOP/s = 2*M*N*K / time; the L2 is flushed (256 MiB
-write) between timed steps, outside the per-step CUDA events.
+workload's resident device inputs.  Default workload: the gate+up projection
+of a Llama-3.3-70B layer in bf16 at 8192 tokens (X [8192, 8192] times
+W [8192, 57344], beta 0), the largest single-GPU shape of the Llama linear
+layers that are 89% of that model's runtime ("Generating State-of-the-Art
+GEMMs with TorchInductor's CuteDSL backend", section 2).  The metric is
+TFLOP/s = 2*M*N*K / time; the L2 is flushed (256 MiB write) between timed
+steps, outside the per-step CUDA events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -56,7 +59,7 @@ def workloads():
     return w
 
 
-DEFAULT_WORKLOAD = "fp16_4096x4096x4096_relu"
+DEFAULT_WORKLOAD = "bf16_llama70b_gate_up_m8192"
 BATCHED_WORKLOAD = "fp16_batched_16x1024x1024x1024"
 
 
@@ -495,6 +498,28 @@ def run_gpu(args):
     total_flops = sum_over_ranks(dist, flops, dev)
     value = total_flops / (ms_step_max * 1e-3) / 1e12
 
+    # host cost of one call at the C boundary: gemm_run_ex through ctypes with
+    # the arguments already converted (the launch parameters come from the
+    # plan's cache after the first call), timed on the host; the launches are
+    # real and drained afterwards, untimed
+    host_c_us = None
+    if not grouped and p0.bias is None:
+        lib = g.load()
+        A, B, C, D = dv[0]
+        lda = p0.M if p0.a_col_major else p0.K
+        ldb = p0.K if p0.b_col_major else p0.N
+        cargs = (plan.handle, A.data_ptr(), lda, B.data_ptr(), ldb,
+                 C.data_ptr() if C is not None else None, p0.N, D.data_ptr(), p0.N, p0.M, p0.N,
+                 p0.K, p0.alpha, p0.beta, scales[0].data_ptr() if scales else None,
+                 scales[1].data_ptr() if scales else None, stream.cuda_stream)
+        n_calls = 50
+        torch.cuda._sleep(int(2e7))  # keep the GPU busy so that launches only queue
+        t0 = time.perf_counter()
+        for _ in range(n_calls):
+            lib.gemm_run_ex(*cargs)
+        host_c_us = 1e6 * (time.perf_counter() - t0) / n_calls
+        torch.cuda.synchronize(dev)
+
     # end to end through the C ABI with pinned host buffers (single problems)
     e2e = None
     if not grouped:
@@ -526,6 +551,7 @@ def run_gpu(args):
     roofline = roofline_entry(flops, algorithmic_bytes(probs), ms_step, p0.a_dtype, pk, pk_kind,
                               recorded_traffic(args.workload))
 
+    clocks = clk.summary()
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         fl_s, cores, desc, secs = cpu_oracle_sample(probs, budget_s=args.cpu_budget)
@@ -552,9 +578,16 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps * int(cfg.get("launches", 1)),
-            "clocks": clk.summary(),
+            "clocks": clocks,
+            # time scaled to the maximum SM clock (median clock under load):
+            # separates clock (power cap) effects from kernel changes
+            "ms_per_step_at_max_clock": (ms_step * clocks["sm_mhz"] / clocks["sm_max_mhz"]
+                                         if clocks.get("sm_mhz") and clocks.get("sm_max_mhz")
+                                         else None),
+            "frac_of_sustained_peak": achieved / tensor_peak(p0.a_dtype, pk, sustained=True),
             "wall_s_timed_region": wall,
             "host_us_per_call": 1e6 * host / args.steps,
+            "host_us_per_call_c": host_c_us,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -565,8 +598,8 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--opt", action="append", help="plan option NAME=VALUE (e.g. schedule=1)")
@@ -586,6 +619,11 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.workload not in workloads() and not args.workload.startswith("custom_"):
         ap.error("unknown workload %s (see --list)" % args.workload)
+    ws = dist_env()[0]
+    if args.gpus != ws:
+        ap.error("--gpus %d but %d process(es) were launched: run N replicas with "
+                 "python -m torch.distributed.run --nproc-per-node N bench.py --gpus N"
+                 % (args.gpus, ws))
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

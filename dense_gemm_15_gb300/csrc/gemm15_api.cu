@@ -84,6 +84,19 @@ struct gemm15_plan {
     gemm15_config_t last{};
     // autotuned choices per computed problem shape (M, N, K after normalisation)
     std::map<std::tuple<int64_t, int64_t, int64_t>, Tuned> tuned;
+    uint64_t tuned_gen = 0;  // bumped whenever `tuned` changes
+    // ordering of calls across streams: the plan's device state (workspace,
+    // flags, status, grouped table, host-path buffers) is used by every call,
+    // so a call on another stream than the previous one first waits for the
+    // work the previous call enqueued (recorded in done_ev)
+    cudaEvent_t done_ev = nullptr;
+    cudaStream_t last_stream = nullptr;
+    bool has_last = false;
+    // gemm_run_host: a second stream for the B copy, with fork / join events
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+    // launch parameters of recent dense problems (see LaunchCache)
+    void* cache = nullptr;
 };
 
 namespace {
@@ -107,6 +120,23 @@ struct DeviceGuard {
 };
 
 bool plan_ok(const gemm15_plan* p) { return p != nullptr && p->magic == PLAN_MAGIC; }
+
+// Orders this call after the previous call of the plan when the two use
+// different streams (same stream: stream order already does it).
+gemm15_status_t order_after_previous(gemm15_plan* plan, cudaStream_t s) {
+    if (plan->has_last && plan->last_stream != s) {
+        if (cudaStreamWaitEvent(s, plan->done_ev, 0) != cudaSuccess) return GEMM15_ERR_CUDA;
+    }
+    return GEMM15_OK;
+}
+
+// Records the end of this call's work on `s` for the next call's ordering.
+gemm15_status_t mark_done(gemm15_plan* plan, cudaStream_t s) {
+    if (cudaEventRecord(plan->done_ev, s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    plan->last_stream = s;
+    plan->has_last = true;
+    return GEMM15_OK;
+}
 
 int esize_of(gemm15_dtype_t t) {
     switch (t) {
@@ -522,6 +552,94 @@ gemm15_status_t attach_trace(gemm15_plan* plan, GemmParams& gp, int grid, cudaSt
     return GEMM15_OK;
 }
 
+// Launch parameters of one dense problem, computed once and reused while the
+// same problem (pointers, shape, leading dimensions, epilogue operands) is run
+// again with the same options: the per-call work is then a lookup and the
+// launch, with the tensor maps already encoded.
+struct LaunchEntry {
+    bool valid = false;
+    Prob p{};
+    bool has_c = false;
+    Options opt{};       // the decision-relevant options at encoding time
+    uint64_t tuned_gen = 0;
+    Decision d{};
+    GemmParams gp{};     // every field that does not change from call to call
+};
+
+constexpr int CACHE_ENTRIES = 8;
+struct LaunchCache {
+    LaunchEntry e[CACHE_ENTRIES];
+    int next = 0;
+};
+
+bool same_prob(const Prob& a, const Prob& b) {
+    return a.M == b.M && a.N == b.N && a.K == b.K && a.A == b.A && a.lda == b.lda &&
+           a.a_kmajor == b.a_kmajor && a.B == b.B && a.ldb == b.ldb && a.b_kmajor == b.b_kmajor &&
+           a.C == b.C && a.ldc == b.ldc && a.D == b.D && a.ldd == b.ldd && a.bias == b.bias &&
+           a.bias_rows == b.bias_rows && a.aux == b.aux && a.ldaux == b.ldaux &&
+           a.aux_op == b.aux_op;
+}
+
+bool same_choice_options(const Options& a, const Options& b) {
+    return a.schedule == b.schedule && a.splits == b.splits && a.cta_group == b.cta_group &&
+           a.tile_n == b.tile_n && a.raster == b.raster && a.grid == b.grid &&
+           a.sk_dp_waves == b.sk_dp_waves;
+}
+
+// Finds or builds the launch parameters of problem p (nullptr on an encoding
+// failure).
+const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& p, bool has_c) {
+    if (!plan->cache) plan->cache = new (std::nothrow) LaunchCache();
+    LaunchCache* cache = static_cast<LaunchCache*>(plan->cache);
+    if (!cache) return nullptr;
+    for (const LaunchEntry& e : cache->e)
+        if (e.valid && e.has_c == has_c && e.tuned_gen == plan->tuned_gen &&
+            same_choice_options(e.opt, plan->opt) && same_prob(e.p, p))
+            return &e;
+    LaunchEntry& e = cache->e[cache->next];
+    cache->next = (cache->next + 1) % CACHE_ENTRIES;
+    e.valid = false;
+    const Decision d = decide(plan, p.M, p.N, p.K);
+    GemmParams& gp = e.gp;
+    std::memset(&gp, 0, sizeof(gp));
+    if (!operand_maps(plan, p, d.bn / d.cg, &gp.tmA, &gp.tmB)) return nullptr;
+    if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return nullptr;
+    gp.D = p.D;
+    gp.ldd = p.ldd;
+    gp.C = has_c ? p.C : nullptr;
+    gp.ldc = p.ldc;
+    gp.M = static_cast<int32_t>(p.M);
+    gp.N = static_cast<int32_t>(p.N);
+    gp.K = static_cast<int32_t>(p.K);
+    gp.k_blocks = d.k_blocks;
+    gp.m_blocks = d.m_blocks;
+    gp.n_blocks = d.n_blocks;
+    gp.tiles = d.tiles;
+    gp.raster = d.raster;
+    gp.sched = d.balanced ? SCHED_SK : d.sched;
+    gp.sk_partials_only = d.balanced ? 1 : 0;
+    gp.dp_tiles = d.dp_tiles;
+    gp.splits = d.splits;
+    gp.has_c = has_c && d.sched != SCHED_SPLIT;
+    gp.sk_units = d.sk_units;
+    gp.act = static_cast<int>(plan->desc.epilogue);
+    gp.bias = d.sched == SCHED_SPLIT ? nullptr : p.bias;  // split-K: the reduction adds it
+    gp.bias_rows = p.bias_rows;
+    gp.aux = p.aux;
+    gp.ldaux = p.ldaux;
+    gp.aux_op = d.sched == SCHED_SPLIT ? 0 : p.aux_op;
+    fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
+    gp.groups = nullptr;
+    gp.num_groups = 0;
+    e.p = p;
+    e.has_c = has_c;
+    e.opt = plan->opt;
+    e.tuned_gen = plan->tuned_gen;
+    e.d = d;
+    e.valid = true;
+    return &e;
+}
+
 gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float beta,
                           const float* scale_a, const float* scale_b, cudaStream_t s) {
     gemm15_status_t st = check_operands(plan, p, beta);
@@ -530,6 +648,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         std::memset(&plan->last, 0, sizeof(plan->last));
         return GEMM15_OK;
     }
+    st = order_after_previous(plan, s);
+    if (st != GEMM15_OK) return st;
     const bool has_c = beta != 0.0f;
     const int act = static_cast<int>(plan->desc.epilogue);
     if (p.K == 0) {
@@ -559,53 +679,25 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         d.splits = 0;
         record_config(plan, d, 1);
         plan->last.grid = 0;
-        return GEMM15_OK;
+        return mark_done(plan, s);
     }
-    Decision d = decide(plan, p.M, p.N, p.K);
+    const LaunchEntry* le = launch_entry(plan, p, has_c);
+    if (!le) return GEMM15_ERR_CUDA;
+    const Decision& d = le->d;
     st = ensure_ws(plan, d.ws_bytes, d.flags);
     if (st != GEMM15_OK) return st;
 
-    GemmParams gp;
-    std::memset(&gp, 0, sizeof(gp));
-    if (!operand_maps(plan, p, d.bn / d.cg, &gp.tmA, &gp.tmB)) return GEMM15_ERR_CUDA;
-    if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return GEMM15_ERR_CUDA;
-    gp.D = p.D;
-    gp.ldd = p.ldd;
-    gp.C = has_c ? p.C : nullptr;
-    gp.ldc = p.ldc;
-    gp.M = static_cast<int32_t>(p.M);
-    gp.N = static_cast<int32_t>(p.N);
-    gp.K = static_cast<int32_t>(p.K);
-    gp.k_blocks = d.k_blocks;
-    gp.m_blocks = d.m_blocks;
-    gp.n_blocks = d.n_blocks;
-    gp.tiles = d.tiles;
-    gp.raster = d.raster;
-    gp.sched = d.balanced ? SCHED_SK : d.sched;
-    gp.sk_partials_only = d.balanced ? 1 : 0;
-    gp.dp_tiles = d.dp_tiles;
-    gp.splits = d.splits;
-    gp.has_c = has_c && d.sched != SCHED_SPLIT;
-    gp.sk_units = d.sk_units;
+    GemmParams gp = le->gp;
     gp.alpha = alpha;
     gp.beta = beta;
     gp.scale_a = scale_a;
     gp.scale_b = scale_b;
-    gp.act = act;
-    gp.bias = d.sched == SCHED_SPLIT ? nullptr : p.bias;  // split-K: the reduction adds it
-    gp.bias_rows = p.bias_rows;
-    gp.aux = p.aux;
-    gp.ldaux = p.ldaux;
-    gp.aux_op = d.sched == SCHED_SPLIT ? 0 : p.aux_op;
-    fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.ws = plan->d_ws;
     gp.flags = plan->d_flags;
     gp.status = plan->d_status;
     gp.epoch = ++plan->epoch == 0 ? ++plan->epoch : plan->epoch;
     gp.timeout_ns = static_cast<uint64_t>(plan->opt.timeout_us) * 1000ull;
     gp.fault_skip_flag = plan->opt.fault_skip_flag;
-    gp.groups = nullptr;
-    gp.num_groups = 0;
     st = attach_trace(plan, gp, d.grid, s);
     if (st != GEMM15_OK) return st;
     if (launch_kernel(plan->elem, d.bn, d.cg, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
@@ -644,7 +736,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         ++launches;
     }
     record_config(plan, d, launches);
-    return GEMM15_OK;
+    return mark_done(plan, s);
 }
 
 }  // namespace
@@ -720,6 +812,14 @@ gemm15_status_t gemm_plan_create(gemm15_plan_t* out, const gemm15_plan_desc_t* d
         delete p;
         return GEMM15_ERR_OOM;
     }
+    if (cudaEventCreateWithFlags(&p->done_ev, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->d_status);
+        cudaFree(p->d_flags);
+        cudaFree(p->d_ws);
+        delete p;
+        return GEMM15_ERR_CUDA;
+    }
     *out = p;
     return GEMM15_OK;
 }
@@ -739,6 +839,11 @@ gemm15_status_t gemm_plan_destroy(gemm15_plan_t plan) {
     for (void* b : plan->d_host_path) cudaFree(b);
     cudaFree(plan->d_scales);
     cudaFree(plan->d_trace);
+    if (plan->done_ev) cudaEventDestroy(plan->done_ev);
+    if (plan->fork_ev) cudaEventDestroy(plan->fork_ev);
+    if (plan->join_ev) cudaEventDestroy(plan->join_ev);
+    if (plan->copy_stream) cudaStreamDestroy(plan->copy_stream);
+    delete static_cast<LaunchCache*>(plan->cache);
     plan->magic = PLAN_DEAD;
     delete plan;
     return GEMM15_OK;
@@ -805,6 +910,7 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
     if (p.M == 0 || p.N == 0 || p.K == 0) return GEMM15_OK;  // one fixed path: nothing to choose
     const auto key = std::make_tuple(p.M, p.N, p.K);
     plan->tuned.erase(key);
+    ++plan->tuned_gen;
 
     // candidates: every schedule on each tile shape, stream-K with and without
     // its data-parallel waves
@@ -883,6 +989,7 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
     cudaFree(flush);
     if (best < 0) return GEMM15_ERR_CUDA;
     plan->tuned[key] = cands[best];
+    ++plan->tuned_gen;
     // leave D holding the chosen configuration's result (and plan->last its config)
     st = run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b, s);
     if (st != GEMM15_OK) return st;
@@ -900,6 +1007,7 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
 gemm15_status_t gemm_plan_forget_tuning(gemm15_plan_t plan) {
     if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
     plan->tuned.clear();
+    ++plan->tuned_gen;
     return GEMM15_OK;
 }
 
@@ -926,6 +1034,8 @@ gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB
     const int es = esize_of(plan->desc.a), eo = esize_of(plan->desc.d);
     const size_t bytes[3] = {static_cast<size_t>(M * K * es), static_cast<size_t>(K * N * es),
                              static_cast<size_t>(M * N * eo)};
+    // the plan's device state may still be in use by its previous call
+    if (order_after_previous(plan, s) != GEMM15_OK) return GEMM15_ERR_CUDA;
     for (int i = 0; i < 3; ++i) {
         const size_t need = (bytes[i] + 255) & ~static_cast<size_t>(255);
         if (need > plan->host_path_cap[i]) {
@@ -941,17 +1051,28 @@ gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB
     }
     if (!plan->d_scales && cudaMalloc(&plan->d_scales, 2 * sizeof(float)) != cudaSuccess)
         return GEMM15_ERR_OOM;
+    if (!plan->copy_stream) {
+        if (cudaStreamCreateWithFlags(&plan->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&plan->fork_ev, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&plan->join_ev, cudaEventDisableTiming) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+    }
     void* dA = plan->d_host_path[0];
     void* dB = plan->d_host_path[1];
     void* dCD = plan->d_host_path[2];  // C is copied in and D overwrites it in place
+    // B goes up on the plan's copy stream while A (and C) go up on `stream`
     if (K > 0) {
-        if (cudaMemcpyAsync(dA, hA, bytes[0], cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpyAsync(dB, hB, bytes[1], cudaMemcpyHostToDevice, s) != cudaSuccess)
+        if (cudaEventRecord(plan->fork_ev, s) != cudaSuccess ||
+            cudaStreamWaitEvent(plan->copy_stream, plan->fork_ev, 0) != cudaSuccess ||
+            cudaMemcpyAsync(dB, hB, bytes[1], cudaMemcpyHostToDevice, plan->copy_stream) != cudaSuccess ||
+            cudaEventRecord(plan->join_ev, plan->copy_stream) != cudaSuccess ||
+            cudaMemcpyAsync(dA, hA, bytes[0], cudaMemcpyHostToDevice, s) != cudaSuccess)
             return GEMM15_ERR_CUDA;
     }
     if (beta != 0.0f &&
         cudaMemcpyAsync(dCD, hC, bytes[2], cudaMemcpyHostToDevice, s) != cudaSuccess)
         return GEMM15_ERR_CUDA;
+    if (K > 0 && cudaStreamWaitEvent(s, plan->join_ev, 0) != cudaSuccess) return GEMM15_ERR_CUDA;
     const float* sa = nullptr;
     const float* sb = nullptr;
     if (plan->elem == ELEM_E4M3) {
@@ -972,9 +1093,14 @@ gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB
     if (cudaMemcpyAsync(hD, dCD, bytes[2], cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return GEMM15_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM15_ERR_CUDA;
+    // read and clear the status word, as gemm_plan_query_error does
     int32_t status = 0;
     if (cudaMemcpy(&status, plan->d_status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
         return GEMM15_ERR_CUDA;
+    if (status != 0) {
+        if (cudaMemset(plan->d_status, 0, sizeof(int32_t)) != cudaSuccess) return GEMM15_ERR_CUDA;
+        if (status < 0 || status > GEMM15_ERR_BAD_PLAN) return GEMM15_ERR_DEVICE_FAULT;
+    }
     return static_cast<gemm15_status_t>(status);
 }
 
@@ -1032,6 +1158,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
             cg = 2;
     }
     const int G = cg == 2 ? clusters : G1;  // scheduling units
+    if (order_after_previous(plan, s) != GEMM15_OK) return GEMM15_ERR_CUDA;
     int32_t tiles = 0;
     const bool reuse = plan->d_groups && plan->groups_ng == ng && plan->groups_key_c == has_c &&
                        plan->groups_key_bn == bn && plan->groups_key_raster == plan->opt.raster &&
@@ -1141,7 +1268,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     d.tiles = tiles;
     d.raster = cg == 2 ? 8 : 16;
     record_config(plan, d, 1);
-    return GEMM15_OK;
+    return mark_done(plan, s);
 }
 
 gemm15_status_t gemm_run_batched(gemm15_plan_t plan, const void* A, int64_t lda, int64_t stride_a,

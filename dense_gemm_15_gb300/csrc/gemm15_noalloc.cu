@@ -145,12 +145,7 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
         return GEMM15_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM15_OK;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM15_ERR_CUDA;
-    DeviceSetup* ds = nullptr;
-    gemm15_status_t st = setup_device(dev, &ds);
-    if (st != GEMM15_OK) return st;
-
+    // every argument check comes before the first device call
     // column-major C/D: compute D^T = B^T . A^T (row-major N x M)
     const bool a_row = d.layout_a == GEMM15_ROW_MAJOR;
     const bool b_row = d.layout_b == GEMM15_ROW_MAJOR;
@@ -190,6 +185,12 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
     const int64_t sp = K > 0 ? std::min<int64_t>(splits, k_blocks) : 0;
     const size_t need = STATUS_BYTES + static_cast<size_t>(tiles) * sp * TILE_M * bn * sizeof(float);
     if (need > SCRATCH_BYTES) return GEMM15_ERR_UNSUPPORTED;  // beyond the fixed scratch
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM15_ERR_CUDA;
+    DeviceSetup* ds = nullptr;
+    gemm15_status_t st = setup_device(dev, &ds);
+    if (st != GEMM15_OK) return st;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t* dev_status = status ? status : reinterpret_cast<int32_t*>(ds->scratch);

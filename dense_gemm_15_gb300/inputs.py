@@ -19,6 +19,7 @@ Workload ids (the ``workload_id`` seed component):
   3  bf16 Llama-3.3-70B linear layers        (W ~ N(0, 0.02), X ~ N(0, 1), beta 0)
   4  fp16 grouped, 32 groups, N 4096, K 2048 (M_g ~ U{64..4096}, U[-1,1])
   5  fp16 stream-K shapes (U[-1,1]) and e4m3 8192^3 (N(0,1) clamped to +-448)
+  8  small-integer operands (exact-arithmetic parity cases)
   11 block-scaled operands (MX / NVFP4 storage of N(0,1) float32 values with a
      per-block spread of 2^U{-8..8}); the quantisation to codes and block
      scales is storage preparation, like the fp8 cast above: the GEMM takes
@@ -67,6 +68,14 @@ def uniform(shape, lo, hi, dtype, workload_id, tensor_id, seed=0) -> torch.Tenso
 
 def normal(shape, std, dtype, workload_id, tensor_id, seed=0) -> torch.Tensor:
     return _store(rng(workload_id, tensor_id, seed).normal(0.0, std, size=shape), dtype)
+
+
+def integers(shape, lo, hi, dtype, workload_id, tensor_id, seed=0) -> torch.Tensor:
+    """Uniform integers in [lo, hi] (inclusive), stored in ``dtype`` (exact for
+    the small ranges used: every integer of magnitude <= 256 is representable
+    in fp16 and bf16, and every one of magnitude <= 16 in e4m3)."""
+    return _store(rng(workload_id, tensor_id, seed).integers(lo, hi, size=shape, endpoint=True)
+                  .astype(np.float64), dtype)
 
 
 def ones(shape, dtype) -> torch.Tensor:
@@ -311,4 +320,34 @@ def random_problem(M, N, K, dtype="f16", out_dtype=None, alpha=1.0, beta=0.0, re
     return Problem("random_%dx%dx%d" % (M, N, K), A, B, C, M, N, K, alpha=alpha, beta=beta,
                    relu=relu, a_dtype=dtype, b_dtype=dtype, c_dtype=out_dtype,
                    d_dtype=out_dtype, a_col_major=a_col_major, b_col_major=b_col_major,
+                   scale_a=scale_a, scale_b=scale_b, act=act, bias=bv, aux=zv, aux_op=aux_op)
+
+
+def integer_problem(M, N, K, dtype="f16", alpha=1.5, beta=0.5, act="relu",
+                    a_col_major=False, b_col_major=False, seed=0, scale_a=1.0, scale_b=1.0,
+                    bias=False, aux_op=None, wid=8) -> Problem:
+    """A seeded problem whose GEMM arithmetic is exact in fp32: A and B hold
+    integers in [-2, 2], C integers in [-4, 4], the bias integers in [-8, 8] and
+    an auxiliary tensor integers in [-3, 3] (powers of two 1/2, 1, 2, 4 for
+    "div").  With alpha, beta and the fp8 scales chosen so that every product
+    is a short binary fraction, every partial sum, every epilogue step and the
+    final value are exact in fp32, so that any k order gives the same result and
+    the output is one round-to-nearest-even of the exact value: a GPU result is
+    then comparable bit for bit with the oracle's rounded result."""
+    out = "bf16" if dtype == "e4m3" else dtype
+    key = (M * 1_000_003 + N * 10_007 + K * 101 + int(a_col_major) * 2 + int(b_col_major)) % (2**31)
+    sa, sb = _mk((M, K), (K, N), a_col_major, b_col_major)
+    A = integers(sa, -2, 2, dtype, wid, key + 0, seed)
+    B = integers(sb, -2, 2, dtype, wid, key + 1, seed)
+    C = integers((M, N), -4, 4, out, wid, key + 2, seed) if beta != 0.0 else None
+    bv = integers((N,), -8, 8, out, wid, key + 3, seed) if bias else None
+    zv = None
+    if aux_op == "div":
+        e = rng(wid, key + 4, seed).integers(-1, 2, size=(M, N), endpoint=True)
+        zv = _store(np.ldexp(1.0, e), out)
+    elif aux_op:
+        zv = integers((M, N), -3, 3, out, wid, key + 4, seed)
+    return Problem("int_%s_%dx%dx%d" % (dtype, M, N, K), A, B, C, M, N, K, alpha=alpha,
+                   beta=beta, relu=act == "relu", a_dtype=dtype, b_dtype=dtype, c_dtype=out,
+                   d_dtype=out, a_col_major=a_col_major, b_col_major=b_col_major,
                    scale_a=scale_a, scale_b=scale_b, act=act, bias=bv, aux=zv, aux_op=aux_op)

@@ -36,7 +36,13 @@
  *     to the plan's status word; read them with gemm_plan_query_error after
  *     synchronising the stream.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
- *   - A plan may be used from one host thread at a time.
+ *   - A plan may be used from one host thread at a time.  Its device state
+ *     (workspace, stream-K flags, status word, grouped table, host-path
+ *     buffers) serves every call, so calls on one plan never run concurrently
+ *     on the GPU: a call enqueued on another stream than the plan's previous
+ *     call first makes its stream wait for the previous call's work (an event
+ *     the plan records after each call).  Independent GEMMs that should overlap
+ *     on different streams need one plan each.
  */
 #ifndef GEMM15_H_
 #define GEMM15_H_
@@ -284,11 +290,11 @@ typedef struct {
     gemm15_status_t status;  /* GEMM15_OK, or why the candidate could not run */
 } gemm15_tune_result_t;
 
-/* Autotuning: "profile every kernel configuration for the problem size and
- * data types, then fix the fastest" (kwkr.cn blog "CUTLASS Python接口",
- * section 6.2, GemmProfiler; autotuning over candidate configurations in
- * "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL backend",
- * section 6.2).  Runs each candidate the library can launch for this problem
+/* Autotuning: the kwkr.cn blog "CUTLASS Python接口", section 6.2, profiles
+ * each kernel configuration for the problem size and data types with its
+ * GemmProfiler and keeps the fastest; "Generating State-of-the-Art GEMMs with
+ * TorchInductor's CuteDSL backend", section 6.2, autotunes over candidate
+ * configurations.  This call runs each candidate the library can launch for this problem
  * -- data-parallel, stream-K (with and without its data-parallel waves) and
  * split-K schedules on single-SM and SM-pair tiles 128 and 256 wide -- once to
  * warm up and then `iterations` times, each timed with CUDA events on

@@ -48,10 +48,61 @@ def assert_matches_oracle(prob, d_bits, rows=None):
     return worst
 
 
-def sample_rows(M, count=3, span=64, seed=0):
-    """A few row windows spread over [0, M), including the last rows."""
-    if M <= span * count:
-        return [(0, M)]
-    rng = np.random.default_rng(seed)
-    starts = sorted(set([0, M - span] + [int(x) for x in rng.integers(0, M - span, count - 2)]))
-    return [(s, s + span) for s in starts]
+def oracle_bits(prob):
+    """The oracle's D rounded once to the output type (nearest even): the
+    expected stored bits of a problem whose arithmetic is exact in fp32."""
+    import oracle
+    a, b = inputs.bits(prob.A), inputs.bits(prob.B)
+    c = inputs.bits(prob.C) if prob.C is not None and prob.beta != 0.0 else None
+    bias = inputs.bits(prob.bias) if prob.bias is not None else None
+    aux = inputs.bits(prob.aux) if prob.aux_op else None
+    d = oracle.gemm(a, prob.a_dtype, b, prob.b_dtype, c, prob.c_dtype, alpha=prob.alpha,
+                    beta=prob.beta, act=prob.act, bias=bias, bias_dtype=prob.d_dtype,
+                    aux=aux, aux_dtype=prob.d_dtype, aux_op=prob.aux_op,
+                    scale_a=prob.scale_a, scale_b=prob.scale_b,
+                    a_col_major=prob.a_col_major, b_col_major=prob.b_col_major)
+    return oracle.round_to(d, prob.d_dtype)
+
+
+def assert_bit_exact(prob, d_bits, want=None):
+    want = oracle_bits(prob) if want is None else want
+    assert d_bits.shape == want.shape
+    bad = np.argwhere(d_bits != want)
+    assert bad.size == 0, "%s: %d elements differ from the oracle, first at %s (%#06x vs %#06x)" % (
+        prob.name, len(bad), tuple(bad[0]), int(d_bits[tuple(bad[0])]), int(want[tuple(bad[0])]))
+
+
+def band_windows(M, band=256, span=8, seed=0):
+    """One window of `span` rows at a seeded offset inside every `band`-row
+    band of [0, M), plus the last `span` rows: every M-tile band of the
+    kernels (128 or 256 rows) is sampled."""
+    rng = np.random.default_rng([seed, M, band])
+    wins = set()
+    for b0 in range(0, M, band):
+        hi = min(M, b0 + band)
+        s = b0 + int(rng.integers(0, max(1, hi - b0 - span + 1)))
+        wins.add((s, min(hi, s + span)))
+    wins.add((max(0, M - span), M))
+    return sorted(wins)
+
+
+def row_subproblem(prob, idx):
+    """The problem restricted to rows `idx` of A, C, Z and D (a row of D
+    depends only on the same row of A, C and Z)."""
+    import copy
+    idx = torch.as_tensor(np.asarray(idx, dtype=np.int64))
+    sub = copy.copy(prob)
+    sub.A = (prob.A[:, idx] if prob.a_col_major else prob.A[idx]).contiguous()
+    sub.C = prob.C[idx].contiguous() if prob.C is not None else None
+    if getattr(prob, "aux", None) is not None:
+        sub.aux = prob.aux[idx].contiguous()
+    sub.M = int(idx.numel())
+    sub.name = prob.name + "[rows]"
+    return sub
+
+
+def assert_windows_match_oracle(prob, d_bits, windows):
+    """Compares the rows of `windows` against one oracle call on those rows."""
+    idx = np.concatenate([np.arange(a, b) for a, b in windows])
+    sub = row_subproblem(prob, idx)
+    return assert_matches_oracle(sub, np.ascontiguousarray(d_bits[idx]))

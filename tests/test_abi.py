@@ -130,3 +130,35 @@ def test_noalloc_argument_checks_precede_any_device_call():
     assert call(ok, M=-1) == g.ERR_INVALID_ARG
     assert call(ok, K=1 << 31) == g.ERR_INVALID_ARG
     assert call(ok, M=0) == g.OK and call(ok, N=0) == g.OK  # nothing to do
+
+
+def test_noalloc_pointer_and_layout_checks_precede_any_device_call():
+    """Null D, a missing C with beta != 0, leading dimensions below the
+    extent, misaligned pointers or leading dimensions and a problem beyond the
+    scratch are answered before any device call (host addresses stand in for
+    device ones: nothing is dereferenced)."""
+    lib = g.load()
+    ok = g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F32, 0, 0, 0, 0)
+    buf = ctypes.create_string_buffer(4096 + 64)
+    base = (ctypes.addressof(buf) + 63) // 64 * 64
+
+    def call(A=base, lda=64, B=base, ldb=64, C=None, ldc=64, D=base, ldd=64, M=64, N=64, K=64,
+             beta=0.0, splits=2, desc=ok):
+        return lib.gemm_run_splitk_noalloc(ctypes.byref(desc), A, lda, B, ldb, C, ldc, D, ldd,
+                                           M, N, K, 1.0, beta, None, None, splits, None, None)
+
+    assert call(D=None) == g.ERR_INVALID_ARG
+    assert call(beta=1.0) == g.ERR_INVALID_ARG                 # C missing
+    assert call(A=None) == g.ERR_INVALID_ARG
+    assert call(ldd=32) == g.ERR_INVALID_ARG                   # below N
+    assert call(lda=32) == g.ERR_INVALID_ARG                   # below K
+    assert call(ldd=68) == g.ERR_ALIGNMENT                     # 136 bytes
+    assert call(D=base + 2) == g.ERR_ALIGNMENT
+    assert call(A=base + 8) == g.ERR_ALIGNMENT
+    assert call(C=base + 4, beta=1.0) == g.ERR_ALIGNMENT
+    # column-major C/D swaps the operands: ldd then covers M
+    col = g.PlanDesc(g.F16, g.F16, g.F16, g.F16, g.F32, 0, 0, 1, 0)
+    assert call(desc=col, M=128, ldd=64) == g.ERR_INVALID_ARG
+    # 32 tiles of 128 x 256 with 64 splits need 256 MiB of partials
+    assert call(M=1024, N=1024, K=4096, lda=4096, ldb=1024, ldd=1024,
+                splits=64) == g.ERR_UNSUPPORTED

@@ -1,0 +1,359 @@
+"""Bit-exact parity on small-integer operands, through every schedule, tile
+shape, layout and entry point.
+
+A and B hold integers in [-2, 2] (C, bias and Z small integers too), and alpha,
+beta and the fp8 scales are short binary fractions, so every partial sum, every
+stream-K / split-K partial and every epilogue step is exact in fp32: whatever
+the order of the k terms, the GPU result is one round-to-nearest-even of the
+exact value, the same rounding the oracle applies to its exact fp64 sum.  A
+dropped, repeated or misplaced k-block, a lost or doubled stream-K partial or a
+wrong tile in a grouped table changes many sums by several units and fails the
+comparison, which the accuracy bound of the random-input tests cannot promise.
+
+The exact-value cases of the pages are the all-ones examples ("Python
+packages associated with CUTLASS", sections "CUTLASS Python Interface" and
+"Installation"); these cases extend that check to random integer operands."""
+import numpy as np
+import pytest
+import torch
+
+from dense_gemm_15_gb300 import binding as g
+from dense_gemm_15_gb300 import inputs
+from helpers import LAYOUT, assert_bit_exact, oracle_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_args(plan, prob, col_major_cd=False):
+    """Runs `prob` (bias, Z and fp8 scales included) through gemm_run_args;
+    returns D as M x N row-major stored bits."""
+    A, B = prob.A.cuda(), prob.B.cuda()
+    C = prob.C.cuda() if prob.C is not None else None
+    Z = prob.aux.cuda() if prob.aux_op else None
+    bias = prob.bias.cuda() if prob.bias is not None else None
+    dt = inputs.TORCH_DTYPE[prob.d_dtype]
+    if col_major_cd:
+        C = C.t().contiguous() if C is not None else None
+        Z = Z.t().contiguous() if Z is not None else None
+        D = torch.full((prob.N, prob.M), float("nan"), dtype=dt, device="cuda")
+    else:
+        D = torch.full((prob.M, prob.N), float("nan"), dtype=dt, device="cuda")
+    sa = sb = None
+    if prob.a_dtype == "e4m3":
+        sa = torch.tensor([prob.scale_a], dtype=torch.float32, device="cuda")
+        sb = torch.tensor([prob.scale_b], dtype=torch.float32, device="cuda")
+    st = g.gemm_run_args(plan.handle, A, B, C, D, prob.M, prob.N, prob.K, prob.alpha,
+                         prob.beta, scale_a=sa, scale_b=sb, bias=bias, aux=Z,
+                         aux_op=prob.aux_op)
+    assert st == g.OK, g.status_string(st)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    Dh = D.cpu()
+    return inputs.bits(Dh.t().contiguous() if col_major_cd else Dh)
+
+
+def _plan(prob, layout_cd=g.ROW_MAJOR, **opts):
+    plan = g.Plan(prob.a_dtype, prob.d_dtype, epilogue=prob.act,
+                  layout_a=LAYOUT[prob.a_col_major], layout_b=LAYOUT[prob.b_col_major],
+                  layout_cd=layout_cd)
+    for k, v in opts.items():
+        plan.set(getattr(g, "OPT_" + k.upper()), v)
+    return plan
+
+
+# ------------------------------------------------------------------ schedules x tiles
+
+TILES = [(1, 128), (1, 256), (2, 256), (2, 128)]
+
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("cg,tile_n", TILES)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_every_schedule_and_tile_bit_exact(sched, cg, tile_n, dtype):
+    """520 x 392 x 4160: ragged M and N, 65 k-blocks; stream-K cuts every
+    tile over about fifteen units, split-K over several splits."""
+    prob = inputs.integer_problem(520, 392, 4160, dtype=dtype, bias=True)
+    plan = _plan(prob, schedule=sched, cta_group=cg, tile_n=tile_n)
+    d = _run_args(plan, prob)
+    cfg = plan.last_config()
+    assert (cfg["schedule"], cfg["cta_group"], cfg["tile_n"]) == (sched, cg, tile_n)
+    assert_bit_exact(prob, d)
+
+
+@pytest.mark.parametrize("a_col,b_col", [(True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("sched,cg", [(g.SCHED_DP, 2), (g.SCHED_SK, 1), (g.SCHED_SK, 2),
+                                      (g.SCHED_SPLIT, 1)])
+def test_operand_layouts_bit_exact(a_col, b_col, sched, cg):
+    prob = inputs.integer_problem(392, 520, 2112, dtype="bf16", a_col_major=a_col,
+                                  b_col_major=b_col)
+    plan = _plan(prob, schedule=sched, cta_group=cg)
+    assert_bit_exact(prob, _run_args(plan, prob))
+
+
+@pytest.mark.parametrize("M,N,K,act", [(16, 8192, 2048, "linear"), (300, 1040, 4096, "relu"),
+                                       (128, 768, 16384, "linear")])
+def test_balanced_split_k_bit_exact(M, N, K, act):
+    prob = inputs.integer_problem(M, N, K, dtype="bf16", act=act, bias=True)
+    plan = _plan(prob, schedule=g.SCHED_SPLIT, splits=-1)
+    d = _run_args(plan, prob)
+    assert plan.last_config()["splits"] == 0
+    assert_bit_exact(prob, d)
+
+
+@pytest.mark.parametrize("splits", [2, 7, 33])
+def test_split_k_split_counts_bit_exact(splits):
+    prob = inputs.integer_problem(256, 264, 8192, dtype="f16")
+    plan = _plan(prob, schedule=g.SCHED_SPLIT, splits=splits, cta_group=1)
+    d = _run_args(plan, prob)
+    assert plan.last_config()["splits"] == splits
+    assert_bit_exact(prob, d)
+
+
+# ------------------------------------------------------------------ stream-K partitions
+
+@pytest.mark.parametrize("cg,grid", [(1, 4), (2, 8)])
+def test_stream_k_tail_head_whole_partition_bit_exact(cg, grid):
+    """Four units over six tiles: each unit holds a whole tile and a tail or
+    a head piece of a split tile."""
+    m = 128 * cg
+    prob = inputs.integer_problem(2 * m, 768, 4096, dtype="f16")
+    plan = _plan(prob, schedule=g.SCHED_SK, cta_group=cg, grid=grid, tile_n=256)
+    d = _run_args(plan, prob)
+    assert plan.last_config()["tiles"] == 6
+    assert_bit_exact(prob, d)
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+def test_stream_k_owner_finishing_last_bit_exact(cg):
+    """Three tiles over five units: the owners hold no head piece, and two
+    units publish two partial tiles each."""
+    prob = inputs.integer_problem(128 * cg, 768, 4096, dtype="bf16", alpha=-1.25, act="linear")
+    plan = _plan(prob, schedule=g.SCHED_SK, cta_group=cg, grid=5 * cg, tile_n=256)
+    d1 = _run_args(plan, prob)
+    assert_bit_exact(prob, d1)
+
+
+@pytest.mark.parametrize("cg,units,N", [(1, 4, 200), (2, 4, 200), (1, 3, 392), (2, 3, 392)])
+def test_stream_k_owner_that_ends_its_unit_bit_exact(cg, units, N):
+    """Owner pieces at the end of their unit add the peers' partials staged in
+    the idle TMEM accumulator."""
+    prob = inputs.integer_problem(128 * cg - 8, N, 4096, dtype="f16")
+    plan = _plan(prob, schedule=g.SCHED_SK, cta_group=cg, grid=units * cg, tile_n=256)
+    assert_bit_exact(prob, _run_args(plan, prob))
+
+
+@pytest.mark.parametrize("waves", [0, 1])
+def test_stream_k_after_data_parallel_waves_bit_exact(waves):
+    """Tiles beyond the data-parallel waves go to stream-K: 9 x 17 SM-pair
+    tiles (about two waves), with and without one data-parallel wave first."""
+    prob = inputs.integer_problem(2304, 4352, 1024, dtype="bf16", bias=True)
+    plan = _plan(prob, schedule=g.SCHED_SK, sk_dp_waves=waves, cta_group=2)
+    assert_bit_exact(prob, _run_args(plan, prob))
+
+
+# ------------------------------------------------------------------ fp8
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("cg", [1, 2])
+def test_e4m3_power_of_two_scales_bit_exact(sched, cg):
+    """e4m3 integer operands, scales 1/2 and 1/4 (alpha * s_a * s_b = 3/16)."""
+    prob = inputs.integer_problem(520, 528, 4224, dtype="e4m3", beta=0.0, scale_a=0.5,
+                                  scale_b=0.25, bias=True)
+    plan = _plan(prob, schedule=sched, cta_group=cg, tile_n=256)
+    assert_bit_exact(prob, _run_args(plan, prob))
+
+
+# ------------------------------------------------------------------ C / D layout, epilogue
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+def test_column_major_c_d_bit_exact(sched):
+    prob = inputs.integer_problem(392, 264, 4096, dtype="f16", bias=True, aux_op="add")
+    plan = _plan(prob, layout_cd=g.COL_MAJOR, schedule=sched)
+    assert_bit_exact(prob, _run_args(plan, prob, col_major_cd=True))
+
+
+@pytest.mark.parametrize("op", ["add", "sub", "mul", "div"])
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+def test_aux_ops_bit_exact(op, sched):
+    prob = inputs.integer_problem(296, 392, 2048, dtype="bf16", bias=True, aux_op=op)
+    plan = _plan(prob, schedule=sched)
+    assert_bit_exact(prob, _run_args(plan, prob))
+
+
+def test_k_zero_bit_exact():
+    prob = inputs.integer_problem(70, 136, 0, dtype="f16", bias=True, aux_op="mul")
+    prob.A = torch.empty(70, 0, dtype=torch.float16)
+    prob.B = torch.empty(0, 136, dtype=torch.float16)
+    assert_bit_exact(prob, _run_args(_plan(prob), prob))
+
+
+# ------------------------------------------------------------------ grouped and batched
+
+@pytest.mark.parametrize("cg", [1, 2])
+def test_grouped_bit_exact(cg):
+    sizes = [(64, 256, 1024), (200, 392, 2112), (1, 16, 64), (385, 512, 576), (520, 1040, 1088),
+             (256, 256, 4096)]
+    probs = [inputs.integer_problem(M, N, K, dtype="f16", seed=i)
+             for i, (M, N, K) in enumerate(sizes)]
+    plan = _plan(probs[0], cta_group=cg)
+    dev = []
+    for p in probs:
+        dev.append(dict(M=p.M, N=p.N, K=p.K, A=p.A.cuda(), B=p.B.cuda(), C=p.C.cuda(),
+                        D=torch.full((p.M, p.N), float("nan"), dtype=torch.float16,
+                                     device="cuda")))
+    plan.grouped(dev, alpha=probs[0].alpha, beta=probs[0].beta)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    assert plan.last_config()["cta_group"] == cg
+    for p, t in zip(probs, dev):
+        assert_bit_exact(p, inputs.bits(t["D"].cpu()))
+
+
+def test_batched_bit_exact():
+    batch, M, N, K = 5, 264, 392, 1040
+    probs = [inputs.integer_problem(M, N, K, dtype="bf16", seed=b) for b in range(batch)]
+    A = torch.stack([p.A for p in probs]).cuda()
+    B = torch.stack([p.B for p in probs]).cuda()
+    C = torch.stack([p.C for p in probs]).cuda()
+    D = torch.full((batch, M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    plan = _plan(probs[0])
+    plan.batched(A, B, C, D, M, N, K, batch, M * K, K * N, M * N, M * N,
+                 alpha=probs[0].alpha, beta=probs[0].beta)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    Dh = D.cpu()
+    for b, p in enumerate(probs):
+        assert_bit_exact(p, inputs.bits(Dh[b].contiguous()))
+
+
+# ------------------------------------------------------------------ special values
+
+def test_relu_of_nan_from_c_stays_nan():
+    """ReLU with beta != 0 and NaN entries in C: those elements of D are NaN
+    (NaN propagates through ReLU), every other element is bit-exact."""
+    prob = inputs.integer_problem(264, 392, 1024, dtype="f16", act="relu")
+    C = prob.C.clone()
+    nan_at = [(0, 0), (17, 255), (130, 3), (263, 391), (200, 256)]
+    for i, j in nan_at:
+        C[i, j] = float("nan")
+    prob.C = C
+    for sched in (g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT):
+        d = _run_args(_plan(prob, schedule=sched), prob)
+        want = oracle_bits(prob)
+        isnan = np.isnan(d.view(np.float16))
+        assert set(map(tuple, np.argwhere(isnan))) == set(nan_at)
+        assert np.array_equal(d[~isnan], want[~isnan])
+
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SPLIT])
+def test_fp16_overflow_rounds_to_inf(sched):
+    """Exact sums around the top of fp16: 65504 stays, 65519 rounds down to
+    65504, 65520 (half way to 65536) rounds to even, which is infinity, and
+    larger sums give +-inf; compared bit for bit with the oracle's rounding."""
+    M, N, K = 128, 128, 64
+    targets = [65504, 65519, 65520, 65535, 70000, 131072, -65519, -65520, -1000000]
+    A = torch.zeros(M, K, dtype=torch.float16)
+    B = torch.ones(K, N, dtype=torch.float16)
+    # row i of A . B = targets[i]: A[i, :] holds the target as a sum of
+    # exactly representable fp16 parts (each rounded toward zero)
+    for i, t in enumerate(targets):
+        r, k = float(t), 0
+        while r != 0.0:
+            p = float(np.float16(r))
+            if abs(p) > abs(r) or not np.isfinite(p):
+                p = float(np.nextafter(np.float16(p if np.isfinite(p) else np.sign(r) * 65504),
+                                       np.float16(0)))
+            p = max(-65504.0, min(65504.0, p))
+            A[i, k] = p
+            r -= p
+            k += 1
+        assert float(A[i].double().sum()) == t
+    prob = inputs.Problem("overflow", A, B, None, M, N, K, act="linear")
+    d = _run_args(_plan(prob, schedule=sched), prob)
+    want = oracle_bits(prob)
+    assert np.array_equal(d, want)
+    v = d.view(np.float16).astype(np.float64)
+    assert np.isposinf(v[2]).all() and np.isposinf(v[5]).all() and np.isneginf(v[7]).all()
+    assert (v[1] == 65504).all()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("act", ["sigmoid", "tanh"])
+def test_activation_saturation(dtype, act):
+    """Pre-activation values of magnitude 20 to 60000: sigmoid gives 0 or 1 and
+    tanh +-1 up to the output rounding, never NaN (compared with the oracle's
+    value rounded to the output type, allowing one unit of the format in the
+    last place for the approximate exponential and tanh)."""
+    M, N, K = 128, 64, 16
+    vals = [20.0, -20.0, 30.0, -30.0, 88.0, -88.0, 100.0, -100.0, 1000.0, -1000.0, 60000.0,
+            -60000.0]
+    A = torch.zeros(M, K, dtype=inputs.TORCH_DTYPE[dtype])
+    for i, v in enumerate(vals):
+        A[i, 0] = v
+    B = torch.zeros(K, N, dtype=inputs.TORCH_DTYPE[dtype])
+    B[0, :] = 1.0
+    prob = inputs.Problem("saturation", A, B, None, M, N, K, act=act, a_dtype=dtype,
+                          b_dtype=dtype, c_dtype=dtype, d_dtype=dtype)
+    d = _run_args(_plan(prob), prob)
+    want = oracle_bits(prob)
+    got = torch.from_numpy(d.view(np.int16)).view(inputs.TORCH_DTYPE[dtype]).double().numpy()
+    ref = torch.from_numpy(want.view(np.int16)).view(inputs.TORCH_DTYPE[dtype]).double().numpy()
+    assert np.isfinite(got).all()
+    ulp = 2.0 ** -10 if dtype == "f16" else 2.0 ** -7
+    assert np.all(np.abs(got - ref) <= ulp * np.maximum(np.abs(ref), 2.0 ** -14) + 1e-30)
+    for i, v in enumerate(vals):
+        if act == "sigmoid":
+            assert np.all(got[i] == (1.0 if v > 0 else ref[i]))
+        else:
+            assert np.all(got[i] == (1.0 if v > 0 else -1.0))
+
+
+# ------------------------------------------------------------------ host-buffer entry point
+
+def _run_host(plan, prob, stream=None):
+    hA, hB = prob.A.pin_memory(), prob.B.pin_memory()
+    hC = prob.C.pin_memory() if prob.C is not None else None
+    hD = torch.full((prob.M, prob.N), float("nan"), dtype=inputs.TORCH_DTYPE[prob.d_dtype]).pin_memory()
+    st = g.gemm_run_host(plan.handle, hA, hB, hC, hD, prob.M, prob.N, prob.K, prob.alpha,
+                         prob.beta, prob.scale_a, prob.scale_b, stream)
+    return st, inputs.bits(hD)
+
+
+@pytest.mark.parametrize("dtype,beta", [("f16", 0.5), ("bf16", 0.0), ("e4m3", 0.0)])
+def test_gemm_run_host_bit_exact(dtype, beta):
+    """gemm_run_host (host buffers, copies inside the call) against the
+    oracle; fp8 with HOST scales 1/2 and 1/4."""
+    kw = dict(scale_a=0.5, scale_b=0.25) if dtype == "e4m3" else {}
+    prob = inputs.integer_problem(520, 528, 4224, dtype=dtype, beta=beta, act="relu", **kw)
+    plan = _plan(prob)
+    for _ in range(2):  # the second call reuses the plan's device buffers
+        st, d = _run_host(plan, prob)
+        assert st == g.OK, g.status_string(st)
+        assert_bit_exact(prob, d)
+
+
+def test_gemm_run_host_k_zero_and_empty():
+    prob = inputs.integer_problem(70, 136, 0, dtype="f16", act="relu")
+    prob.A = torch.empty(70, 0, dtype=torch.float16)
+    prob.B = torch.empty(0, 136, dtype=torch.float16)
+    plan = _plan(prob)
+    st, d = _run_host(plan, prob)
+    assert st == g.OK
+    assert_bit_exact(prob, d)
+    hD = torch.full((4, 8), 3.0, dtype=torch.float16)
+    assert g.gemm_run_host(plan.handle, None, None, None, hD, 0, 8, 16, 1.0, 0.0) == g.OK
+    assert torch.all(hD == 3.0)
+
+
+def test_gemm_run_host_reports_and_clears_a_timeout():
+    """A stream-K peer that skips its flag (test hook): gemm_run_host returns
+    the device timeout and clears the status word, so the next call is OK."""
+    prob = inputs.integer_problem(256, 512, 8192, dtype="f16")
+    plan = _plan(prob, schedule=g.SCHED_SK, timeout_us=20000, fault_skip_flag=1)
+    st, _ = _run_host(plan, prob)
+    assert st == g.ERR_TIMEOUT
+    plan.set(g.OPT_FAULT_SKIP_FLAG, -1)
+    st, d = _run_host(plan, prob)
+    assert st == g.OK, g.status_string(st)
+    assert plan.query_error() == g.OK
+    assert_bit_exact(prob, d)

@@ -116,3 +116,42 @@ def test_block_scaled_problem_through_the_oracle(elem, block, scale):
     p.block_scales = (sa, sb.clone().fill_(127 if scale == "ue8m0" else 0x38), sdt, blk)
     d_bad, _, _ = check.reference(p, I.bits)
     assert not check.compare(oracle.round_to(d_bad, "bf16"), "bf16", d_ref, absab, c64, p)[0]
+
+
+def test_integer_problems_are_exact_in_fp32():
+    """The small-integer problems of the bit-exact GPU tests: the oracle's
+    result equals exact integer arithmetic (numpy int64 on the decoded
+    operands, scaled by alpha, beta and the fp8 scales as exact fractions),
+    and every magnitude the GPU forms (the k sums, alpha * sum, the epilogue
+    terms) stays below 2^24, so fp32 holds each of them exactly."""
+    from fractions import Fraction
+    import oracle
+    for dtype, kw in (("f16", dict(bias=True, aux_op="mul")), ("bf16", dict(aux_op="div")),
+                      ("e4m3", dict(beta=0.0, scale_a=0.5, scale_b=0.25, bias=True))):
+        p = I.integer_problem(24, 40, 4224, dtype=dtype, act="linear", **kw)
+        a = p.A.double().numpy().astype(np.int64)
+        b = p.B.double().numpy().astype(np.int64)
+        assert np.abs(a).max() <= 2 and np.abs(b).max() <= 2
+        s = a @ b
+        assert np.abs(s).max() * 4 < 2 ** 24
+        alpha = Fraction(p.alpha) * Fraction(p.scale_a) * Fraction(p.scale_b)
+        want = s.astype(object) * alpha
+        if p.beta != 0.0:
+            want = want + p.C.double().numpy().astype(np.int64).astype(object) * Fraction(p.beta)
+        if p.bias is not None:
+            want = want + p.bias.double().numpy().astype(np.int64).astype(object)[None, :]
+        if p.aux_op == "mul":
+            want = want * p.aux.double().numpy().astype(np.int64).astype(object)
+        elif p.aux_op == "div":
+            z = p.aux.double().numpy()
+            assert set(np.unique(z)) <= {0.5, 1.0, 2.0, 4.0}
+            want = want / np.vectorize(Fraction)(z).astype(object)
+        got = oracle.gemm(I.bits(p.A), p.a_dtype, I.bits(p.B), p.b_dtype,
+                          I.bits(p.C) if p.C is not None else None, p.c_dtype,
+                          alpha=p.alpha, beta=p.beta, scale_a=p.scale_a, scale_b=p.scale_b,
+                          bias=I.bits(p.bias) if p.bias is not None else None,
+                          bias_dtype=p.d_dtype,
+                          aux=I.bits(p.aux) if p.aux_op else None, aux_dtype=p.d_dtype,
+                          aux_op=p.aux_op)
+        assert all(Fraction(float(x)) == y for x, y in zip(got.ravel(), want.ravel()))
+        assert max(abs(float(y)) for y in want.ravel()) < 2 ** 23
