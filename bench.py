@@ -503,7 +503,7 @@ def run_gpu(args):
     # plan's cache after the first call), timed on the host; the launches are
     # real and drained afterwards, untimed
     host_c_us = None
-    if not grouped and p0.bias is None:
+    if not grouped and p0.bias is None and not args.no_e2e:
         lib = g.load()
         A, B, C, D = dv[0]
         lda = p0.M if p0.a_col_major else p0.K
@@ -522,7 +522,7 @@ def run_gpu(args):
 
     # end to end through the C ABI with pinned host buffers (single problems)
     e2e = None
-    if not grouped:
+    if not grouped and not args.no_e2e:
         hA, hB = p0.A.pin_memory(), p0.B.pin_memory()
         hC = p0.C.pin_memory() if p0.C is not None else None
         hD = torch.empty(p0.M, p0.N, dtype=I.TORCH_DTYPE[p0.d_dtype]).pin_memory()
@@ -605,6 +605,9 @@ def main(argv=None):
     ap.add_argument("--opt", action="append", help="plan option NAME=VALUE (e.g. schedule=1)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the host-buffer and host-overhead measurements (short launch "
+                         "lists for profiling)")
     ap.add_argument("--list", action="store_true")
     ap.add_argument("--autotune", action="store_true",
                     help="time every kernel configuration first and keep the fastest")

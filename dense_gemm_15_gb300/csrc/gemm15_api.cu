@@ -38,11 +38,12 @@ struct Options {
     int fault_skip_flag = -1;
     int sk_dp_waves = -1;
     int trace_items = 0;
+    int swap_ab = 0;  // 0 automatic, 1 never, 2 always (dense problems)
 };
 
 // Kernel choice fixed by gemm_plan_autotune for one problem shape.
 struct Tuned {
-    int schedule, cta_group, tile_n, sk_dp_waves, splits;
+    int schedule, cta_group, tile_n, sk_dp_waves, splits, swap_ab;
 };
 
 }  // namespace
@@ -205,6 +206,7 @@ struct Prob {
     const void* aux = nullptr;   // auxiliary tensor Z (layout of C / D), or null
     int64_t ldaux = 0;
     int aux_op = 0;
+    bool out_trans = false;      // computed (r, c) is stored at C / D / Z + c * ld + r
 };
 
 // Column-major C/D: compute D^T = B^T . A^T, which is row-major N x M.
@@ -223,6 +225,24 @@ Prob normalise(const gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const v
         p.bias_rows = true;  // the user's columns are the computed rows
     }
     return p;
+}
+
+// Swap-AB: the same product computed as its transpose, D^T = B^T . A^T, so
+// that a short M becomes the narrow N side of the MMA and the long N side
+// fills its 128 rows; the tile is then stored transposed.
+Prob swapped(const Prob& p) {
+    Prob q = p;
+    q.M = p.N;
+    q.N = p.M;
+    q.A = p.B;
+    q.lda = p.ldb;
+    q.a_kmajor = p.b_kmajor;
+    q.B = p.A;
+    q.ldb = p.lda;
+    q.b_kmajor = p.a_kmajor;
+    q.bias_rows = !p.bias_rows;
+    q.out_trans = !p.out_trans;
+    return q;
 }
 
 gemm15_status_t check_operands(const gemm15_plan* plan, const Prob& p, float beta) {
@@ -308,19 +328,32 @@ Options effective_options(const gemm15_plan* plan, int64_t M, int64_t N, int64_t
     }
     if (o.cta_group == 0) o.cta_group = t.cta_group;
     if (o.tile_n == 0) o.tile_n = t.tile_n;
+    if (o.swap_ab == 0) o.swap_ab = t.swap_ab;
     return o;
 }
 
-Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K) {
+// Swap-AB for a short computed M against a long N (decode-size token counts
+// against a weight matrix): unless the plan's option says otherwise.
+bool use_swap(const Options& o, const Prob& p) {
+    if (o.swap_ab == 1) return false;
+    if (o.swap_ab == 2) return true;
+    return p.M <= 128 && p.N >= 1024 && p.K >= 256;
+}
+
+// With `swap` the problem is a swapped one (swap-AB): single-SM tiles whose N
+// covers the short side, 64 wide for 16-bit operands when it fits (the
+// narrowest B stage that is a whole 128-byte swizzle row), else 128.
+Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const Options& o,
+                bool swap = false) {
     Decision d;
-    const Options o = effective_options(plan, M, N, K);
     d.bk = plan->elem == ELEM_E4M3 ? 128 : 64;
     d.bn = o.tile_n ? o.tile_n : (N <= 128 ? 128 : 256);
+    if (swap) d.bn = (plan->elem != ELEM_E4M3 && N <= 64) ? 64 : 128;
     const int G1 = o.grid > 0 ? std::min(o.grid, plan->num_sms) : plan->num_sms;
     int cg = 1;
     // SM-pair tiles 256 x 128 exist for 16-bit operands only (an fp8 half-tile
     // of B would be narrower than one 128-byte swizzle row)
-    const bool pair_ok = d.bn == 256 || plan->elem != ELEM_E4M3;
+    const bool pair_ok = !swap && (d.bn == 256 || plan->elem != ELEM_E4M3);
     const int clusters = std::min(pair_clusters(plan), G1 / 2);
     if (pair_ok && o.cta_group != 1) {
         const int64_t tiles2 = cdiv(M, 2 * TILE_M) * cdiv(N, 256);
@@ -443,8 +476,14 @@ cudaError_t launch_kernel(int elem, int bn, int cg, const GemmParams& gp, int gr
         if (elem == ELEM_BF16) return bn == 128 ? launch_gemm<ELEM_BF16, 128, 2>(gp, grid, s) : launch_gemm<ELEM_BF16, 256, 2>(gp, grid, s);
         return launch_gemm<ELEM_E4M3, 256, 2>(gp, grid, s);
     }
-    if (elem == ELEM_F16) return bn == 128 ? launch_gemm<ELEM_F16, 128>(gp, grid, s) : launch_gemm<ELEM_F16, 256>(gp, grid, s);
-    if (elem == ELEM_BF16) return bn == 128 ? launch_gemm<ELEM_BF16, 128>(gp, grid, s) : launch_gemm<ELEM_BF16, 256>(gp, grid, s);
+    if (elem == ELEM_F16) {
+        if (bn == 64) return launch_gemm<ELEM_F16, 64>(gp, grid, s);
+        return bn == 128 ? launch_gemm<ELEM_F16, 128>(gp, grid, s) : launch_gemm<ELEM_F16, 256>(gp, grid, s);
+    }
+    if (elem == ELEM_BF16) {
+        if (bn == 64) return launch_gemm<ELEM_BF16, 64>(gp, grid, s);
+        return bn == 128 ? launch_gemm<ELEM_BF16, 128>(gp, grid, s) : launch_gemm<ELEM_BF16, 256>(gp, grid, s);
+    }
     return bn == 128 ? launch_gemm<ELEM_E4M3, 128>(gp, grid, s) : launch_gemm<ELEM_E4M3, 256>(gp, grid, s);
 }
 
@@ -558,7 +597,9 @@ gemm15_status_t attach_trace(gemm15_plan* plan, GemmParams& gp, int grid, cudaSt
 // launch, with the tensor maps already encoded.
 struct LaunchEntry {
     bool valid = false;
-    Prob p{};
+    Prob p{};            // the caller's problem (after layout normalisation)
+    Prob pe{};           // the problem the kernel computes (swapped for swap-AB)
+    bool swap = false;
     bool has_c = false;
     Options opt{};       // the decision-relevant options at encoding time
     uint64_t tuned_gen = 0;
@@ -577,33 +618,39 @@ bool same_prob(const Prob& a, const Prob& b) {
            a.a_kmajor == b.a_kmajor && a.B == b.B && a.ldb == b.ldb && a.b_kmajor == b.b_kmajor &&
            a.C == b.C && a.ldc == b.ldc && a.D == b.D && a.ldd == b.ldd && a.bias == b.bias &&
            a.bias_rows == b.bias_rows && a.aux == b.aux && a.ldaux == b.ldaux &&
-           a.aux_op == b.aux_op;
+           a.aux_op == b.aux_op && a.out_trans == b.out_trans;
 }
 
 bool same_choice_options(const Options& a, const Options& b) {
     return a.schedule == b.schedule && a.splits == b.splits && a.cta_group == b.cta_group &&
            a.tile_n == b.tile_n && a.raster == b.raster && a.grid == b.grid &&
-           a.sk_dp_waves == b.sk_dp_waves;
+           a.sk_dp_waves == b.sk_dp_waves && a.swap_ab == b.swap_ab;
 }
 
 // Finds or builds the launch parameters of problem p (nullptr on an encoding
 // failure).
-const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& p, bool has_c) {
+const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& key, bool has_c) {
     if (!plan->cache) plan->cache = new (std::nothrow) LaunchCache();
     LaunchCache* cache = static_cast<LaunchCache*>(plan->cache);
     if (!cache) return nullptr;
     for (const LaunchEntry& e : cache->e)
         if (e.valid && e.has_c == has_c && e.tuned_gen == plan->tuned_gen &&
-            same_choice_options(e.opt, plan->opt) && same_prob(e.p, p))
+            same_choice_options(e.opt, plan->opt) && same_prob(e.p, key))
             return &e;
     LaunchEntry& e = cache->e[cache->next];
     cache->next = (cache->next + 1) % CACHE_ENTRIES;
     e.valid = false;
-    const Decision d = decide(plan, p.M, p.N, p.K);
+    // options with this shape's autotuned choice filled in
+    const Options o = effective_options(plan, key.M, key.N, key.K);
+    const bool swap = use_swap(o, key);
+    const Prob p = swap ? swapped(key) : key;  // the problem the kernel computes
+    const Decision d = decide(plan, p.M, p.N, p.K, o, swap);
     GemmParams& gp = e.gp;
     std::memset(&gp, 0, sizeof(gp));
     if (!operand_maps(plan, p, d.bn / d.cg, &gp.tmA, &gp.tmB)) return nullptr;
-    if (!output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return nullptr;
+    // a transposed output is read and written element-wise (no tensor maps)
+    if (!p.out_trans && !output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return nullptr;
+    gp.out_trans = p.out_trans ? 1 : 0;
     gp.D = p.D;
     gp.ldd = p.ldd;
     gp.C = has_c ? p.C : nullptr;
@@ -631,7 +678,9 @@ const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& p, bool has_c) {
     fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.groups = nullptr;
     gp.num_groups = 0;
-    e.p = p;
+    e.p = key;
+    e.pe = p;
+    e.swap = swap;
     e.has_c = has_c;
     e.opt = plan->opt;
     e.tuned_gen = plan->tuned_gen;
@@ -684,6 +733,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     const LaunchEntry* le = launch_entry(plan, p, has_c);
     if (!le) return GEMM15_ERR_CUDA;
     const Decision& d = le->d;
+    const Prob& pe = le->pe;
     st = ensure_ws(plan, d.ws_bytes, d.flags);
     if (st != GEMM15_OK) return st;
 
@@ -710,21 +760,22 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.n_blocks = d.n_blocks;
         rp.M = gp.M;
         rp.N = gp.N;
-        rp.C = p.C;
-        rp.ldc = p.ldc;
-        rp.D = p.D;
-        rp.ldd = p.ldd;
+        rp.C = pe.C;
+        rp.ldc = pe.ldc;
+        rp.D = pe.D;
+        rp.ldd = pe.ldd;
         rp.alpha = alpha;
         rp.beta = beta;
         rp.scale_a = scale_a;
         rp.scale_b = scale_b;
         rp.act = act;
         rp.has_c = has_c;
-        rp.bias = p.bias;
-        rp.bias_rows = p.bias_rows;
-        rp.aux = p.aux;
-        rp.ldaux = p.ldaux;
-        rp.aux_op = p.aux_op;
+        rp.bias = pe.bias;
+        rp.bias_rows = pe.bias_rows;
+        rp.aux = pe.aux;
+        rp.ldaux = pe.ldaux;
+        rp.aux_op = pe.aux_op;
+        rp.out_trans = pe.out_trans ? 1 : 0;
         if (d.balanced) {
             rp.units = d.grid;
             rp.sk_units = d.sk_units;
@@ -736,6 +787,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         ++launches;
     }
     record_config(plan, d, launches);
+    if (le->swap) plan->last.swap_ab ^= 1;
     return mark_done(plan, s);
 }
 
@@ -920,11 +972,13 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
             for (int bn : {128, 256}) {
                 if (cg == 2 && bn == 128 && plan->elem == ELEM_E4M3) continue;
                 if (sched == SCHED_SK) {
-                    for (int w : {-1, 0}) cands.push_back(Tuned{sched, cg, bn, w, 0});
+                    for (int w : {-1, 0}) cands.push_back(Tuned{sched, cg, bn, w, 0, 1});
                 } else {
-                    cands.push_back(Tuned{sched, cg, bn, -1, 0});
+                    cands.push_back(Tuned{sched, cg, bn, -1, 0, 1});
                 }
             }
+    // swap-AB (its own tile shape): each schedule once
+    for (int sched : {SCHED_DP, SCHED_SK, SCHED_SPLIT}) cands.push_back(Tuned{sched, 1, 0, -1, 0, 2});
     const Options saved = plan->opt;
     // every timed run starts from an L2 that holds none of the operands (a
     // write of twice the L2 size), as when they do not stay in L2 between uses
@@ -952,6 +1006,7 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
         plan->opt.tile_n = c.tile_n;
         plan->opt.sk_dp_waves = c.sk_dp_waves;
         plan->opt.splits = c.splits;
+        plan->opt.swap_ab = c.swap_ab;
         gemm15_tune_result_t r{};
         r.sk_dp_waves = c.sk_dp_waves;
         r.us = -1.0f;
@@ -1358,6 +1413,10 @@ gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option,
         case GEMM15_OPT_TRACE_ITEMS:
             if (v < 0 || v > 65536) return GEMM15_ERR_INVALID_ARG;
             o.trace_items = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_SWAP_AB:
+            if (v < 0 || v > 2) return GEMM15_ERR_INVALID_ARG;
+            o.swap_ab = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_FAULT_SKIP_FLAG:
             if (v < -1 || v > 100000) return GEMM15_ERR_INVALID_ARG;

@@ -779,7 +779,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int32_t row0 = m0 + q * 32;      // first row of this warp
             const bool rows_live = row0 < M;
             const bool to_ws = (w.kind == WK_PEER || w.kind == WK_SPLIT);
-            const bool stage_c = has_c && !to_ws && rows_live;
+            // a transposed output (swap-AB) reads C and writes D element-wise
+            const bool stage_c = has_c && !to_ws && rows_live && !p.out_trans;
             const int nch = min(NCH, (N - n0 + EPI_COLS - 1) / EPI_COLS);
             // bias of this thread's row (bias indexed by output row)
             float bias_row = 0.0f;
@@ -966,6 +967,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     continue;
                 }
+                if (p.out_trans) {
+                    // swap-AB: computed element (row, n0 + col0 + i) is stored element
+                    // (n0 + col0 + i, row) of C / D / Z; for a fixed i the warp's 32
+                    // lanes touch 32 consecutive elements (64 bytes)
+                    const int32_t my_row = row0 + lane;
+                    const int32_t cvalid = N - (n0 + col0);  // columns of this chunk in range
+                    const bool live = my_row < M;
+                    const int64_t c0 = static_cast<int64_t>(n0) + col0;
+                    if (has_c && live) {
+                        const uint16_t* cb = static_cast<const uint16_t*>(p.C) + my_row;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            const float cv = i < cvalid ? half_bits_to_float<ELEM>(cb[(c0 + i) * p.ldc]) : 0.0f;
+                            v[i] = fmaf(beta, cv, alpha * v[i]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) v[i] *= alpha;
+                    }
+                    if (has_bias && p.bias_rows) {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) v[i] += bias_row;
+                    } else if (has_bias) {
+                        // bias by computed column: the same 64 elements for every lane
+                        const uint16_t* bb = static_cast<const uint16_t*>(p.bias) + c0;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            v[i] += i < cvalid ? half_bits_to_float<ELEM>(__ldg(bb + i)) : 0.0f;
+                    }
+                    activate_all(v, act);
+                    if (p.aux_op && live) {
+                        const uint16_t* zb = static_cast<const uint16_t*>(p.aux) + my_row;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            const float z = i < cvalid ? half_bits_to_float<ELEM>(zb[(c0 + i) * p.ldaux]) : 1.0f;
+                            v[i] = aux_apply(v[i], z, p.aux_op);
+                        }
+                    }
+                    if (live) {
+                        uint16_t* db = reinterpret_cast<uint16_t*>(Dptr) + my_row;
+#pragma unroll
+                        for (int i = 0; i < 64; i += 2) {
+                            const uint32_t pr = pack2<ELEM>(v[i], v[i + 1]);
+                            if (i < cvalid) db[(c0 + i) * ldd] = static_cast<uint16_t>(pr);
+                            if (i + 1 < cvalid) db[(c0 + i + 1) * ldd] = static_cast<uint16_t>(pr >> 16);
+                        }
+                    }
+                    continue;
+                }
                 if (stage_c) {
                     if (!wait_bar(ctl, c_bar(e, b), (c_phase >> b) & 1u)) {
                         ok = false;
@@ -1137,7 +1187,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // split order, eight splits' loads in flight at a time.
 template <int ELEM>
 __global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
-    using OutT = typename OutType<ELEM>::T;
     constexpr int V = REDUCE_COLS;
     const int64_t nv = (p.N + V - 1) / V;
     const int64_t total = static_cast<int64_t>(p.M) * nv;
@@ -1222,31 +1271,28 @@ __global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __g
                 else if (t < nvalid) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + n + t));
             }
         }
-        const OutT* crow = reinterpret_cast<const OutT*>(p.C) + static_cast<int64_t>(m) * p.ldc + n;
-        OutT* drow = reinterpret_cast<OutT*>(p.D) + static_cast<int64_t>(m) * p.ldd + n;
+        // element (m, n + t) of the computed output: row-major, or transposed (swap-AB)
+        auto at = [&](int64_t ld, int t) -> int64_t {
+            return p.out_trans ? static_cast<int64_t>(n + t) * ld + m : static_cast<int64_t>(m) * ld + n + t;
+        };
+        const uint16_t* cb = static_cast<const uint16_t*>(p.C);
+        uint16_t* db = static_cast<uint16_t*>(p.D);
         float o[V];
 #pragma unroll
         for (int t = 0; t < V; ++t) {
             float x = alpha * acc[t];
-            if (p.has_c && t < nvalid) {
-                float cv;
-                if constexpr (ELEM == ELEM_F16) cv = __half2float(crow[t]);
-                else cv = __bfloat162float(crow[t]);
-                x = fmaf(p.beta, cv, x);
-            }
+            if (p.has_c && t < nvalid) x = fmaf(p.beta, half_bits_to_float<ELEM>(cb[at(p.ldc, t)]), x);
             o[t] = activate(x + bias[t], p.act);
             if (p.aux_op && t < nvalid) {
-                const uint16_t z = static_cast<const uint16_t*>(p.aux)[static_cast<int64_t>(m) * p.ldaux + n + t];
+                const uint16_t z = static_cast<const uint16_t*>(p.aux)[at(p.ldaux, t)];
                 o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);
             }
         }
-        if (nvalid == V) {
-            *reinterpret_cast<uint2*>(drow) = make_uint2(pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3]));
+        const uint32_t pk[2] = {pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3])};
+        if (nvalid == V && !p.out_trans) {
+            *reinterpret_cast<uint2*>(db + at(p.ldd, 0)) = make_uint2(pk[0], pk[1]);
         } else {
-            for (int t = 0; t < nvalid; ++t) {
-                if constexpr (ELEM == ELEM_F16) drow[t] = __float2half_rn(o[t]);
-                else drow[t] = __float2bfloat16_rn(o[t]);
-            }
+            for (int t = 0; t < nvalid; ++t) db[at(p.ldd, t)] = static_cast<uint16_t>(pk[t >> 1] >> (16 * (t & 1)));
         }
     }
 }

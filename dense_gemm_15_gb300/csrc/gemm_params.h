@@ -58,6 +58,9 @@ struct GemmParams {
     const void* aux;                  // auxiliary tensor Z (output type, row-major), or null
     int64_t ldaux;
     int32_t aux_op;                   // 0 none, 1 add, 2 sub, 3 mul, 4 div
+    int32_t out_trans;                // 1: the computed tile is the transpose of the stored
+                                      // one (swap-AB): element (r, c) of the computed output
+                                      // lives at C / D / Z + c * ld + r
     // operand layouts in shared memory (bytes) and the MMA instruction descriptor
     uint32_t a_kmajor, b_kmajor;
     uint32_t a_lbo, a_sbo, a_kstep;
@@ -105,6 +108,7 @@ struct ReduceParams {
     const void* aux;
     int64_t ldaux;
     int32_t aux_op;
+    int32_t out_trans;                // as in GemmParams
     // balanced split-K: the partials come from a stream-K partition of
     // sk_units iterations over units units (0 = classic split-K layout)
     int32_t units;

@@ -2,6 +2,7 @@
 #include "launch_impl.cuh"
 
 namespace g15 {
+template cudaError_t launch_gemm<ELEM_BF16, 64>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_BF16, 128>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_BF16, 256>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_BF16, 256, 2>(const GemmParams&, int, cudaStream_t);

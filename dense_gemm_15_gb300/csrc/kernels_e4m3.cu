@@ -10,6 +10,7 @@ template int max_pair_clusters<ELEM_E4M3>();
 int gemm_smem_bytes(int elem, int bn, int cg) {
     if (cg == 2) return bn == 128 ? Traits<ELEM_F16, 128, 2>::SMEM_BYTES : Traits<ELEM_F16, 256, 2>::SMEM_BYTES;
     if (elem == ELEM_E4M3) return bn == 128 ? Traits<ELEM_E4M3, 128>::SMEM_BYTES : Traits<ELEM_E4M3, 256>::SMEM_BYTES;
+    if (bn == 64) return Traits<ELEM_F16, 64>::SMEM_BYTES;
     return bn == 128 ? Traits<ELEM_F16, 128>::SMEM_BYTES : Traits<ELEM_F16, 256>::SMEM_BYTES;
 }
 int gemm_stages(int elem, int bn, int cg) {
@@ -18,6 +19,7 @@ int gemm_stages(int elem, int bn, int cg) {
         return bn == 128 ? Traits<ELEM_F16, 128, 2>::STAGES : Traits<ELEM_F16, 256, 2>::STAGES;
     }
     if (elem == ELEM_E4M3) return bn == 128 ? Traits<ELEM_E4M3, 128>::STAGES : Traits<ELEM_E4M3, 256>::STAGES;
+    if (bn == 64) return Traits<ELEM_F16, 64>::STAGES;
     return bn == 128 ? Traits<ELEM_F16, 128>::STAGES : Traits<ELEM_F16, 256>::STAGES;
 }
 int gemm_max_pair_clusters(int elem) {

@@ -255,9 +255,16 @@ typedef enum {
                                        partial-ready flag (-1 = none) */
     GEMM15_OPT_SK_DP_WAVES = 8,    /* stream-K: full waves run data-parallel before
                                       the stream-K region (-1 = auto) */
-    GEMM15_OPT_TRACE_ITEMS = 9     /* record a per-CTA timeline of up to this many
+    GEMM15_OPT_TRACE_ITEMS = 9,    /* record a per-CTA timeline of up to this many
                                       work items per launch (0 = off); read it
                                       with gemm_plan_trace */
+    GEMM15_OPT_SWAP_AB = 10        /* dense runs: 0 auto (swap-AB when the computed
+                                      M <= 128 against N >= 1024 and K >= 256),
+                                      1 never, 2 always.  Swap-AB computes
+                                      D^T = B^T . A^T on 128 x 64 (16-bit, M <= 64)
+                                      or 128 x 128 single-SM tiles and stores the
+                                      tile transposed; GEMM15_OPT_TILE_N and
+                                      GEMM15_OPT_CTA_GROUP do not apply to it */
 } gemm15_option_t;
 
 /* Sets an option on the plan; INVALID_ARG for unknown options or values. */
@@ -277,7 +284,10 @@ typedef struct {
                             each tile's pieces) */
     int32_t raster;      /* M-blocks per raster band */
     int32_t launches;    /* kernels launched by the run */
-    int32_t swap_ab;     /* 1 if the run computed D^T = B^T . A^T */
+    int32_t swap_ab;     /* 1 if the kernel computed the transpose of the stored
+                            product with A and B swapped: D^T = B^T . A^T for
+                            row-major C/D under swap-AB, or column-major C/D
+                            without it */
 } gemm15_config_t;
 
 gemm15_status_t gemm_plan_last_config(gemm15_plan_t plan, gemm15_config_t* out);

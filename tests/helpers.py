@@ -92,7 +92,10 @@ def row_subproblem(prob, idx):
     import copy
     idx = torch.as_tensor(np.asarray(idx, dtype=np.int64))
     sub = copy.copy(prob)
-    sub.A = (prob.A[:, idx] if prob.a_col_major else prob.A[idx]).contiguous()
+    # rows are gathered on the stored bytes (torch has no CPU indexing for fp8)
+    a = prob.A.view(torch.uint8) if prob.A.element_size() == 1 else prob.A
+    a = (a[:, idx] if prob.a_col_major else a[idx]).contiguous()
+    sub.A = a.view(prob.A.dtype) if prob.A.element_size() == 1 else a
     sub.C = prob.C[idx].contiguous() if prob.C is not None else None
     if getattr(prob, "aux", None) is not None:
         sub.aux = prob.aux[idx].contiguous()

@@ -247,6 +247,7 @@ def test_llama70b_layers(layer):
                                   a_dtype="bf16", b_dtype="bf16", c_dtype="bf16", d_dtype="bf16")
         plan = plan or plan_for(prob)
         d = run_gpu(plan, prob)
+        assert plan.last_config()["swap_ab"] == (1 if M <= 128 else 0)
         # one window in every 256-row band (each M-tile band of the kernels)
         assert_windows_match_oracle(prob, d, band_windows(M, band=256, span=4, seed=M))
 
