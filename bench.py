@@ -175,6 +175,8 @@ def algorithmic_bytes(probs):
             tot += p.N * 2
         if getattr(p, "aux", None) is not None:
             tot += p.M * p.N * 2
+        if getattr(p, "pre", None) is not None:
+            tot += p.M * p.N * 2
     return tot
 
 

@@ -51,7 +51,8 @@ class Args(ctypes.Structure):
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("alpha", ctypes.c_float),
                 ("beta", ctypes.c_float), ("scale_a", ctypes.c_void_p),
                 ("scale_b", ctypes.c_void_p), ("bias", ctypes.c_void_p),
-                ("aux", ctypes.c_void_p), ("ldaux", ctypes.c_int64), ("aux_op", ctypes.c_int32)]
+                ("aux", ctypes.c_void_p), ("ldaux", ctypes.c_int64), ("aux_op", ctypes.c_int32),
+                ("pre", ctypes.c_void_p), ("ldpre", ctypes.c_int64)]
 
 
 class Problem(ctypes.Structure):
@@ -220,11 +221,12 @@ def grouped_gemm_run(plan, problems, alpha=1.0, beta=0.0, stream=None):
 
 def gemm_run_args(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0, ldd=0,
                   scale_a=None, scale_b=None, bias=None, aux=None, ldaux=0, aux_op=None,
-                  stream=None):
-    """aux_op: None, "add", "sub", "mul", "div" (or its code)."""
+                  pre=None, ldpre=0, stream=None):
+    """aux_op: None, "add", "sub", "mul", "div" (or its code); pre: optional
+    output of the pre-activation value."""
     op = AUX_OPS[aux_op] if aux_op is None or isinstance(aux_op, str) else int(aux_op)
     args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
-                _ptr(scale_a), _ptr(scale_b), _ptr(bias), _ptr(aux), ldaux, op)
+                _ptr(scale_a), _ptr(scale_b), _ptr(bias), _ptr(aux), ldaux, op, _ptr(pre), ldpre)
     return load().gemm_run_args(plan, ctypes.byref(args), _stream(stream))
 
 
@@ -233,7 +235,7 @@ def gemm_plan_autotune(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ld
                        stream=None):
     """Returns (status, [result dicts, fastest first])."""
     args = Args(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K, alpha, beta,
-                _ptr(scale_a), _ptr(scale_b), _ptr(bias), None, 0, 0)
+                _ptr(scale_a), _ptr(scale_b), _ptr(bias), None, 0, 0, None, 0)
     cap = 64
     out = (TuneResult * cap)()
     n = ctypes.c_int32()

@@ -206,7 +206,9 @@ struct Prob {
     const void* aux = nullptr;   // auxiliary tensor Z (layout of C / D), or null
     int64_t ldaux = 0;
     int aux_op = 0;
-    bool out_trans = false;      // computed (r, c) is stored at C / D / Z + c * ld + r
+    void* pre = nullptr;         // pre-activation output Y (layout of D), or null
+    int64_t ldpre = 0;
+    bool out_trans = false;      // computed (r, c) is stored at C / D / Z / Y + c * ld + r
 };
 
 // Column-major C/D: compute D^T = B^T . A^T, which is row-major N x M.
@@ -273,6 +275,10 @@ gemm15_status_t check_operands(const gemm15_plan* plan, const Prob& p, float bet
     if (p.aux_op) {
         if (!p.aux || p.ldaux < p.N) return GEMM15_ERR_INVALID_ARG;
         if (!aligned16(p.aux) || (p.ldaux * eo) % 16) return GEMM15_ERR_ALIGNMENT;
+    }
+    if (p.pre) {
+        if (p.ldpre < p.N) return GEMM15_ERR_INVALID_ARG;
+        if (!aligned16(p.pre) || (p.ldpre * eo) % 16) return GEMM15_ERR_ALIGNMENT;
     }
     return GEMM15_OK;
 }
@@ -618,7 +624,8 @@ bool same_prob(const Prob& a, const Prob& b) {
            a.a_kmajor == b.a_kmajor && a.B == b.B && a.ldb == b.ldb && a.b_kmajor == b.b_kmajor &&
            a.C == b.C && a.ldc == b.ldc && a.D == b.D && a.ldd == b.ldd && a.bias == b.bias &&
            a.bias_rows == b.bias_rows && a.aux == b.aux && a.ldaux == b.ldaux &&
-           a.aux_op == b.aux_op && a.out_trans == b.out_trans;
+           a.aux_op == b.aux_op && a.pre == b.pre && a.ldpre == b.ldpre &&
+           a.out_trans == b.out_trans;
 }
 
 bool same_choice_options(const Options& a, const Options& b) {
@@ -675,6 +682,8 @@ const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& key, bool has_c) 
     gp.aux = p.aux;
     gp.ldaux = p.ldaux;
     gp.aux_op = d.sched == SCHED_SPLIT ? 0 : p.aux_op;
+    gp.pre = d.sched == SCHED_SPLIT ? nullptr : p.pre;  // split-K: the reduction stores it
+    gp.ldpre = p.ldpre;
     fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.groups = nullptr;
     gp.num_groups = 0;
@@ -722,6 +731,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.aux = p.aux;
         rp.ldaux = p.ldaux;
         rp.aux_op = p.aux_op;
+        rp.pre = p.pre;
+        rp.ldpre = p.ldpre;
         if (launch_reduce_kernel(plan->out_elem, rp, s, plan->num_sms) != cudaSuccess) return GEMM15_ERR_CUDA;
         Decision d;
         d.sched = SCHED_SPLIT;
@@ -775,6 +786,8 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
         rp.aux = pe.aux;
         rp.ldaux = pe.ldaux;
         rp.aux_op = pe.aux_op;
+        rp.pre = pe.pre;
+        rp.ldpre = pe.ldpre;
         rp.out_trans = pe.out_trans ? 1 : 0;
         if (d.balanced) {
             rp.units = d.grid;
@@ -931,6 +944,8 @@ gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* a, void* 
     p.aux_op = a->aux_op;
     p.aux = a->aux_op ? a->aux : nullptr;
     p.ldaux = a->ldaux ? a->ldaux : (cd_row ? a->N : a->M);
+    p.pre = a->pre;
+    p.ldpre = a->ldpre ? a->ldpre : (cd_row ? a->N : a->M);
     return run_dense(plan, p, a->alpha, a->beta, a->scale_a, a->scale_b,
                      static_cast<cudaStream_t>(stream));
 }
@@ -957,6 +972,8 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
     p.aux_op = a->aux_op;
     p.aux = a->aux_op ? a->aux : nullptr;
     p.ldaux = a->ldaux ? a->ldaux : (cd_row ? a->N : a->M);
+    p.pre = a->pre;
+    p.ldpre = a->ldpre ? a->ldpre : (cd_row ? a->N : a->M);
     gemm15_status_t st = check_operands(plan, p, a->beta);
     if (st != GEMM15_OK) return st;
     if (p.M == 0 || p.N == 0 || p.K == 0) return GEMM15_OK;  // one fixed path: nothing to choose
@@ -977,8 +994,9 @@ gemm15_status_t gemm_plan_autotune(gemm15_plan_t plan, const gemm15_args_t* a, i
                     cands.push_back(Tuned{sched, cg, bn, -1, 0, 1});
                 }
             }
-    // swap-AB (its own tile shape): each schedule once
-    for (int sched : {SCHED_DP, SCHED_SK, SCHED_SPLIT}) cands.push_back(Tuned{sched, 1, 0, -1, 0, 2});
+    // swap-AB (its own tile shape), each schedule once, where one side is short
+    if (std::min(p.M, p.N) <= 256)
+        for (int sched : {SCHED_DP, SCHED_SK, SCHED_SPLIT}) cands.push_back(Tuned{sched, 1, 0, -1, 0, 2});
     const Options saved = plan->opt;
     // every timed run starts from an L2 that holds none of the operands (a
     // write of twice the L2 size), as when they do not stay in L2 between uses

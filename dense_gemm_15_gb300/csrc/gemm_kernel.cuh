@@ -195,6 +195,27 @@ __device__ __forceinline__ uint4 load_bias8(const void* bias, int64_t c, int64_t
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Stores the first min(64, left) of 64 fp32 values, rounded to the 16-bit
+// output type, at dst (a row of 64 elements starting on a 16-byte boundary):
+// 16-byte stores when the row is whole, element stores otherwise.
+template <int ELEM>
+__device__ __forceinline__ void store_row64(uint16_t* dst, const float (&v)[64], int32_t left) {
+    if (left >= 64) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(dst + 8 * j) =
+                make_uint4(pack2<ELEM>(v[8 * j], v[8 * j + 1]), pack2<ELEM>(v[8 * j + 2], v[8 * j + 3]),
+                           pack2<ELEM>(v[8 * j + 4], v[8 * j + 5]), pack2<ELEM>(v[8 * j + 6], v[8 * j + 7]));
+    } else {
+#pragma unroll
+        for (int t = 0; t < 64; t += 2) {
+            const uint32_t pr = pack2<ELEM>(v[t], v[t + 1]);
+            if (t < left) dst[t] = static_cast<uint16_t>(pr);
+            if (t + 1 < left) dst[t + 1] = static_cast<uint16_t>(pr >> 16);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ errors
 
 struct Ctl {
@@ -996,6 +1017,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int i = 0; i < 64; ++i)
                             v[i] += i < cvalid ? half_bits_to_float<ELEM>(__ldg(bb + i)) : 0.0f;
                     }
+                    if (p.pre && live) {
+                        // the pre-activation output, transposed like D
+                        uint16_t* yb = static_cast<uint16_t*>(p.pre) + my_row;
+#pragma unroll
+                        for (int i = 0; i < 64; i += 2) {
+                            const uint32_t pr = pack2<ELEM>(v[i], v[i + 1]);
+                            if (i < cvalid) yb[(c0 + i) * p.ldpre] = static_cast<uint16_t>(pr);
+                            if (i + 1 < cvalid) yb[(c0 + i + 1) * p.ldpre] = static_cast<uint16_t>(pr >> 16);
+                        }
+                    }
                     activate_all(v, act);
                     if (p.aux_op && live) {
                         const uint16_t* zb = static_cast<const uint16_t*>(p.aux) + my_row;
@@ -1074,6 +1105,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
+                if (p.pre && my_row < M)  // the pre-activation output
+                    store_row64<ELEM>(static_cast<uint16_t*>(p.pre) + static_cast<int64_t>(my_row) * p.ldpre +
+                                          n0 + col0, v, left);
                 activate_all(v, act);
                 if (p.aux_op && my_row < M) {
                     // the auxiliary tensor's 64 columns of this row, 16 bytes at a time
@@ -1282,7 +1316,12 @@ __global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __g
         for (int t = 0; t < V; ++t) {
             float x = alpha * acc[t];
             if (p.has_c && t < nvalid) x = fmaf(p.beta, half_bits_to_float<ELEM>(cb[at(p.ldc, t)]), x);
-            o[t] = activate(x + bias[t], p.act);
+            x += bias[t];
+            if (p.pre && t < nvalid) {
+                const uint32_t pr = pack2<ELEM>(x, x);
+                static_cast<uint16_t*>(p.pre)[at(p.ldpre, t)] = static_cast<uint16_t>(pr);
+            }
+            o[t] = activate(x, p.act);
             if (p.aux_op && t < nvalid) {
                 const uint16_t z = static_cast<const uint16_t*>(p.aux)[at(p.ldaux, t)];
                 o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);

@@ -58,6 +58,8 @@ struct GemmParams {
     const void* aux;                  // auxiliary tensor Z (output type, row-major), or null
     int64_t ldaux;
     int32_t aux_op;                   // 0 none, 1 add, 2 sub, 3 mul, 4 div
+    void* pre;                        // pre-activation output Y (output type, layout of D),
+    int64_t ldpre;                    // or null
     int32_t out_trans;                // 1: the computed tile is the transpose of the stored
                                       // one (swap-AB): element (r, c) of the computed output
                                       // lives at C / D / Z + c * ld + r
@@ -108,6 +110,8 @@ struct ReduceParams {
     const void* aux;
     int64_t ldaux;
     int32_t aux_op;
+    void* pre;                        // as in GemmParams
+    int64_t ldpre;
     int32_t out_trans;                // as in GemmParams
     // balanced split-K: the partials come from a stream-K partition of
     // sk_units iterations over units units (0 = classic split-K layout)

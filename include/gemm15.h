@@ -169,13 +169,23 @@ typedef struct {
     const void* aux;      /* DEVICE M x N tensor Z of D's type and layout, or NULL */
     int64_t ldaux;        /* its leading dimension (0 = packed) */
     int32_t aux_op;       /* gemm15_aux_op_t; GEMM15_AUX_NONE ignores aux */
+    void* pre;            /* DEVICE M x N output Y of D's type and layout receiving the
+                             pre-activation alpha * s_a * s_b * (A . B) + beta * C + bias
+                             (rounded once to D's type), or NULL */
+    int64_t ldpre;        /* its leading dimension (0 = packed) */
 } gemm15_args_t;
 
 /* D = act(alpha * s_a * s_b * (A . B) + beta * C + bias) [op Z], bias[j]
  * added to every element of column j of D -- the LinearCombinationBiasReLU
  * epilogue of the kwkr.cn blog "CUTLASS Python接口", section 5.2 (bias vector of
  * length N in the output type, fp32 arithmetic, activation last) -- and an
- * optional auxiliary tensor Z entering the activated value by aux_op.
+ * optional auxiliary tensor Z entering the activated value by aux_op.  With
+ * `pre` set, the epilogue also stores the value before the activation to Y
+ * (the auxiliary tensor store of the EFC epilogue operations in the roadmap
+ * section of "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL
+ * backend"; what a backward pass through the activation needs).  Y follows
+ * the rules of Z: 16-byte aligned pointer and ldpre * 2 (ALIGNMENT otherwise),
+ * ldpre >= the contiguous extent (INVALID_ARG otherwise).
  * Everything else as gemm_run_ex; the bias and aux pointers and ldaux * 2 must
  * be 16-byte aligned (ALIGNMENT otherwise), ldaux >= the contiguous extent
  * (INVALID_ARG otherwise).  With K == 0, D = act(beta * C + bias) [op Z]. */

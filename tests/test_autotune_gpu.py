@@ -74,3 +74,19 @@ def test_autotune_argument_errors():
     st, _ = g.gemm_plan_autotune(plan.handle, A, B, None, D, 64, 128, 64,
                                  bias=torch.zeros(136, dtype=torch.float16, device="cuda")[4:])
     assert st == g.ERR_ALIGNMENT
+
+
+def test_autotune_includes_swap_ab_for_a_short_side():
+    """A decode-size problem (M = 32) adds the three swap-AB schedules to the
+    candidates; whichever wins, later runs of the shape reproduce it."""
+    prob = inputs.random_problem(32, 4096, 4096, dtype="bf16")
+    plan = plan_for(prob)
+    A, B, C, D = _dev(prob)
+    res = plan.autotune(A, B, C, D, prob.M, prob.N, prob.K, 1.0, 0.0, iterations=2)
+    assert len(res) == 19
+    assert sum(r["config"]["swap_ab"] for r in res) == 3
+    best = res[0]["config"]
+    torch.cuda.synchronize()
+    assert_matches_oracle(prob, inputs.bits(D.cpu()))
+    plan.run(A, B, C, D, prob.M, prob.N, prob.K)
+    assert all(plan.last_config()[k] == best[k] for k in KEYS + ("swap_ab",))

@@ -187,3 +187,39 @@ def test_aux_argument_errors():
     assert run(aux=Z, aux_op="add", ldaux=100) == g.ERR_INVALID_ARG   # < N
     assert run(aux=Z, aux_op="add", ldaux=132) == g.ERR_ALIGNMENT     # 264 bytes
     assert run(aux=Z, aux_op="add") == g.OK
+
+
+@pytest.mark.parametrize("act", ["sigmoid", "tanh"])
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+def test_pre_activation_output_matches_oracle(act, sched):
+    """Random operands: Y (pre-activation) against the oracle's linear
+    epilogue, D against the full one, with C, a bias and Z."""
+    import copy
+    prob = inputs.random_problem(392, 520, 1096, dtype="f16", alpha=0.75, beta=0.5, act=act,
+                                 bias=True, aux_op="add")
+    plan = _plan(prob, schedule=sched)
+    A, B, C, Z = prob.A.cuda(), prob.B.cuda(), prob.C.cuda(), prob.aux.cuda()
+    D = torch.full((prob.M, prob.N), float("nan"), dtype=torch.float16, device="cuda")
+    Y = torch.full_like(D, float("nan"))
+    st = g.gemm_run_args(plan.handle, A, B, C, D, prob.M, prob.N, prob.K, prob.alpha,
+                         prob.beta, bias=prob.bias.cuda(), aux=Z, aux_op="add", pre=Y)
+    assert st == g.OK
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    assert_matches_oracle(prob, inputs.bits(D.cpu()))
+    lin = copy.copy(prob)
+    lin.act, lin.relu, lin.aux, lin.aux_op = "linear", False, None, None
+    assert_matches_oracle(lin, inputs.bits(Y.cpu()))
+
+
+def test_pre_activation_argument_errors():
+    prob = inputs.random_problem(64, 128, 64)
+    plan = _plan(prob)
+    A, B = prob.A.cuda(), prob.B.cuda()
+    D = torch.empty(64, 128, dtype=torch.float16, device="cuda")
+    Y = torch.empty(64, 136, dtype=torch.float16, device="cuda")
+    run = lambda **kw: g.gemm_run_args(plan.handle, A, B, None, D, 64, 128, 64, 1.0, 0.0, **kw)
+    assert run(pre=Y, ldpre=100) == g.ERR_INVALID_ARG    # below N
+    assert run(pre=Y, ldpre=132) == g.ERR_ALIGNMENT      # 264 bytes
+    assert run(pre=Y.view(-1)[4:], ldpre=136) == g.ERR_ALIGNMENT
+    assert run(pre=Y, ldpre=136) == g.OK

@@ -24,9 +24,10 @@ from helpers import LAYOUT, assert_bit_exact, oracle_bits
 pytestmark = pytest.mark.gpu
 
 
-def _run_args(plan, prob, col_major_cd=False):
+def _run_args(plan, prob, col_major_cd=False, with_pre=False):
     """Runs `prob` (bias, Z and fp8 scales included) through gemm_run_args;
-    returns D as M x N row-major stored bits."""
+    returns D as M x N row-major stored bits (and the pre-activation output Y
+    the same way with `with_pre`)."""
     A, B = prob.A.cuda(), prob.B.cuda()
     C = prob.C.cuda() if prob.C is not None else None
     Z = prob.aux.cuda() if prob.aux_op else None
@@ -38,18 +39,29 @@ def _run_args(plan, prob, col_major_cd=False):
         D = torch.full((prob.N, prob.M), float("nan"), dtype=dt, device="cuda")
     else:
         D = torch.full((prob.M, prob.N), float("nan"), dtype=dt, device="cuda")
+    Y = torch.full_like(D, float("nan")) if with_pre else None
     sa = sb = None
     if prob.a_dtype == "e4m3":
         sa = torch.tensor([prob.scale_a], dtype=torch.float32, device="cuda")
         sb = torch.tensor([prob.scale_b], dtype=torch.float32, device="cuda")
     st = g.gemm_run_args(plan.handle, A, B, C, D, prob.M, prob.N, prob.K, prob.alpha,
                          prob.beta, scale_a=sa, scale_b=sb, bias=bias, aux=Z,
-                         aux_op=prob.aux_op)
+                         aux_op=prob.aux_op, pre=Y)
     assert st == g.OK, g.status_string(st)
     torch.cuda.synchronize()
     assert plan.query_error() == g.OK
-    Dh = D.cpu()
-    return inputs.bits(Dh.t().contiguous() if col_major_cd else Dh)
+    out = [D.cpu()] + ([Y.cpu()] if with_pre else [])
+    out = [inputs.bits(t.t().contiguous() if col_major_cd else t) for t in out]
+    return tuple(out) if with_pre else out[0]
+
+
+def _linear_part(prob):
+    """The same problem without activation and auxiliary operation: its D is
+    the pre-activation value alpha * s_a * s_b * A.B + beta * C + bias."""
+    import copy
+    lin = copy.copy(prob)
+    lin.act, lin.relu, lin.aux, lin.aux_op = "linear", False, None, None
+    return lin
 
 
 def _plan(prob, layout_cd=g.ROW_MAJOR, **opts):
@@ -243,6 +255,42 @@ def test_swap_ab_is_the_automatic_choice_for_decode_sizes(M):
     d = _run_args(plan, prob)
     assert plan.last_config()["swap_ab"] == 1
     assert_bit_exact(prob, d)
+
+
+# ------------------------------------------------------------------ pre-activation output
+
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("cg,tile_n", [(1, 256), (2, 256), (2, 128)])
+def test_pre_activation_output_bit_exact(sched, cg, tile_n):
+    """The auxiliary tensor store: Y = alpha*A.B + beta*C + bias (before the
+    ReLU and the auxiliary operation) next to D = relu(Y) * Z, both exact.
+    N = 392 ends inside a 64-column chunk (element-wise tail)."""
+    prob = inputs.integer_problem(520, 392, 4160, dtype="bf16", bias=True, aux_op="mul")
+    plan = _plan(prob, schedule=sched, cta_group=cg, tile_n=tile_n)
+    d, y = _run_args(plan, prob, with_pre=True)
+    assert_bit_exact(prob, d)
+    assert_bit_exact(_linear_part(prob), y)
+
+
+@pytest.mark.parametrize("swap,col_major_cd", [(2, False), (2, True), (1, True)])
+@pytest.mark.parametrize("sched", [g.SCHED_SK, g.SCHED_SPLIT])
+def test_pre_activation_output_transposed_bit_exact(swap, col_major_cd, sched):
+    """Y under swap-AB and column-major C/D (transposed stores), including the
+    split-K reduction kernel's store."""
+    prob = inputs.integer_problem(48, 1048, 2112, dtype="f16", bias=True, aux_op="add")
+    plan = _plan(prob, layout_cd=LAYOUT[col_major_cd], schedule=sched, swap_ab=swap)
+    d, y = _run_args(plan, prob, col_major_cd=col_major_cd, with_pre=True)
+    assert_bit_exact(prob, d)
+    assert_bit_exact(_linear_part(prob), y)
+
+
+def test_pre_activation_output_with_k_zero():
+    prob = inputs.integer_problem(70, 136, 0, dtype="bf16", bias=True, aux_op="sub")
+    prob.A = torch.empty(70, 0, dtype=torch.bfloat16)
+    prob.B = torch.empty(0, 136, dtype=torch.bfloat16)
+    d, y = _run_args(_plan(prob), prob, with_pre=True)
+    assert_bit_exact(prob, d)
+    assert_bit_exact(_linear_part(prob), y)
 
 
 # ------------------------------------------------------------------ grouped and batched
