@@ -6,8 +6,9 @@ of a Llama-3.3-70B layer in bf16 at 8192 tokens (X [8192, 8192] times
 W [8192, 57344], beta 0), the largest single-GPU shape of the Llama linear
 layers that are 89% of that model's runtime ("Generating State-of-the-Art
 GEMMs with TorchInductor's CuteDSL backend", section 2).  The metric is
-TFLOP/s = 2*M*N*K / time; the L2 is flushed (256 MiB write) between timed
-steps, outside the per-step CUDA events.
+TFLOP/s = 2*M*N*K / time; the L2 is flushed (256 MiB write, then a 256 MiB
+read that leaves it holding clean lines) between timed steps, outside the
+per-step CUDA events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -614,8 +615,11 @@ def main(argv=None):
     ap.add_argument("--autotune", action="store_true",
                     help="time every kernel configuration first and keep the fastest")
     ap.add_argument("--trace", help="after timing, save one step's per-CTA timeline (.npy)")
-    ap.add_argument("--flush", choices=["write", "write+read"], default="write",
-                    help="L2 flush between timed steps")
+    ap.add_argument("--flush", choices=["write", "write+read"], default="write+read",
+                    help="L2 flush between timed steps: a 256 MiB write, then (default) a "
+                         "256 MiB read so that the L2 holds clean lines: after the write "
+                         "alone the next kernel first pays for writing back ~L2-size dirty "
+                         "lines (~19 us at HBM speed), a cost of the flush, not of the GEMM")
     args = ap.parse_args(argv)
     if args.list:
         print("\n".join(workloads()))

@@ -494,10 +494,10 @@ cudaError_t launch_kernel(int elem, int bn, int cg, const GemmParams& gp, int gr
 }
 
 cudaError_t launch_reduce_kernel(int out_elem, const ReduceParams& rp, cudaStream_t s, int num_sms) {
-    const int64_t work = static_cast<int64_t>(rp.M) * cdiv(rp.N, REDUCE_COLS);
-    const int grid = static_cast<int>(
-        std::max<int64_t>(1, std::min<int64_t>(cdiv(work, REDUCE_THREADS), num_sms * 16)));
-    return out_elem == ELEM_F16 ? launch_reduce<ELEM_F16>(rp, grid, s) : launch_reduce<ELEM_BF16>(rp, grid, s);
+    int grid = 1, groups = 1;
+    reduce_shape(rp, num_sms, &grid, &groups);
+    return out_elem == ELEM_F16 ? launch_reduce<ELEM_F16>(rp, grid, groups, s)
+                                : launch_reduce<ELEM_BF16>(rp, grid, groups, s);
 }
 
 // Fills the operand-layout part of the kernel parameters.

@@ -274,10 +274,9 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
     rp.scale_b = scale_b;
     rp.act = act;
     rp.has_c = has_c;
-    const int64_t work = m * ((n + REDUCE_COLS - 1) / REDUCE_COLS);
-    const int rgrid = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>((work + REDUCE_THREADS - 1) / REDUCE_THREADS, ds->num_sms * 16)));
-    const cudaError_t e = out_elem == ELEM_F16 ? launch_reduce<ELEM_F16>(rp, rgrid, s)
-                                               : launch_reduce<ELEM_BF16>(rp, rgrid, s);
+    int rgrid = 1, groups = 1;
+    reduce_shape(rp, ds->num_sms, &rgrid, &groups);
+    const cudaError_t e = out_elem == ELEM_F16 ? launch_reduce<ELEM_F16>(rp, rgrid, groups, s)
+                                               : launch_reduce<ELEM_BF16>(rp, rgrid, groups, s);
     return e == cudaSuccess ? GEMM15_OK : GEMM15_ERR_CUDA;
 }

@@ -520,6 +520,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile uint32_t* tmem_slot = misc;
     volatile uint32_t* abort_flag = misc + 1;
 
+    // a programmatic dependent (the split-K reduction) may be scheduled now;
+    // it waits for this grid's completion before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     Ctl ctl{abort_flag, p.status, p.timeout_ns};
@@ -1216,123 +1219,128 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------------ split-K reduction
 
 // D = act(alpha * sum_s partial_s + beta * C + bias) [op Z] for split-K runs
-// (splits >= 1), or D = act(beta * C + bias) [op Z] when K == 0 (splits == 0).  Each thread
-// owns REDUCE_COLS consecutive columns of one row; partial tiles are summed in
-// split order, eight splits' loads in flight at a time.
+// (splits >= 1), or D = act(beta * C + bias) [op Z] when K == 0 (splits == 0);
+// the value before the activation also goes to Y when requested.  A block is
+// G warps (G = blockDim.x / 32, at most REDUCE_MAX_GROUPS) over 32 output
+// elements of REDUCE_COLS consecutive columns: warp g sums its fixed share of
+// the partials in order, then warp 0 adds the G group sums in order and runs
+// the epilogue, so the result does not depend on timing.  Launched as a
+// programmatic dependent of the GEMM kernel: it waits for that grid here.
 template <int ELEM>
-__global__ void __launch_bounds__(REDUCE_THREADS) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(32 * REDUCE_MAX_GROUPS) splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int V = REDUCE_COLS;
+    __shared__ float4 group_sum[REDUCE_MAX_GROUPS][32];
+    const int G = static_cast<int>(blockDim.x >> 5);
+    const int g = static_cast<int>(threadIdx.x >> 5);
+    const int lane = static_cast<int>(threadIdx.x & 31);
     const int64_t nv = (p.N + V - 1) / V;
     const int64_t total = static_cast<int64_t>(p.M) * nv;
+    const int64_t batches = (total + 31) / 32;
     float alpha = p.alpha;
     if (p.scale_a) alpha *= __ldg(p.scale_a);
     if (p.scale_b) alpha *= __ldg(p.scale_b);
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int32_t m = static_cast<int32_t>(idx / nv);
-        const int32_t n = static_cast<int32_t>(idx - static_cast<int64_t>(m) * nv) * V;
-        float acc[V];
-#pragma unroll
-        for (int t = 0; t < V; ++t) acc[t] = 0.0f;
-        if (p.units > 0) {
-            // balanced split-K: tile t's pieces are held by units h0..h1 of the
-            // stream-K partition; h0's piece (the tile's head) sits in slot
-            // 2*h0 + 1, the others' in slot 2*v; summed in unit order
+    const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;
+    for (int64_t bt = blockIdx.x; bt < batches; bt += gridDim.x) {  // uniform per block
+        const int64_t idx = bt * 32 + lane;
+        const bool live = idx < total;
+        const int32_t m = live ? static_cast<int32_t>(idx / nv) : 0;
+        const int32_t n = live ? static_cast<int32_t>(idx - static_cast<int64_t>(m) * nv) * V : 0;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (live && (p.units > 0 || p.splits > 0)) {
             const int32_t mb = m / TILE_M, r = m - mb * TILE_M;
             const int32_t nb = n / p.tile_n, cc = n - nb * p.tile_n;
-            const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;
-            const int64_t t0 = static_cast<int64_t>(raster_tile(mb, nb, p.m_blocks, p.n_blocks, p.raster)) * p.k_blocks;
-            auto begin = [&](int64_t u) { return (p.sk_units * u) / p.units; };
-            auto unit_of = [&](int64_t x) {
-                int64_t u = (x * p.units) / p.sk_units;
-                while (u > 0 && begin(u) > x) --u;
-                while (u + 1 < p.units && begin(u + 1) <= x) ++u;
-                return u;
-            };
-            const int64_t h0 = unit_of(t0), h1 = unit_of(t0 + p.k_blocks - 1);
             const float* base = p.ws + static_cast<size_t>(r) * p.tile_n + cc;
-            const float4 a0 = __ldcg(reinterpret_cast<const float4*>(base + (2 * h0 + 1) * tile_elems));
-            acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
+            // the partials of this element in their fixed order: split order, or
+            // for balanced split-K the unit order of the tile's holders h0..h1
+            // (h0's piece, the tile's head, sits in slot 2*h0 + 1, the others' in 2*v)
+            int64_t P, h0 = 0;
+            if (p.units > 0) {
+                const int64_t t0 = static_cast<int64_t>(raster_tile(mb, nb, p.m_blocks, p.n_blocks, p.raster)) * p.k_blocks;
+                auto begin = [&](int64_t u) { return (p.sk_units * u) / p.units; };
+                auto unit_of = [&](int64_t x) {
+                    int64_t u = (x * p.units) / p.sk_units;
+                    while (u > 0 && begin(u) > x) --u;
+                    while (u + 1 < p.units && begin(u + 1) <= x) ++u;
+                    return u;
+                };
+                h0 = unit_of(t0);
+                P = unit_of(t0 + p.k_blocks - 1) - h0 + 1;
+            } else {
+                base += static_cast<size_t>(mb * p.n_blocks + nb) * p.splits * tile_elems;
+                P = p.splits;
+            }
+            auto partial = [&](int64_t j) -> const float4* {
+                const int64_t slot = p.units > 0 ? (j == 0 ? 2 * h0 + 1 : 2 * (h0 + j)) : j;
+                return reinterpret_cast<const float4*>(base + slot * tile_elems);
+            };
+            const int64_t j0 = P * g / G, j1 = P * (g + 1) / G;
             constexpr int U = 8;
-            int64_t v = h0 + 1;
-            for (; v + U - 1 <= h1; v += U) {
+            int64_t j = j0;
+            for (; j + U <= j1; j += U) {
                 float4 a[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    a[u] = __ldcg(reinterpret_cast<const float4*>(base + 2 * (v + u) * tile_elems));
+                for (int u = 0; u < U; ++u) a[u] = __ldcg(partial(j + u));
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    acc[0] += a[u].x; acc[1] += a[u].y; acc[2] += a[u].z; acc[3] += a[u].w;
+                    acc.x += a[u].x; acc.y += a[u].y; acc.z += a[u].z; acc.w += a[u].w;
                 }
             }
-            for (; v <= h1; ++v) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(base + 2 * v * tile_elems));
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            }
-        } else if (p.splits > 0) {
-            const int32_t mb = m / TILE_M, r = m - mb * TILE_M;
-            const int32_t nb = n / p.tile_n, cc = n - nb * p.tile_n;
-            const size_t tile_elems = static_cast<size_t>(TILE_M) * p.tile_n;
-            const float* src = p.ws + static_cast<size_t>(mb * p.n_blocks + nb) * p.splits * tile_elems +
-                               static_cast<size_t>(r) * p.tile_n + cc;
-            constexpr int U = 8;
-            int32_t s = 0;
-            for (; s + U <= p.splits; s += U) {
-                float4 a[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) a[u] = __ldcg(reinterpret_cast<const float4*>(src + u * tile_elems));
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    acc[0] += a[u].x; acc[1] += a[u].y; acc[2] += a[u].z; acc[3] += a[u].w;
-                }
-                src += U * tile_elems;
-            }
-            for (; s < p.splits; ++s) {
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                src += tile_elems;
+            for (; j < j1; ++j) {
+                const float4 a = __ldcg(partial(j));
+                acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
             }
         }
-        const int nvalid = min(V, p.N - n);
-        float bias[V];
+        if (g > 0) group_sum[g][lane] = acc;
+        __syncthreads();
+        if (g == 0 && live) {
+            for (int gg = 1; gg < G; ++gg) {
+                const float4 a = group_sum[gg][lane];
+                acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+            }
+            const float av[V] = {acc.x, acc.y, acc.z, acc.w};
+            const int nvalid = min(V, p.N - n);
+            float bias[V];
 #pragma unroll
-        for (int t = 0; t < V; ++t) bias[t] = 0.0f;
-        if (p.bias) {
-            const uint16_t* bv = static_cast<const uint16_t*>(p.bias);
+            for (int t = 0; t < V; ++t) bias[t] = 0.0f;
+            if (p.bias) {
+                const uint16_t* bv = static_cast<const uint16_t*>(p.bias);
+#pragma unroll
+                for (int t = 0; t < V; ++t) {
+                    if (p.bias_rows) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + m));
+                    else if (t < nvalid) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + n + t));
+                }
+            }
+            // element (m, n + t) of the computed output: row-major, or transposed (swap-AB)
+            auto at = [&](int64_t ld, int t) -> int64_t {
+                return p.out_trans ? static_cast<int64_t>(n + t) * ld + m : static_cast<int64_t>(m) * ld + n + t;
+            };
+            const uint16_t* cb = static_cast<const uint16_t*>(p.C);
+            uint16_t* db = static_cast<uint16_t*>(p.D);
+            float o[V];
 #pragma unroll
             for (int t = 0; t < V; ++t) {
-                if (p.bias_rows) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + m));
-                else if (t < nvalid) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + n + t));
+                float x = alpha * av[t];
+                if (p.has_c && t < nvalid) x = fmaf(p.beta, half_bits_to_float<ELEM>(cb[at(p.ldc, t)]), x);
+                x += bias[t];
+                if (p.pre && t < nvalid) {
+                    const uint32_t pr = pack2<ELEM>(x, x);
+                    static_cast<uint16_t*>(p.pre)[at(p.ldpre, t)] = static_cast<uint16_t>(pr);
+                }
+                o[t] = activate(x, p.act);
+                if (p.aux_op && t < nvalid) {
+                    const uint16_t z = static_cast<const uint16_t*>(p.aux)[at(p.ldaux, t)];
+                    o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);
+                }
+            }
+            const uint32_t pk[2] = {pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3])};
+            if (nvalid == V && !p.out_trans) {
+                *reinterpret_cast<uint2*>(db + at(p.ldd, 0)) = make_uint2(pk[0], pk[1]);
+            } else {
+                for (int t = 0; t < nvalid; ++t) db[at(p.ldd, t)] = static_cast<uint16_t>(pk[t >> 1] >> (16 * (t & 1)));
             }
         }
-        // element (m, n + t) of the computed output: row-major, or transposed (swap-AB)
-        auto at = [&](int64_t ld, int t) -> int64_t {
-            return p.out_trans ? static_cast<int64_t>(n + t) * ld + m : static_cast<int64_t>(m) * ld + n + t;
-        };
-        const uint16_t* cb = static_cast<const uint16_t*>(p.C);
-        uint16_t* db = static_cast<uint16_t*>(p.D);
-        float o[V];
-#pragma unroll
-        for (int t = 0; t < V; ++t) {
-            float x = alpha * acc[t];
-            if (p.has_c && t < nvalid) x = fmaf(p.beta, half_bits_to_float<ELEM>(cb[at(p.ldc, t)]), x);
-            x += bias[t];
-            if (p.pre && t < nvalid) {
-                const uint32_t pr = pack2<ELEM>(x, x);
-                static_cast<uint16_t*>(p.pre)[at(p.ldpre, t)] = static_cast<uint16_t>(pr);
-            }
-            o[t] = activate(x, p.act);
-            if (p.aux_op && t < nvalid) {
-                const uint16_t z = static_cast<const uint16_t*>(p.aux)[at(p.ldaux, t)];
-                o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);
-            }
-        }
-        const uint32_t pk[2] = {pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3])};
-        if (nvalid == V && !p.out_trans) {
-            *reinterpret_cast<uint2*>(db + at(p.ldd, 0)) = make_uint2(pk[0], pk[1]);
-        } else {
-            for (int t = 0; t < nvalid; ++t) db[at(p.ldd, t)] = static_cast<uint16_t>(pk[t >> 1] >> (16 * (t & 1)));
-        }
+        __syncthreads();  // group_sum is reused by the next batch
     }
 }
 

@@ -17,8 +17,8 @@ constexpr int EPI_WARPS = 4;        // epilogue warps (one per 32-lane TMEM quar
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, then epilogue
 constexpr int EPI_COLS = 64;        // output columns per epilogue chunk (128 B of 16-bit)
 constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32-row x 128-byte epilogue staging box
-constexpr int REDUCE_COLS = 4;      // split-K reduction: output columns per thread
-constexpr int REDUCE_THREADS = 128; // split-K reduction: threads per block
+constexpr int REDUCE_COLS = 4;      // split-K reduction: output columns per element
+constexpr int REDUCE_MAX_GROUPS = 8; // split-K reduction: warps (split groups) per block
 
 // One group of a grouped GEMM as the kernel reads it from device memory.
 struct alignas(128) GroupEntry {

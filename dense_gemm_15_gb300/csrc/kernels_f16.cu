@@ -8,5 +8,5 @@ template cudaError_t launch_gemm<ELEM_F16, 256>(const GemmParams&, int, cudaStre
 template cudaError_t launch_gemm<ELEM_F16, 256, 2>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_F16, 128, 2>(const GemmParams&, int, cudaStream_t);
 template int max_pair_clusters<ELEM_F16>();
-template cudaError_t launch_reduce<ELEM_F16>(const ReduceParams&, int, cudaStream_t);
+template cudaError_t launch_reduce<ELEM_F16>(const ReduceParams&, int, int, cudaStream_t);
 }  // namespace g15

@@ -17,9 +17,13 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 // (0 if the query fails).
 int gemm_max_pair_clusters(int elem);
 
-// Split-K reduction / K == 0 epilogue (ELEM selects the 16-bit C/D type).
+// Split-K reduction / K == 0 epilogue (ELEM selects the 16-bit C/D type):
+// `grid` blocks of `groups` warps (1..REDUCE_MAX_GROUPS).
 template <int ELEM>
-cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_reduce(const ReduceParams& p, int grid, int groups, cudaStream_t stream);
+
+// Grid and warps per block of the reduction for its parameters.
+void reduce_shape(const ReduceParams& p, int num_sms, int* grid, int* groups);
 
 // Shared-memory bytes and pipeline depth of a GEMM instantiation.
 int gemm_smem_bytes(int elem, int bn, int cg);

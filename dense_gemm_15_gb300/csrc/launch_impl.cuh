@@ -68,9 +68,20 @@ int max_pair_clusters() {
 }
 
 template <int ELEM>
-cudaError_t launch_reduce(const ReduceParams& p, int grid, cudaStream_t stream) {
-    splitk_reduce_kernel<ELEM><<<grid, REDUCE_THREADS, 0, stream>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_reduce(const ReduceParams& p, int grid, int groups, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * groups), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    // programmatic dependent launch: scheduled while the GEMM kernel before it
+    // runs, the kernel itself waits for that grid (griddepcontrol.wait)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<ELEM>, p);
 }
 
 }  // namespace g15
