@@ -39,6 +39,7 @@ struct Options {
     int sk_dp_waves = -1;
     int trace_items = 0;
     int swap_ab = 0;  // 0 automatic, 1 never, 2 always (dense problems)
+    int splitk_inline = 0;  // split-K reduced by the last split: 0 automatic, 1 never, 2 always
 };
 
 // Kernel choice fixed by gemm_plan_autotune for one problem shape.
@@ -295,6 +296,7 @@ struct Decision {
     int32_t dp_tiles = 0, splits = 1, raster = 1;
     int64_t sk_units = 0;
     bool balanced = false;  // split-K over a stream-K partition of all units
+    bool inline_split = false;  // split-K reduced inside the GEMM kernel (last split)
     size_t ws_bytes = 0;
     int flags = 0;
 };
@@ -443,6 +445,11 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const Option
         d.splits = splits;
         units = static_cast<int>(std::min<int64_t>(G, static_cast<int64_t>(d.tiles) * splits));
         d.ws_bytes = static_cast<size_t>(d.tiles) * cg * splits * half_tile;
+        // the last split of a tile adds the partials itself when they are few
+        // (one CTA reads them all: at most 256 KiB); else a reduction kernel
+        d.inline_split = o.splitk_inline == 2 ||
+                         (o.splitk_inline == 0 && static_cast<size_t>(splits) * half_tile <= (256u << 10));
+        if (d.inline_split) d.flags = 2 * d.tiles * cg;  // one 64-bit arrival counter per tile half
     }
     d.grid = units * cg;
     return d;
@@ -631,7 +638,8 @@ bool same_prob(const Prob& a, const Prob& b) {
 bool same_choice_options(const Options& a, const Options& b) {
     return a.schedule == b.schedule && a.splits == b.splits && a.cta_group == b.cta_group &&
            a.tile_n == b.tile_n && a.raster == b.raster && a.grid == b.grid &&
-           a.sk_dp_waves == b.sk_dp_waves && a.swap_ab == b.swap_ab;
+           a.sk_dp_waves == b.sk_dp_waves && a.swap_ab == b.swap_ab &&
+           a.splitk_inline == b.splitk_inline;
 }
 
 // Finds or builds the launch parameters of problem p (nullptr on an encoding
@@ -674,15 +682,18 @@ const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& key, bool has_c) 
     gp.sk_partials_only = d.balanced ? 1 : 0;
     gp.dp_tiles = d.dp_tiles;
     gp.splits = d.splits;
-    gp.has_c = has_c && d.sched != SCHED_SPLIT;
+    // split-K with a reduction kernel: that kernel reads C and applies the epilogue
+    const bool epi_here = d.sched != SCHED_SPLIT || d.inline_split;
+    gp.splitk_inline = d.inline_split ? 1 : 0;
+    gp.has_c = has_c && epi_here;
     gp.sk_units = d.sk_units;
     gp.act = static_cast<int>(plan->desc.epilogue);
-    gp.bias = d.sched == SCHED_SPLIT ? nullptr : p.bias;  // split-K: the reduction adds it
+    gp.bias = epi_here ? p.bias : nullptr;
     gp.bias_rows = p.bias_rows;
     gp.aux = p.aux;
     gp.ldaux = p.ldaux;
-    gp.aux_op = d.sched == SCHED_SPLIT ? 0 : p.aux_op;
-    gp.pre = d.sched == SCHED_SPLIT ? nullptr : p.pre;  // split-K: the reduction stores it
+    gp.aux_op = epi_here ? p.aux_op : 0;
+    gp.pre = epi_here ? p.pre : nullptr;
     gp.ldpre = p.ldpre;
     fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.groups = nullptr;
@@ -763,7 +774,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     if (st != GEMM15_OK) return st;
     if (launch_kernel(plan->elem, d.bn, d.cg, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
     int launches = 1;
-    if (d.sched == SCHED_SPLIT) {
+    if (d.sched == SCHED_SPLIT && !d.inline_split) {
         ReduceParams rp{};
         rp.ws = plan->d_ws;
         rp.splits = d.splits;
@@ -1435,6 +1446,10 @@ gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option,
         case GEMM15_OPT_SWAP_AB:
             if (v < 0 || v > 2) return GEMM15_ERR_INVALID_ARG;
             o.swap_ab = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_SPLITK_INLINE:
+            if (v < 0 || v > 2) return GEMM15_ERR_INVALID_ARG;
+            o.splitk_inline = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_FAULT_SKIP_FLAG:
             if (v < -1 || v > 100000) return GEMM15_ERR_INVALID_ARG;

@@ -482,6 +482,25 @@ __device__ __forceinline__ bool sched_sk_last(const SchedState& s) {
     return s.phase == 1 && (s.step == 2 || s.o_begin >= s.u_end) && s.u >= s.o_begin;
 }
 
+// ------------------------------------------------------------------ split-K arrivals
+
+// Counts one arrival at a split tile's counter for launch `epoch` and returns
+// the arrival number (1 = first).  The counter holds the launch epoch in its
+// high word and the count in its low word, so values left by an earlier launch
+// (one that stopped early) read as zero.  0 if the update never succeeded.
+__device__ __forceinline__ uint32_t count_arrival(unsigned long long* ctr, uint32_t epoch) {
+    unsigned long long old = atomicAdd(ctr, 0ull);
+#pragma unroll 1
+    for (int it = 0; it < (1 << 20); ++it) {
+        const uint32_t cnt = static_cast<uint32_t>(old >> 32) == epoch ? static_cast<uint32_t>(old) : 0u;
+        const unsigned long long nw = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+        const unsigned long long prev = atomicCAS(ctr, old, nw);
+        if (prev == old) return cnt + 1u;
+        old = prev;
+    }
+    return 0u;
+}
+
 // ------------------------------------------------------------------ tracing
 
 __device__ __forceinline__ uint64_t* trace_rec(const GemmParams& p, int32_t item) {
@@ -808,31 +827,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int nch = min(NCH, (N - n0 + EPI_COLS - 1) / EPI_COLS);
             // bias of this thread's row (bias indexed by output row)
             float bias_row = 0.0f;
-            if (has_bias && p.bias_rows && !to_ws && row0 + lane < M)
+            if (has_bias && p.bias_rows && row0 + lane < M)
                 bias_row = half_bits_to_float<ELEM>(__ldg(static_cast<const uint16_t*>(p.bias) + row0 + lane));
 
             // C is fetched while the mainloop still runs: the whole tile when
             // every chunk has its own box, else the first chunk, with the rest
             // prefetched into L2
-            if (WHOLE && !to_ws && lane == 0) {
-                bulk_wait_read<0>();  // the previous tile's stores have read their boxes
-                if (stage_c) {
-                    for (int c = 0; c < nch; ++c) {
-                        mbar_arrive_expect_tx(c_bar(e, c), EPI_BUF_BYTES);
-                        tma_load_2d_hint(ebuf0 + c * EPI_BUF_BYTES, tC, c_bar(e, c), n0 + c * EPI_COLS, row0, pol_once);
-                        c_pending |= 1u << c;
+            auto issue_c = [&](bool to_ws_, bool stage_c_) {
+                if (WHOLE && !to_ws_ && lane == 0) {
+                    bulk_wait_read<0>();  // the previous tile's stores have read their boxes
+                    if (stage_c_) {
+                        for (int c = 0; c < nch; ++c) {
+                            mbar_arrive_expect_tx(c_bar(e, c), EPI_BUF_BYTES);
+                            tma_load_2d_hint(ebuf0 + c * EPI_BUF_BYTES, tC, c_bar(e, c), n0 + c * EPI_COLS, row0, pol_once);
+                            c_pending |= 1u << c;
+                        }
                     }
+                } else if (!WHOLE && stage_c_ && lane == 0) {
+                    // the latest store read the other box; the one before it read this one
+                    const uint32_t b = n_chunk & 1u;
+                    bulk_wait_read<1>();
+                    mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
+                    tma_load_2d_hint(ebuf0 + b * EPI_BUF_BYTES, tC, c_bar(e, b), n0, row0, pol_once);
+                    c_pending |= 1u << b;
+                    for (int c = 1; c < nch; ++c) tma_prefetch_l2_2d(tC, n0 + c * EPI_COLS, row0);
                 }
-            } else if (!WHOLE && stage_c && lane == 0) {
-                // the latest store read the other box; the one before it read this one
-                const uint32_t b = n_chunk & 1u;
-                bulk_wait_read<1>();
-                mbar_arrive_expect_tx(c_bar(e, b), EPI_BUF_BYTES);
-                tma_load_2d_hint(ebuf0 + b * EPI_BUF_BYTES, tC, c_bar(e, b), n0, row0, pol_once);
-                c_pending |= 1u << b;
-                for (int c = 1; c < nch; ++c) tma_prefetch_l2_2d(tC, n0 + c * EPI_COLS, row0);
-            }
-            __syncwarp();  // lane 0's wait for the stores orders the warp's writes to the boxes
+                __syncwarp();  // lane 0's wait for the stores orders the warp's writes to the boxes
+            };
+            issue_c(to_ws, stage_c);
 
             // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
@@ -911,6 +933,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
 
             if (tr) tr[5] = globaltimer_ns();
+            // the output chunks of this item: values from TMEM (plus stream-K
+            // peers), or with from_ws the sum of the tile's split partials
+            auto run_chunks = [&](bool from_ws, bool to_ws, bool stage_c) {
 #pragma unroll 1
             for (int c = 0; ok && rows_live && c < nch; ++c) {
                 const int32_t col0 = c * EPI_COLS;
@@ -938,12 +963,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) bulk_wait_read<1>();
                     __syncwarp();
                 }
+                float v[64];
+                if (from_ws) {
+                    // the tile's split partials in split order (this CTA's own included)
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = 0.0f;
+                    const int32_t slot0 = (w.slot / p.splits) * p.splits;
+                    for (int32_t sp = 0; sp < p.splits; ++sp) {
+                        const float4* src = reinterpret_cast<const float4*>(
+                                                p.ws + static_cast<size_t>(slot0 + sp) * TILE_M * BN) + peer_off(col0);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
+                            v[4 * i + 0] += t.x;
+                            v[4 * i + 1] += t.y;
+                            v[4 * i + 2] += t.z;
+                            v[4 * i + 3] += t.w;
+                        }
+                    }
+                } else {
                 uint32_t r[2][32];
                 const uint32_t taddr = tmem_base + lane_base + ab * BN + col0;
                 tmem_ld32(taddr, r[0]);
                 tmem_ld32(taddr + 32, r[1]);
                 tmem_ld_wait();
-                float v[64];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     v[i] = __uint_as_float(r[0][i]);
@@ -974,10 +1017,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
+                }  // from TMEM
                 if (to_ws) {
                     float4* dst = reinterpret_cast<float4*>(p.ws + static_cast<size_t>(w.slot) * TILE_M * BN);
-                    if (w.kind == WK_PEER) {
-                        // read back only by the owner's epilogue, in the same layout
+                    if (w.kind == WK_PEER || p.splitk_inline) {
+                        // read back by the owner's (or the last split's) epilogue, in the same layout
                         dst += peer_off(col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -1162,6 +1206,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 __syncwarp();
             }
+            };
+            run_chunks(false, to_ws, stage_c);
             // accumulator fully read: hand the TMEM buffer back to the MMA warp
             // (the leader's barrier counts the epilogue warps of both CTAs)
             tc_fence_before();
@@ -1183,6 +1229,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (tr) tr[7] = globaltimer_ns();
                 }
                 if (!synced) ok = false;
+            }
+            if (w.kind == WK_SPLIT && p.splitk_inline && ok) {
+                // this split's partial is written: count the tile's arrivals; the
+                // split that arrives last adds every partial in split order and
+                // writes the tile (no CTA waits for another)
+                __threadfence();
+                volatile uint32_t* last_flag = misc + 3;
+                if (!epi_sync()) ok = false;
+                if (ok && threadIdx.x == 64) {
+                    unsigned long long* ctr =
+                        reinterpret_cast<unsigned long long*>(p.flags) + (static_cast<int64_t>(w.tile) * CG + un.rank);
+                    const uint32_t n = count_arrival(ctr, p.epoch);
+                    if (n == 0u) raise_error(ctl.abort, ctl.status, DEV_ERR_TIMEOUT);
+                    *last_flag = (n == static_cast<uint32_t>(p.splits)) ? 1u : 0u;
+                }
+                if (ok && !epi_sync()) ok = false;
+                if (ok && *last_flag && !*abort_flag) {
+                    __threadfence();
+                    const bool sc = has_c && rows_live && !p.out_trans;
+                    issue_c(false, sc);
+                    run_chunks(true, false, sc);
+                }
             }
             if (*abort_flag) ok = false;
         }

@@ -49,6 +49,9 @@ struct GemmParams {
     int64_t sk_units;                 // SK: (tiles - dp_tiles) * k_blocks
     int32_t sk_partials_only;         // SK partition whose every piece leaves a partial tile
                                       // for the reduction kernel (balanced split-K)
+    int32_t splitk_inline;            // SPLIT: the split that finishes a tile last adds the
+                                      // partials and writes it (no reduction kernel); the
+                                      // arrival counters are 64-bit words in `flags`
     float alpha, beta;
     const float* scale_a;             // fp8 per-tensor scales (device), or null
     const float* scale_b;

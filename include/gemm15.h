@@ -268,13 +268,19 @@ typedef enum {
     GEMM15_OPT_TRACE_ITEMS = 9,    /* record a per-CTA timeline of up to this many
                                       work items per launch (0 = off); read it
                                       with gemm_plan_trace */
-    GEMM15_OPT_SWAP_AB = 10        /* dense runs: 0 auto (swap-AB when the computed
+    GEMM15_OPT_SWAP_AB = 10,       /* dense runs: 0 auto (swap-AB when the computed
                                       M <= 128 against N >= 1024 and K >= 256),
                                       1 never, 2 always.  Swap-AB computes
                                       D^T = B^T . A^T on 128 x 64 (16-bit, M <= 64)
                                       or 128 x 128 single-SM tiles and stores the
                                       tile transposed; GEMM15_OPT_TILE_N and
                                       GEMM15_OPT_CTA_GROUP do not apply to it */
+    GEMM15_OPT_SPLITK_INLINE = 11  /* split-K: 0 auto (when a tile's partials total at
+                                      most 256 KiB), 1 never, 2 always: the split that
+                                      finishes a tile last (a per-tile arrival
+                                      counter) adds all partials in split order and
+                                      writes the tile, instead of a separate
+                                      reduction kernel; no CTA waits for another */
 } gemm15_option_t;
 
 /* Sets an option on the plan; INVALID_ARG for unknown options or values. */

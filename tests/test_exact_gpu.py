@@ -121,6 +121,32 @@ def test_split_k_split_counts_bit_exact(splits):
     assert_bit_exact(prob, d)
 
 
+@pytest.mark.parametrize("inline", [1, 2])
+@pytest.mark.parametrize("cg,tile_n,swap", [(1, 128, 1), (1, 256, 1), (2, 256, 1), (2, 128, 1),
+                                            (1, 0, 2)])
+def test_split_k_in_kernel_and_kernel_reduction_bit_exact(inline, cg, tile_n, swap):
+    """Split-K reduced by the split that finishes a tile last (inline = 2, one
+    launch) or by the reduction kernel (inline = 1, two launches), with C, a
+    bias, Z and the pre-activation output."""
+    prob = inputs.integer_problem(520, 392, 4160, dtype="bf16", bias=True, aux_op="mul")
+    plan = _plan(prob, schedule=g.SCHED_SPLIT, splits=3, cta_group=cg, tile_n=tile_n,
+                 swap_ab=swap, splitk_inline=inline)
+    d, y = _run_args(plan, prob, with_pre=True)
+    cfg = plan.last_config()
+    assert cfg["splits"] == 3 and cfg["launches"] == (1 if inline == 2 else 2)
+    assert_bit_exact(prob, d)
+    assert_bit_exact(_linear_part(prob), y)
+
+
+def test_split_k_in_kernel_reduction_is_deterministic():
+    prob = inputs.random_problem(264, 1032, 8192, dtype="f16", beta=0.5, relu=True)
+    plan = _plan(prob, schedule=g.SCHED_SPLIT, splits=4, splitk_inline=2, tile_n=128)
+    d1 = _run_args(plan, prob)
+    d2 = _run_args(plan, prob)
+    assert plan.last_config()["launches"] == 1
+    assert np.array_equal(d1, d2)
+
+
 # ------------------------------------------------------------------ stream-K partitions
 
 @pytest.mark.parametrize("cg,grid", [(1, 4), (2, 8)])
