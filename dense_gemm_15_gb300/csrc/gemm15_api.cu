@@ -446,9 +446,14 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const Option
         units = static_cast<int>(std::min<int64_t>(G, static_cast<int64_t>(d.tiles) * splits));
         d.ws_bytes = static_cast<size_t>(d.tiles) * cg * splits * half_tile;
         // the last split of a tile adds the partials itself when they are few
-        // (one CTA reads them all: at most 256 KiB); else a reduction kernel
+        // (one CTA reads them all: at most 256 KiB) and the tile is stored
+        // as computed; else a reduction kernel (measured on GB300: 1536^2 x
+        // 16384 on SM-pair tiles 91 -> 75 us in-kernel, while swap-AB decode
+        // shapes, whose transposed stores make the last split's pass long,
+        // were 4 us faster with the kernel)
         d.inline_split = o.splitk_inline == 2 ||
-                         (o.splitk_inline == 0 && static_cast<size_t>(splits) * half_tile <= (256u << 10));
+                         (o.splitk_inline == 0 && !swap &&
+                          static_cast<size_t>(splits) * half_tile <= (256u << 10));
         if (d.inline_split) d.flags = 2 * d.tiles * cg;  // one 64-bit arrival counter per tile half
     }
     d.grid = units * cg;
