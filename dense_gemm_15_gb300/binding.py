@@ -15,7 +15,8 @@ import threading
 from . import build as _build
 
 # enums mirrored from include/gemm15.h
-F16, BF16, F32, E4M3 = 0, 1, 2, 3
+F16, BF16, F32, E4M3, E5M2, E2M1 = 0, 1, 2, 3, 4, 5
+SCALE_MX, SCALE_NV = 1, 2
 ROW_MAJOR, COL_MAJOR = 0, 1
 EPI_LINEAR, EPI_RELU, EPI_SIGMOID, EPI_TANH = 0, 1, 2, 3
 EPILOGUES = {"linear": EPI_LINEAR, "relu": EPI_RELU, "sigmoid": EPI_SIGMOID, "tanh": EPI_TANH}
@@ -27,14 +28,14 @@ OPT_SCHEDULE, OPT_SPLITS, OPT_CTA_GROUP, OPT_TILE_N, OPT_RASTER, OPT_GRID, \
     OPT_SPLITK_INLINE = range(12)
 SCHED_AUTO, SCHED_DP, SCHED_SK, SCHED_SPLIT = range(4)
 
-DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3}
+DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1}
 
 EXPORTED = (
     "gemm_plan_create", "gemm_plan_destroy", "gemm_run", "gemm_run_ex", "gemm_run_host",
     "grouped_gemm_run", "gemm_plan_query_error", "gemm15_status_string",
     "gemm_plan_set_option", "gemm_plan_last_config", "gemm_run_splitk_noalloc",
     "gemm_plan_trace", "gemm_run_batched", "gemm_run_args", "gemm_plan_autotune",
-    "gemm_plan_forget_tuning",
+    "gemm_plan_forget_tuning", "gemm_run_block_scaled",
 )
 
 
@@ -54,6 +55,15 @@ class Args(ctypes.Structure):
                 ("scale_b", ctypes.c_void_p), ("bias", ctypes.c_void_p),
                 ("aux", ctypes.c_void_p), ("ldaux", ctypes.c_int64), ("aux_op", ctypes.c_int32),
                 ("pre", ctypes.c_void_p), ("ldpre", ctypes.c_int64)]
+
+
+class ScaledArgs(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("B", ctypes.c_void_p),
+                ("ldb", ctypes.c_int64), ("SFA", ctypes.c_void_p), ("SFB", ctypes.c_void_p),
+                ("scale_kind", ctypes.c_int32), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("alpha", ctypes.c_float),
+                ("beta", ctypes.c_float), ("bias", ctypes.c_void_p)]
 
 
 class Problem(ctypes.Structure):
@@ -119,6 +129,7 @@ def load(build_if_missing: bool = True):
                                            ctypes.POINTER(TuneResult), i32,
                                            ctypes.POINTER(i32), vp]
         lib.gemm_plan_forget_tuning.argtypes = [vp]
+        lib.gemm_run_block_scaled.argtypes = [vp, ctypes.POINTER(ScaledArgs), vp]
         lib.gemm_run_batched.argtypes = [vp, vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
                                          i64, i64, i64, i64, i32, f32, f32, vp]
         lib.gemm_plan_query_error.argtypes = [vp]
@@ -243,6 +254,16 @@ def gemm_plan_autotune(plan, A, B, C, D, M, N, K, alpha=1.0, beta=0.0, lda=0, ld
     st = load().gemm_plan_autotune(plan, ctypes.byref(args), int(iterations), out, cap,
                                    ctypes.byref(n), _stream(stream))
     return st, [out[i].as_dict() for i in range(min(n.value, cap))]
+
+
+def gemm_run_block_scaled(plan, A, B, SFA, SFB, D, M, N, K, scale_kind=SCALE_MX, C=None,
+                          alpha=1.0, beta=0.0, lda=0, ldb=0, ldc=0, ldd=0, bias=None,
+                          stream=None):
+    """Block-scaled GEMM (A row-major, B column-major, scale factors in the
+    128 x 4 blocked layout; see include/gemm15.h)."""
+    args = ScaledArgs(_ptr(A), lda, _ptr(B), ldb, _ptr(SFA), _ptr(SFB), int(scale_kind), _ptr(C),
+                      ldc, _ptr(D), ldd, M, N, K, alpha, beta, _ptr(bias))
+    return load().gemm_run_block_scaled(plan, ctypes.byref(args), _stream(stream))
 
 
 def gemm_plan_forget_tuning(plan):

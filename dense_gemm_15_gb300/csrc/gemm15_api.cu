@@ -714,8 +714,14 @@ const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& key, bool has_c) 
     return &e;
 }
 
+// Element types whose plans run only the block-scaled entry point.
+bool block_scaled_only(const gemm15_plan* plan) {
+    return plan->elem == ELEM_E5M2 || plan->elem == ELEM_E2M1;
+}
+
 gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float beta,
                           const float* scale_a, const float* scale_b, cudaStream_t s) {
+    if (block_scaled_only(plan)) return GEMM15_ERR_UNSUPPORTED;
     gemm15_status_t st = check_operands(plan, p, beta);
     if (st != GEMM15_OK) return st;
     if (p.M == 0 || p.N == 0) {
@@ -846,7 +852,7 @@ gemm15_status_t gemm_plan_create(gemm15_plan_t* out, const gemm15_plan_desc_t* d
     if (!out || !desc) return GEMM15_ERR_INVALID_ARG;
     *out = nullptr;
     const gemm15_plan_desc_t& d = *desc;
-    auto valid_t = [](int t) { return t >= GEMM15_F16 && t <= GEMM15_E4M3; };
+    auto valid_t = [](int t) { return t >= GEMM15_F16 && t <= GEMM15_E2M1; };
     auto valid_l = [](int l) { return l == GEMM15_ROW_MAJOR || l == GEMM15_COL_MAJOR; };
     if (!valid_t(d.a) || !valid_t(d.b) || !valid_t(d.c) || !valid_t(d.d) || !valid_t(d.acc) ||
         !valid_l(d.layout_a) || !valid_l(d.layout_b) || !valid_l(d.layout_cd) ||
@@ -860,6 +866,9 @@ gemm15_status_t gemm_plan_create(gemm15_plan_t* out, const gemm15_plan_desc_t* d
         elem = out_elem = ELEM_BF16;
     } else if (d.a == GEMM15_E4M3 && d.c == GEMM15_BF16 && d.d == GEMM15_BF16) {
         elem = ELEM_E4M3;
+        out_elem = ELEM_BF16;
+    } else if ((d.a == GEMM15_E5M2 || d.a == GEMM15_E2M1) && d.c == GEMM15_BF16 && d.d == GEMM15_BF16) {
+        elem = d.a == GEMM15_E5M2 ? ELEM_E5M2 : ELEM_E2M1;  // block-scaled runs only
         out_elem = ELEM_BF16;
     } else {
         return GEMM15_ERR_UNSUPPORTED;
@@ -1114,6 +1123,7 @@ gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB
                               void* hD, int64_t M, int64_t N, int64_t K, float alpha, float beta,
                               float scale_a, float scale_b, void* stream) {
     if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (block_scaled_only(plan)) return GEMM15_ERR_UNSUPPORTED;
     if (M < 0 || N < 0 || K < 0) return GEMM15_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM15_OK;
     if (!hD || (K > 0 && (!hA || !hB)) || (beta != 0.0f && !hC)) return GEMM15_ERR_INVALID_ARG;
@@ -1197,6 +1207,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
                                  int32_t count, float alpha, float beta, void* stream) {
     if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
     if (count < 0 || (count > 0 && !problems)) return GEMM15_ERR_INVALID_ARG;
+    if (block_scaled_only(plan)) return GEMM15_ERR_UNSUPPORTED;
     DeviceGuard g(plan->device);
     if (!g.ok) return GEMM15_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1392,6 +1403,137 @@ gemm15_status_t gemm_run_batched(gemm15_plan_t plan, const void* A, int64_t lda,
         q.ldd = ldd;
     }
     return grouped_gemm_run(plan, probs.data(), batch, alpha, beta, stream);
+}
+
+gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_args_t* a,
+                                      void* stream) {
+    if (!plan_ok(plan)) return GEMM15_ERR_BAD_PLAN;
+    if (!a) return GEMM15_ERR_INVALID_ARG;
+    int sf = -1;
+    if (plan->elem == ELEM_E4M3 || plan->elem == ELEM_E5M2) {
+        if (a->scale_kind == GEMM15_SCALE_MX) sf = SF_MXF8;
+    } else if (plan->elem == ELEM_E2M1) {
+        if (a->scale_kind == GEMM15_SCALE_MX) sf = SF_MXF4;
+        else if (a->scale_kind == GEMM15_SCALE_NV) sf = SF_NVF4;
+    }
+    if (a->scale_kind != GEMM15_SCALE_MX && a->scale_kind != GEMM15_SCALE_NV) return GEMM15_ERR_INVALID_ARG;
+    if (sf < 0) return GEMM15_ERR_UNSUPPORTED;
+    if (plan->desc.layout_a != GEMM15_ROW_MAJOR || plan->desc.layout_b != GEMM15_COL_MAJOR ||
+        plan->desc.layout_cd != GEMM15_ROW_MAJOR)
+        return GEMM15_ERR_UNSUPPORTED;
+    const int64_t M = a->M, N = a->N, K = a->K;
+    if (M < 0 || N < 0 || K < 0) return GEMM15_ERR_INVALID_ARG;
+    if (M > (1ll << 31) - 256 || N > (1ll << 31) - 256 || K > (1ll << 31) - 256)
+        return GEMM15_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) {
+        std::memset(&plan->last, 0, sizeof(plan->last));
+        return GEMM15_OK;
+    }
+    const bool fp4 = plan->elem == ELEM_E2M1;
+    const int64_t bk = fp4 ? 256 : 128;  // elements of one 128-byte k-block
+    if (K == 0 || K % bk) return GEMM15_ERR_UNSUPPORTED;
+    const int64_t block = sf == SF_NVF4 ? 16 : 32;
+    const int64_t lda = a->lda ? a->lda : K, ldb = a->ldb ? a->ldb : K;
+    const int64_t ldd = a->ldd ? a->ldd : N, ldc = a->ldc ? a->ldc : N;
+    const bool has_c = a->beta != 0.0f;
+    if (!a->A || !a->B || !a->SFA || !a->SFB || !a->D || (has_c && !a->C)) return GEMM15_ERR_INVALID_ARG;
+    if (lda < K || ldb < K || ldd < N || (has_c && ldc < N)) return GEMM15_ERR_INVALID_ARG;
+    if (fp4 && (lda % 2 || ldb % 2)) return GEMM15_ERR_ALIGNMENT;
+    const int64_t lda_b = fp4 ? lda / 2 : lda, ldb_b = fp4 ? ldb / 2 : ldb;  // bytes
+    if (!aligned16(a->A) || !aligned16(a->B) || !aligned16(a->SFA) || !aligned16(a->SFB) ||
+        !aligned16(a->D) || (has_c && !aligned16(a->C)) || (a->bias && !aligned16(a->bias)))
+        return GEMM15_ERR_ALIGNMENT;
+    if (lda_b % 16 || ldb_b % 16 || (ldd * 2) % 16 || (has_c && (ldc * 2) % 16))
+        return GEMM15_ERR_ALIGNMENT;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return GEMM15_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (order_after_previous(plan, s) != GEMM15_OK) return GEMM15_ERR_CUDA;
+
+    constexpr int BN = 256;
+    Decision d;
+    d.cg = 1;
+    d.bn = BN;
+    d.bk = static_cast<int>(bk);
+    d.sched = SCHED_DP;
+    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M));
+    d.n_blocks = static_cast<int32_t>(cdiv(N, BN));
+    d.tiles = d.m_blocks * d.n_blocks;
+    d.k_blocks = static_cast<int32_t>(K / bk);
+    const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
+    d.grid = static_cast<int>(std::min<int64_t>(G, d.tiles));
+    d.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, d.m_blocks)
+                                    : std::min<int32_t>(d.m_blocks, 16);
+
+    GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    // operands as bytes: 128-byte boxes of K, 128 rows of A and 256 of B
+    const uint64_t kbytes = static_cast<uint64_t>(fp4 ? K / 2 : K);
+    bool ok = make_tmap(&gp.tmA, ELEM_E4M3, a->A, kbytes, M, lda_b, 128, TILE_M);
+    ok = ok && make_tmap(&gp.tmB, ELEM_E4M3, a->B, kbytes, N, ldb_b, 128, BN);
+    Prob po{};
+    po.M = M;
+    po.N = N;
+    po.D = a->D;
+    po.ldd = ldd;
+    po.C = a->C;
+    po.ldc = ldc;
+    ok = ok && output_maps(plan, po, has_c, &gp.tmC, &gp.tmD);
+    if (!ok) return GEMM15_ERR_CUDA;
+    gp.D = a->D;
+    gp.ldd = ldd;
+    gp.C = has_c ? a->C : nullptr;
+    gp.ldc = ldc;
+    gp.M = static_cast<int32_t>(M);
+    gp.N = static_cast<int32_t>(N);
+    gp.K = static_cast<int32_t>(K);
+    gp.k_blocks = d.k_blocks;
+    gp.m_blocks = d.m_blocks;
+    gp.n_blocks = d.n_blocks;
+    gp.tiles = d.tiles;
+    gp.raster = d.raster;
+    gp.sched = SCHED_DP;
+    gp.splits = 1;
+    gp.has_c = has_c;
+    gp.alpha = a->alpha;
+    gp.beta = a->beta;
+    gp.act = static_cast<int>(plan->desc.epilogue);
+    gp.bias = a->bias;
+    gp.sfa = static_cast<const uint8_t*>(a->SFA);
+    gp.sfb = static_cast<const uint8_t*>(a->SFB);
+    gp.sf_cb = static_cast<int32_t>(K / block / 4);
+    gp.sfb_rows = static_cast<int32_t>(cdiv(N, TILE_M));
+    gp.a_kmajor = gp.b_kmajor = 1;
+    gp.a_lbo = gp.b_lbo = 16;
+    gp.a_sbo = gp.b_sbo = 1024;
+    gp.a_kstep = gp.b_kstep = 32;
+    // instruction descriptor of the block-scaled kinds: A / B format (E4M3 0,
+    // E5M2 1; E2M1 1 for the fp4 kinds), K-major operands, N >> 3, scale
+    // format (bit 23: 1 UE8M0, 0 UE4M3), M >> 4; the scale-factor IDs (bits
+    // 29-30 and 4-5) are set per MMA by the kernel
+    const uint32_t fmt = plan->elem == ELEM_E4M3 ? 0u : 1u;
+    gp.idesc = (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+               ((sf == SF_NVF4 ? 0u : 1u) << 23) | (static_cast<uint32_t>(TILE_M >> 4) << 24);
+    gp.ws = plan->d_ws;
+    gp.flags = plan->d_flags;
+    gp.status = plan->d_status;
+    gp.epoch = ++plan->epoch == 0 ? ++plan->epoch : plan->epoch;
+    gp.timeout_ns = static_cast<uint64_t>(plan->opt.timeout_us) * 1000ull;
+    gp.fault_skip_flag = -1;
+    gemm15_status_t st = attach_trace(plan, gp, d.grid, s);
+    if (st != GEMM15_OK) return st;
+    cudaError_t e;
+    if (sf == SF_MXF8)
+        e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, BN, 1, SF_MXF8>(gp, d.grid, s)
+                                    : launch_gemm<ELEM_E5M2, BN, 1, SF_MXF8>(gp, d.grid, s);
+    else if (sf == SF_MXF4)
+        e = launch_gemm<ELEM_E2M1, BN, 1, SF_MXF4>(gp, d.grid, s);
+    else
+        e = launch_gemm<ELEM_E2M1, BN, 1, SF_NVF4>(gp, d.grid, s);
+    if (e != cudaSuccess) return GEMM15_ERR_CUDA;
+    record_config(plan, d, 1);
+    plan->last.stages = gemm_scaled_stages(sf);
+    return mark_done(plan, s);
 }
 
 gemm15_status_t gemm_plan_query_error(gemm15_plan_t plan) {

@@ -42,17 +42,27 @@ namespace g15 {
 // two CTAs) computes a 256 x BN tile with tcgen05 cta_group::2 -- each CTA
 // stages its own 128 rows of A and its own BN/2 columns of B, and holds its
 // 128 rows of the accumulator in its own TMEM.
-template <int ELEM, int BN, int CG = 1>
+template <int ELEM, int BN, int CG = 1, int SF = SF_NONE>
 struct Traits {
-    static constexpr bool F8 = (ELEM == ELEM_E4M3);
-    static constexpr int ESIZE = F8 ? 1 : 2;           // bytes per A/B element
-    static constexpr int BK = 128 / ESIZE;             // one 128-byte swizzle row of K
-    static constexpr int UMMA_K = 32 / ESIZE;          // K per tcgen05.mma
+    static constexpr bool FP4 = (ELEM == ELEM_E2M1);   // packed, two elements per byte
+    static constexpr bool F8 = (ELEM == ELEM_E4M3 || ELEM == ELEM_E5M2 || FP4);
+    static constexpr int ESIZE = F8 ? 1 : 2;           // bytes per A/B element (fp4: per pair)
+    static constexpr int BK = FP4 ? 256 : 128 / ESIZE; // elements of one 128-byte swizzle row of K
+    static constexpr int UMMA_K = FP4 ? 64 : 32 / ESIZE;  // K per tcgen05.mma (32 bytes)
     static constexpr int KSTEPS = BK / UMMA_K;         // MMAs per k-block (4)
     static constexpr int A_STAGE = TILE_M * 128;       // 16 KB
     static constexpr int B_COLS = BN / CG;             // B columns staged by one CTA
     static constexpr int B_STAGE = B_COLS * 128;       // 16 or 32 KB
-    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    // block-scaled kinds: 512-byte scale atoms per k-block and 128 rows (1 for
+    // the 4 scales of an MXFP8 k-block, 2 for MXFP4's 8, 4 for NVFP4's 16)
+    static constexpr int SF_APK = SF == SF_NONE ? 0 : SF == SF_MXF8 ? 1 : SF == SF_MXF4 ? 2 : 4;
+    static constexpr int SF_BROWS = BN / 128;          // 128-row blocks of B
+    static constexpr int SF_STAGE = SF_APK * 512 * (1 + SF_BROWS);
+    static constexpr int SF_COLS = SF_APK * 4 * (1 + SF_BROWS);  // TMEM columns per stage
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE + SF_STAGE;
+    // accumulators in TMEM: two (the epilogue of one tile overlaps the next
+    // tile's mainloop), or one when the scale factors need the other half
+    static constexpr int ACC_BUFS = SF == SF_NONE ? 2 : 1;
     // Epilogue staging: one 32 x 64 box per warp and output chunk of the tile
     // when that leaves room for six stages (the whole C tile is then fetched
     // as soon as the tile starts), else a ring of two boxes per warp (the rest
@@ -69,18 +79,22 @@ struct Traits {
     // an N-major B stage is whole 128-byte swizzle rows of N
     static_assert(B_COLS * ESIZE >= 128 && (B_COLS * ESIZE) % 128 == 0, "B columns per CTA");
     static_assert(EPI_BUFS <= 8, "C barrier parity bits");
+    static_assert(SF == SF_NONE || (CG == 1 && BN % 128 == 0), "block-scaled tiles");
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
-    static constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SF = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
     // barriers: full[S], empty[S], acc_full[2], acc_empty[2], cbar[4][EPI_BUFS], drain, epi
     static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_BUFS * EPI_WARPS + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem base, abort flag
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;      // + alignment slack
-    static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators
+    // TMEM: the accumulators, then (block-scaled) one scale-factor slot per stage
+    static constexpr uint32_t TMEM_COLS = SF == SF_NONE ? 2 * BN : 512;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(TMEM_COLS <= 512, "TMEM budget");
+    static_assert(SF == SF_NONE || ACC_BUFS * BN + STAGES * SF_COLS <= 512, "TMEM scale-factor slots");
 };
 
 template <int ELEM>
@@ -95,6 +109,14 @@ struct OutType<ELEM_BF16> {
 };
 template <>
 struct OutType<ELEM_E4M3> {
+    using T = __nv_bfloat16;
+};
+template <>
+struct OutType<ELEM_E5M2> {
+    using T = __nv_bfloat16;
+};
+template <>
+struct OutType<ELEM_E2M1> {
     using T = __nv_bfloat16;
 };
 
@@ -510,10 +532,11 @@ __device__ __forceinline__ uint64_t* trace_rec(const GemmParams& p, int32_t item
 
 // ------------------------------------------------------------------ the kernel
 
-template <int ELEM, int BN, int CG>
+template <int ELEM, int BN, int CG, int SF>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ GemmParams p) {
-    using TR = Traits<ELEM, BN, CG>;
+    using TR = Traits<ELEM, BN, CG, SF>;
+    constexpr int ACC_BUFS = TR::ACC_BUFS;
     using OutT = typename OutType<ELEM>::T;
     constexpr int STAGES = TR::STAGES;
     constexpr int TILE_ROWS = TILE_M * CG;  // output rows per tile
@@ -525,6 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sA = sbase + TR::OFF_A;
     const uint32_t sB = sbase + TR::OFF_B;
+    const uint32_t sSF = sbase + TR::OFF_SF;
     const uint32_t sEpi = sbase + TR::OFF_EPI;
     const uint32_t bar0 = sbase + TR::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -625,10 +649,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // which the leader arms for the pair's bytes
                     uint32_t fb = full_bar(s);
                     if constexpr (CG == 2) fb = map_cluster(fb, 0);
-                    if (leader) mbar_arrive_expect_tx(full_bar(s), CG * TR::STAGE_BYTES);
+                    if constexpr (SF != SF_NONE) {
+                        // the stage's scale atoms: A's 128 rows, then each 128-row
+                        // block of B that exists (absent ones are not read; their
+                        // columns lie past N)
+                        const int32_t rb0 = w.n_blk * TR::SF_BROWS;
+                        const int32_t nb_live = min(TR::SF_BROWS, p.sfb_rows - rb0);
+                        const uint32_t atoms = TR::SF_APK * 512u;
+                        mbar_arrive_expect_tx(full_bar(s), TR::A_STAGE + TR::B_STAGE + atoms * (1 + nb_live));
+                        const uint32_t dS = sSF + s * TR::SF_STAGE;
+                        const int64_t cb0 = static_cast<int64_t>(kb) * TR::SF_APK;
+                        bulk_g2s(dS, p.sfa + (static_cast<int64_t>(w.m_blk) * p.sf_cb + cb0) * 512, atoms, fb);
+                        for (int32_t nb = 0; nb < nb_live; ++nb)
+                            bulk_g2s(dS + (1 + nb) * atoms, p.sfb + (static_cast<int64_t>(rb0 + nb) * p.sf_cb + cb0) * 512,
+                                     atoms, fb);
+                    } else if (leader) {
+                        mbar_arrive_expect_tx(full_bar(s), CG * TR::STAGE_BYTES);
+                    }
                     const uint32_t dA = sA + s * TR::A_STAGE;
                     const uint32_t dB = sB + s * TR::B_STAGE;
-                    const int32_t k0 = kb * TR::BK;
+                    // K coordinate in tensor-map units: elements, or bytes for packed fp4
+                    const int32_t k0 = kb * (TR::FP4 ? 128 : TR::BK);
                     auto load = [&](uint32_t dst, const CUtensorMap* t, int32_t x, int32_t y) {
                         if constexpr (CG == 2) tma_load_2d_pair(dst, t, fb, x, y);
                         else tma_load_2d(dst, t, fb, x, y);
@@ -695,8 +736,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             };
             while (ok && sched_next(p, un, st, w)) {
-                const uint32_t ab = n_acc & 1u;
-                const uint32_t aph = (n_acc >> 1) & 1u;
+                const uint32_t ab = ACC_BUFS == 2 ? (n_acc & 1u) : 0u;
+                const uint32_t aph = ACC_BUFS == 2 ? ((n_acc >> 1) & 1u) : (n_acc & 1u);
                 if (!wait_bar(ctl, acce_bar(ab), aph ^ 1u)) {
                     ok = false;
                     break;
@@ -715,11 +756,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
                     const uint32_t a_addr = sA + s * TR::A_STAGE;
                     const uint32_t b_addr = sB + s * TR::B_STAGE;
+                    if constexpr (SF != SF_NONE) {
+                        // the stage's scale atoms into its TMEM slot (after the
+                        // accumulator): A's atom j at +4j, B's atom j of row block
+                        // nb at +4*APK + 4*SF_BROWS*j + 4*nb
+                        const uint32_t sf_t = tmem_base + ACC_BUFS * BN + s * TR::SF_COLS;
+                        const uint32_t sfb_t = sf_t + 4 * TR::SF_APK;
+                        const uint32_t dS = sSF + s * TR::SF_STAGE;
+#pragma unroll
+                        for (int j = 0; j < TR::SF_APK; ++j) {
+                            tmem_cp_32x128b_x4(sf_t + 4 * j, sdesc_atom(dS + 512 * j));
+#pragma unroll
+                            for (int nb = 0; nb < TR::SF_BROWS; ++nb)
+                                tmem_cp_32x128b_x4(sfb_t + 4 * TR::SF_BROWS * j + 4 * nb,
+                                                   sdesc_atom(dS + (1 + nb) * 512 * TR::SF_APK + 512 * j));
+                        }
+#pragma unroll
+                        for (int k = 0; k < TR::KSTEPS; ++k) {
+                            // MXFP8: one scale per row and MMA, byte k of atom 0;
+                            // MXFP4: two per MMA, bytes 2(k%2).. of atom k/2;
+                            // NVFP4: four per MMA, atom k
+                            uint32_t atom = 0, id = 0;
+                            if constexpr (SF == SF_MXF8) { id = k; }
+                            else if constexpr (SF == SF_MXF4) { atom = k >> 1; id = 2 * (k & 1); }
+                            else { atom = k; }
+                            const uint32_t idesc = p.idesc | (id << 29) | (id << 4);
+                            umma_block_scaled<SF>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
+                                                  sdesc_at(bdesc0, b_addr + k * p.b_kstep), idesc,
+                                                  sf_t + 4 * atom, sfb_t + 4 * TR::SF_BROWS * atom,
+                                                  (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        }
+                    } else {
 #pragma unroll
                     for (int k = 0; k < TR::KSTEPS; ++k) {
                         umma<CG, TR::F8>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
                                          sdesc_at(bdesc0, b_addr + k * p.b_kstep), p.idesc,
                                          (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
                     }
                     issued = true;
                     commit(empty_bar(s));
@@ -793,8 +866,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int last_group = -1;
         bool ok = true;
         while (ok && sched_next(p, un, st, w)) {
-            const uint32_t ab = n_acc & 1u;
-            const uint32_t aph = (n_acc >> 1) & 1u;
+            const uint32_t ab = ACC_BUFS == 2 ? (n_acc & 1u) : 0u;
+            const uint32_t aph = ACC_BUFS == 2 ? ((n_acc >> 1) & 1u) : (n_acc & 1u);
 
             int32_t M = p.M, N = p.N;
             const CUtensorMap* tC = &p.tmC;
@@ -883,7 +956,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // the peers' partial tiles is loaded into it while this item's
             // mainloop still runs, so the fix-up reads TMEM instead of L2.
             const int32_t pb0 = w.kind == WK_OWNER ? next_peer(w, w.h0) : -1;
-            const bool preload = pb0 >= 0 && sched_sk_last(st) && ok;
+            const bool preload = ACC_BUFS == 2 && pb0 >= 0 && sched_sk_last(st) && ok;
             if (preload && rows_live) {
                 for (int c = 0; c < nch; ++c) {
                     const int32_t col0 = c * EPI_COLS;

@@ -6,7 +6,14 @@
 
 namespace g15 {
 
-enum ElemKind : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_E4M3 = 2 };
+enum ElemKind : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_E4M3 = 2, ELEM_E5M2 = 3, ELEM_E2M1 = 4 };
+// block-scaled MMA kinds (tcgen05 .block_scale): scale factors per 32 or 16 K
+enum ScaleKind : int {
+    SF_NONE = 0,
+    SF_MXF8 = 1,   // kind::mxf8f6f4, UE8M0 per 32, scale_vec::1X (E4M3 / E5M2 elements)
+    SF_MXF4 = 2,   // kind::mxf4, UE8M0 per 32, scale_vec::2X (packed E2M1)
+    SF_NVF4 = 3    // kind::mxf4nvf4, UE4M3 per 16, scale_vec::4X (packed E2M1)
+};
 enum Schedule : int { SCHED_DP = 1, SCHED_SK = 2, SCHED_SPLIT = 3 };
 enum DeviceError : int { DEV_ERR_TIMEOUT = 5, DEV_ERR_FAULT = 7 };
 // epilogue activation (values of gemm15_epilogue_t)
@@ -66,6 +73,12 @@ struct GemmParams {
     int32_t out_trans;                // 1: the computed tile is the transpose of the stored
                                       // one (swap-AB): element (r, c) of the computed output
                                       // lives at C / D / Z + c * ld + r
+    // block-scaled operands: scale factors in the 128 x 4 atom layout (512-byte
+    // atoms, one per 128 rows and 4 consecutive scales along K; atom (rb, cb)
+    // at (rb * sf_cb + cb) * 512); sfb_rows = number of 128-row blocks of B
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    int32_t sf_cb, sfb_rows;
     // operand layouts in shared memory (bytes) and the MMA instruction descriptor
     uint32_t a_kmajor, b_kmajor;
     uint32_t a_lbo, a_sbo, a_kstep;

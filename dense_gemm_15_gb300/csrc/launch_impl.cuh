@@ -6,21 +6,21 @@
 
 namespace g15 {
 
-template <int ELEM, int BN, int CG>
+template <int ELEM, int BN, int CG, int SF>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
-    using TR = Traits<ELEM, BN, CG>;
+    using TR = Traits<ELEM, BN, CG, SF>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        err = cudaFuncSetAttribute(gemm_tc_kernel<ELEM, BN, CG>,
+        err = cudaFuncSetAttribute(gemm_tc_kernel<ELEM, BN, CG, SF>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, TR::SMEM_BYTES);
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
     if constexpr (CG == 1) {
-        gemm_tc_kernel<ELEM, BN, 1><<<grid, NUM_THREADS, TR::SMEM_BYTES, stream>>>(p);
+        gemm_tc_kernel<ELEM, BN, 1, SF><<<grid, NUM_THREADS, TR::SMEM_BYTES, stream>>>(p);
         return cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
@@ -35,14 +35,14 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<ELEM, BN, 2>, p);
+        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<ELEM, BN, 2, SF>, p);
     }
 }
 
 template <int ELEM>
 int max_pair_clusters() {
     using TR = Traits<ELEM, 256, 2>;
-    if (cudaFuncSetAttribute(gemm_tc_kernel<ELEM, 256, 2>,
+    if (cudaFuncSetAttribute(gemm_tc_kernel<ELEM, 256, 2, SF_NONE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              TR::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
@@ -60,7 +60,7 @@ int max_pair_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<ELEM, 256, 2>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<ELEM, 256, 2, SF_NONE>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }

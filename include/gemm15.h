@@ -57,7 +57,10 @@ typedef enum {
     GEMM15_F16 = 0,  /* IEEE binary16 */
     GEMM15_BF16 = 1, /* bfloat16 */
     GEMM15_F32 = 2,  /* binary32: accumulator type only */
-    GEMM15_E4M3 = 3  /* OCP fp8 e4m3 (finite-only variant), A and B only */
+    GEMM15_E4M3 = 3, /* OCP fp8 e4m3 (finite-only variant), A and B only */
+    GEMM15_E5M2 = 4, /* OCP fp8 e5m2, A and B only, block-scaled runs only */
+    GEMM15_E2M1 = 5  /* OCP fp4 e2m1, two per byte (element 2i in the low nibble),
+                        A and B only, block-scaled runs only */
 } gemm15_dtype_t;
 
 typedef enum { GEMM15_ROW_MAJOR = 0, GEMM15_COL_MAJOR = 1 } gemm15_layout_t;
@@ -94,9 +97,10 @@ typedef enum {
 typedef struct gemm15_plan* gemm15_plan_t;
 
 /* Plan description: element types and layouts, fixed for the plan's life.
- * Supported: a == b in {F16, BF16} with c == d == a; or a == b == E4M3 with
- * c == d == BF16.  acc must be F32.  layout_a / layout_b are free; layout_cd
- * applies to both C and D. */
+ * Supported: a == b in {F16, BF16} with c == d == a; or a == b in {E4M3,
+ * E5M2, E2M1} with c == d == BF16 (E5M2 and E2M1 plans run only
+ * gemm_run_block_scaled).  acc must be F32.  layout_a / layout_b are free;
+ * layout_cd applies to both C and D. */
 typedef struct {
     gemm15_dtype_t a, b, c, d, acc;
     gemm15_layout_t layout_a, layout_b, layout_cd;
@@ -354,6 +358,58 @@ gemm15_status_t gemm_plan_forget_tuning(gemm15_plan_t plan);
  * off or `capacity` is too small (*ctas and *items are still set). */
 gemm15_status_t gemm_plan_trace(gemm15_plan_t plan, void* out, int64_t capacity, int32_t* ctas,
                                 int32_t* items);
+
+/* Block scaling of fp8 / fp4 operands: one scale per `block` consecutive K
+ * elements of a row of A and of a column of B (the _scaled_mm formats MXFP8,
+ * MXFP4 and NVFP4 of "Generating State-of-the-Art GEMMs with TorchInductor's
+ * CuteDSL backend", section 5.1; their scale types and block sizes are the
+ * OCP MX and NVFP4 definitions). */
+typedef enum {
+    GEMM15_SCALE_MX = 1, /* UE8M0 scales (2^(e-127)) per 32 elements: MXFP8 (E4M3 /
+                            E5M2 plans) and MXFP4 (E2M1 plans) */
+    GEMM15_SCALE_NV = 2  /* UE4M3 scales (e4m3 bits, positive) per 16 elements:
+                            NVFP4 (E2M1 plans); a per-tensor fp32 scale goes in alpha */
+} gemm15_scale_kind_t;
+
+/* Arguments of gemm_run_block_scaled.  A is M x K row-major (K contiguous),
+ * B is K x N column-major (stored as N rows of K contiguous elements): the
+ * "TN" layout.  lda / ldb are in elements (0 = K); for E2M1 they count 4-bit
+ * elements and must be even.  SFA holds the M x K/block scales of A, SFB the
+ * N x K/block scales of B, both in the 128 x 4 blocked layout the tensor
+ * cores read: 512-byte atoms, one per 128 rows (row block rb) and 4
+ * consecutive scales along K (column block cb), atom (rb, cb) at byte
+ * (rb * K/(4*block) + cb) * 512, the scale of row r, column c at byte
+ * 16 * (r % 32) + 4 * ((r % 128) / 32) + c % 4 inside it; rows beyond M (N)
+ * up to the next multiple of 128 are padding (any value).  C, D are M x N
+ * bf16 row-major (ldc / ldd 0 = N), bias an optional N-vector of bf16. */
+typedef struct {
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    const void* SFA;
+    const void* SFB;
+    int32_t scale_kind;  /* gemm15_scale_kind_t */
+    const void* C;
+    int64_t ldc;
+    void* D;
+    int64_t ldd;
+    int64_t M, N, K;
+    float alpha, beta;
+    const void* bias;
+} gemm15_scaled_args_t;
+
+/* D = act(alpha * sum_k (A[i,k] * SFA[i, k/block]) * (B[k,j] * SFB[j, k/block])
+ *        + beta * C + bias): the block-scaled GEMM, on tcgen05 block-scaled MMAs
+ * (kind::mxf8f6f4 for MXFP8, kind::mxf4 for MXFP4, kind::mxf4nvf4 for NVFP4;
+ * scale factors copied to tensor memory beside the accumulator).  The plan
+ * must have layout_a ROW_MAJOR, layout_b COL_MAJOR, layout_cd ROW_MAJOR
+ * (UNSUPPORTED otherwise).  K must be a multiple of 128 (fp8) or 256 (fp4)
+ * (UNSUPPORTED otherwise); pointers 16-byte aligned and leading dimensions
+ * whole multiples of 16 bytes (ALIGNMENT otherwise).  M == 0 or N == 0: OK,
+ * nothing launched; K == 0: UNSUPPORTED.  Asynchronous on `stream`. */
+gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_args_t* args,
+                                      void* stream);
 
 /* ---- Split-K GEMM that allocates nothing.  The pages have no counterpart of
  * this entry point; it exists for callers that cannot call cudaMalloc: code

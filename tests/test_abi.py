@@ -83,7 +83,7 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
     compare every struct's size and field offsets with the ctypes mirrors."""
     mirrors = {"gemm15_plan_desc_t": g.PlanDesc, "gemm15_problem_t": g.Problem,
                "gemm15_config_t": g.Config, "gemm15_args_t": g.Args,
-               "gemm15_tune_result_t": g.TuneResult}
+               "gemm15_tune_result_t": g.TuneResult, "gemm15_scaled_args_t": g.ScaledArgs}
     lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "gemm15.h"', "int main(void) {"]
     for cname, cls in mirrors.items():
         lines.append('printf("%s size %%zu\\n", sizeof(%s));' % (cname, cname))
