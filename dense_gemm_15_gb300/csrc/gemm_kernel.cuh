@@ -83,7 +83,9 @@ struct Traits {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SF = OFF_B + STAGES * B_STAGE;
-    static constexpr int OFF_EPI = OFF_SF + STAGES * SF_STAGE;
+    // the epilogue's 128-byte-swizzled staging boxes start on a 1024-byte boundary
+    static constexpr int OFF_EPI = OFF_SF + (STAGES * SF_STAGE + 1023) / 1024 * 1024;
+    static_assert(OFF_EPI % 1024 == 0, "epilogue staging alignment");
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
     // barriers: full[S], empty[S], acc_full[2], acc_empty[2], cbar[4][EPI_BUFS], drain, epi
     static constexpr int NUM_BARS = 2 * STAGES + 4 + EPI_BUFS * EPI_WARPS + 2;
