@@ -51,6 +51,11 @@ def workloads():
                                                                  bias=True)],
         # batch_count 16 of one shape, packed strides (kwkr.cn blog section 6.3)
         BATCHED_WORKLOAD: lambda: [I.random_problem(1024, 1024, 1024, seed=b) for b in range(16)],
+        # block-scaled _scaled_mm formats (CuteDSL page, section 5.1)
+        "mxfp8_e4m3_8192": lambda: [I.block_scaled_problem(8192, 8192, 8192, elem="e4m3")],
+        "mxfp4_8192": lambda: [I.block_scaled_problem(8192, 8192, 8192, elem="e2m1")],
+        "nvfp4_8192": lambda: [I.block_scaled_problem(8192, 8192, 8192, elem="e2m1", block=16,
+                                                      scale="e4m3")],
     }
     for layer in I.LLAMA70B_LAYERS:
         for m in I.LLAMA70B_TOKENS:
@@ -108,10 +113,13 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# nominal dense tensor-core ratios to bf16 (2.25 / 4.5 / 13.5 PFLOP/s on GB300)
+PEAK_RATIO = {"f16": 1.0, "bf16": 1.0, "e4m3": 2.0, "e5m2": 2.0, "e2m1": 6.0}
+
+
 def tensor_peak(dtype, pk, sustained=False):
     bf16 = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    # nominal dense ratios: fp16 = bf16, fp8 = 2 x bf16
-    return bf16 * (2.0 if dtype == "e4m3" else 1.0)
+    return bf16 * PEAK_RATIO[dtype]
 
 
 def code_only(src: str) -> str:
@@ -168,8 +176,11 @@ def recorded_traffic(workload):
 def algorithmic_bytes(probs):
     tot = 0
     for p in probs:
-        ea = 1 if p.a_dtype == "e4m3" else 2
-        tot += p.M * p.K * ea + p.K * p.N * ea + p.M * p.N * 2
+        ea = {"e4m3": 1, "e5m2": 1, "e2m1": 0.5}.get(p.a_dtype, 2)
+        tot += int(p.M * p.K * ea + p.K * p.N * ea) + p.M * p.N * 2
+        scales = getattr(p, "block_scales", None)
+        if scales is not None:  # one byte per block of A's rows and B's columns
+            tot += (p.M + p.N) * (p.K // scales[3])
         if p.beta != 0.0:
             tot += p.M * p.N * 2
         if getattr(p, "bias", None) is not None:
@@ -197,7 +208,9 @@ def roofline_entry(flops, abytes, ms, dtype, pk, pk_kind, traffic):
                 "achieved_tflops": achieved, "intensity_flop_per_byte": flops / abytes}
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": traffic,
-            "peak_source": "%s bf16 burst%s" % (pk_kind, " x2 (fp8)" if dtype == "e4m3" else ""),
+            "peak_source": "%s bf16 burst%s" % (
+                pk_kind, "" if PEAK_RATIO[dtype] == 1.0 else
+                " x%g (%s, nominal dense ratio)" % (PEAK_RATIO[dtype], dtype)),
             "algorithmic_bytes": abytes, "achieved_gbs": achieved_gbs,
             "intensity_flop_per_byte": flops / abytes}
 
@@ -272,12 +285,16 @@ def cpu_oracle_sample(probs, budget_s=10.0, max_rows=None):
     c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
     bv = I.bits(p.bias) if p.bias is not None else None
 
+    sc = getattr(p, "block_scales", None)
+    scales = (I.bits(sc[0]), I.bits(sc[1]), sc[2], sc[3]) if sc is not None else None
+
     def run(rows):
         t0 = time.perf_counter()
         oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
                     act=p.act, bias=bv, bias_dtype=p.d_dtype, scale_a=p.scale_a,
                     scale_b=p.scale_b, a_col_major=p.a_col_major, b_col_major=p.b_col_major,
-                    rows=(0, rows), threads=threads)
+                    rows=(0, rows), threads=threads,
+                    scales=(scales[0][:rows], scales[1], scales[2], scales[3]) if scales else None)
         return time.perf_counter() - t0
 
     rows = min(p.M, max(1, threads))
@@ -399,14 +416,22 @@ def run_gpu(args):
     p0 = probs[0]
     flops = sum(p.flops for p in probs)
 
+    scaled = getattr(p0, "block_scales", None) is not None
     plan = g.Plan(p0.a_dtype, p0.d_dtype, epilogue=p0.act,
                   layout_a=g.COL_MAJOR if p0.a_col_major else g.ROW_MAJOR,
-                  layout_b=g.COL_MAJOR if p0.b_col_major else g.ROW_MAJOR)
+                  layout_b=g.COL_MAJOR if (p0.b_col_major or scaled) else g.ROW_MAJOR)
     for opt in args.opt or []:
         k, v = opt.split("=")
         plan.set(getattr(g, "OPT_" + k.upper()), int(v))
     dv = []
+    if scaled:  # TN storage, packed fp4, scale atoms (inputs.block_scaled_storage)
+        st_arrays = [torch.from_numpy(x).to(dev) for x in I.block_scaled_storage(p0)]
+        scaled_kind = g.SCALE_NV if p0.block_scales[2] == "e4m3" else g.SCALE_MX
     for p in probs:
+        if scaled:
+            dv.append((st_arrays[0], st_arrays[1], None,
+                       torch.empty(p.M, p.N, dtype=torch.bfloat16, device=dev)))
+            continue
         A, B = p.A.to(dev), p.B.to(dev)
         C = p.C.to(dev) if p.C is not None else None
         D = torch.empty(p.M, p.N, dtype=I.TORCH_DTYPE[p.d_dtype], device=dev)
@@ -435,7 +460,14 @@ def run_gpu(args):
         del dv[1:]
 
     def step():
-        if batched:
+        if scaled:
+            A, B, _, D = dv[0]
+            st = g.gemm_run_block_scaled(plan.handle, A, B, st_arrays[2], st_arrays[3], D,
+                                         p0.M, p0.N, p0.K, scale_kind=scaled_kind,
+                                         alpha=p0.alpha, stream=stream)
+            if st != g.OK:
+                raise RuntimeError("gemm_run_block_scaled: " + g.status_string(st))
+        elif batched:
             plan.batched(bA, bB, None, bD, p0.M, p0.N, p0.K, len(probs), p0.M * p0.K,
                          p0.K * p0.N, 0, p0.M * p0.N, alpha=p0.alpha, beta=p0.beta,
                          stream=stream)
@@ -448,7 +480,7 @@ def run_gpu(args):
                      scale_b=scales[1] if scales else None, stream=stream, bias=bias_dev)
 
     tuned = None
-    if args.autotune and not grouped:
+    if args.autotune and not grouped and not scaled:
         A, B, C, D = dv[0]
         res = plan.autotune(A, B, C, D, p0.M, p0.N, p0.K, alpha=p0.alpha, beta=p0.beta,
                             bias=bias_dev, scale_a=scales[0] if scales else None,
@@ -506,7 +538,7 @@ def run_gpu(args):
     # plan's cache after the first call), timed on the host; the launches are
     # real and drained afterwards, untimed
     host_c_us = None
-    if not grouped and p0.bias is None and not args.no_e2e:
+    if not grouped and not scaled and p0.bias is None and not args.no_e2e:
         lib = g.load()
         A, B, C, D = dv[0]
         lda = p0.M if p0.a_col_major else p0.K
@@ -525,7 +557,7 @@ def run_gpu(args):
 
     # end to end through the C ABI with pinned host buffers (single problems)
     e2e = None
-    if not grouped and not args.no_e2e:
+    if not grouped and not scaled and not args.no_e2e:
         hA, hB = p0.A.pin_memory(), p0.B.pin_memory()
         hC = p0.C.pin_memory() if p0.C is not None else None
         hD = torch.empty(p0.M, p0.N, dtype=I.TORCH_DTYPE[p0.d_dtype]).pin_memory()
@@ -566,12 +598,15 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3"}[p0.a_dtype],
+            "dtype": p0.a_dtype,
             "data": "synthetic",
             "config": {"workload": args.workload, "M": p0.M if not grouped else [p.M for p in probs],
                        "N": p0.N, "K": p0.K, "alpha": p0.alpha, "beta": p0.beta,
                        "relu": p0.relu, "epilogue": p0.act,
-                       "bias": p0.bias is not None, "layout": "row-major A, B, C, D",
+                       "bias": p0.bias is not None,
+                       "layout": ("A row-major, B column-major (TN), D row-major; %s block %d"
+                                  % (p0.block_scales[2], p0.block_scales[3]) if scaled
+                                  else "row-major A, B, C, D"),
                        "l2": ("flushed between steps (256 MiB write%s, outside the step events)"
                               % (" then 256 MiB read" if args.flush == "write+read" else "")),
                        "parallelism": "replicas" if ws > 1 else "single",

@@ -294,6 +294,47 @@ def block_scaled_problem(M, N, K, elem="e4m3", block=32, scale="ue8m0", alpha=1.
     return p
 
 
+SCALE_ONE = {"ue8m0": 0x7F, "e4m3": 0x38}  # scale code of 1.0
+
+
+def scale_atoms(codes: np.ndarray, one: int) -> np.ndarray:
+    """Scale codes [R, SK] (R rows of a K-major operand, SK = K / block scales
+    each, SK a multiple of 4) in the 128 x 4 blocked layout the tensor cores
+    read: 512-byte atoms, atom (rb, cb) holding rows 128 rb .. 128 rb + 127 and
+    scale columns 4 cb .. 4 cb + 3 at byte offset (rb * SK/4 + cb) * 512, the
+    code of (r, c) at 16 * (r % 32) + 4 * ((r % 128) // 32) + c % 4 inside it.
+    Rows past R up to the next multiple of 128 hold `one`."""
+    R, SK = codes.shape
+    if SK % 4:
+        raise ValueError("the scale count along K must be a multiple of 4")
+    RB = -(-R // 128)
+    pad = np.full((RB * 128, SK), one, dtype=np.uint8)
+    pad[:R] = codes
+    t = pad.reshape(RB, 4, 32, SK // 4, 4)          # rb, q, i, cb, j with r = 128 rb + 32 q + i
+    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """E2M1 codes [R, K] (one per byte, low nibble) packed two per byte along
+    K, element 2i in the low nibble: [R, K / 2]."""
+    c = np.asarray(codes, dtype=np.uint8) & 0xF
+    return np.ascontiguousarray(c[:, 0::2] | (c[:, 1::2] << 4))
+
+
+def block_scaled_storage(prob):
+    """The device storage of a block-scaled problem for the GEMM's TN layout:
+    (A [M, K] codes, B as [N, K] codes (column-major B), SFA atoms, SFB atoms),
+    fp4 codes packed two per byte; numpy uint8 arrays."""
+    a = bits(prob.A)
+    b = np.ascontiguousarray(bits(prob.B).T)
+    sa, sb, scale, _ = prob.block_scales
+    if prob.a_dtype == "e2m1":
+        a, b = pack_e2m1(a), pack_e2m1(b)
+    sfa = scale_atoms(bits(sa), SCALE_ONE[scale])
+    sfb = scale_atoms(np.ascontiguousarray(bits(sb).T), SCALE_ONE[scale])
+    return np.ascontiguousarray(a), b, sfa, sfb
+
+
 def random_problem(M, N, K, dtype="f16", out_dtype=None, alpha=1.0, beta=0.0, relu=False,
                    a_col_major=False, b_col_major=False, seed=0, lo=-1.0, hi=1.0,
                    scale_a=1.0, scale_b=1.0, wid=9, act=None, bias=False,

@@ -61,7 +61,7 @@ def test_roofline_picks_the_roof_met_first():
     f8 = shape(8192, 8192, 8192, "e4m3")
     flops, ab = 2.0 * 8192 ** 3, bench.algorithmic_bytes([f8])
     r = bench.roofline_entry(flops, ab, 0.3, "e4m3", PK, "fallback", None)
-    assert r["bound"] == "tensor" and r["peak"] == 4000.0 and "x2 (fp8)" in r["peak_source"]
+    assert r["bound"] == "tensor" and r["peak"] == 4000.0 and "x2 (e4m3" in r["peak_source"]
     assert r["peak_source"].startswith("fallback")
 
 
@@ -134,3 +134,13 @@ def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
     assert bench.kernel_hash() == real
     k.write_text(k.read_text(encoding="utf-8") + "\nint one_more_line;\n", encoding="utf-8")
     assert bench.kernel_hash() != real
+
+
+def test_block_scaled_peaks_and_bytes():
+    """fp4 against 6 x the bf16 peak (the nominal 13.5 / 2.25 PFLOP/s ratio),
+    fp8 against 2 x; fp4 operands are half a byte, and each scale block adds a
+    byte per row of A and per column of B."""
+    assert bench.tensor_peak("e2m1", PK) == 12000.0 and bench.tensor_peak("e5m2", PK) == 4000.0
+    p = shape(8192, 8192, 8192, "e2m1")
+    p.block_scales = (None, None, "e4m3", 16)
+    assert bench.algorithmic_bytes([p]) == 2 * 8192 * 4096 + 8192 * 8192 * 2 + 2 * 8192 * 512

@@ -2,11 +2,11 @@
 "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL backend",
 section 5.1) against the oracle, through the C ABI.
 
-The operands are prepared on the host in the layout the entry point takes:
-A row-major and B column-major (both K contiguous), fp4 codes packed two per
-byte, scale factors in the 128 x 4 blocked atom layout.  The oracle takes the
-codes one per byte and the scales as plain M x K/block and K/block x N
-arrays, so the two sides share no layout code."""
+The operands are stored on the host in the layout the entry point takes
+(inputs.block_scaled_storage): A row-major and B column-major (both K
+contiguous), fp4 codes packed two per byte, scale factors in the 128 x 4
+blocked atom layout.  The oracle takes the codes one per byte and the scales
+as plain M x K/block and K/block x N arrays."""
 import numpy as np
 import pytest
 import torch
@@ -17,38 +17,9 @@ from helpers import assert_bit_exact, assert_matches_oracle
 
 pytestmark = pytest.mark.gpu
 
-ONE = {"ue8m0": 0x7F, "e4m3": 0x38}  # scale code of 1.0 (padding)
-
-
-def blocked(codes, one):
-    """Scale codes [R, SK] (SK a multiple of 4) in the 128 x 4 atom layout:
-    atom (rb, cb) at (rb * SK/4 + cb) * 512, code (r, c) at byte
-    16 * (r % 32) + 4 * ((r % 128) // 32) + c % 4 inside it."""
-    R, SK = codes.shape
-    assert SK % 4 == 0
-    RB = -(-R // 128)
-    pad = np.full((RB * 128, SK), one, dtype=np.uint8)
-    pad[:R] = codes
-    t = pad.reshape(RB, 4, 32, SK // 4, 4)          # rb, q, i, cb, j  (r = 128 rb + 32 q + i)
-    return np.ascontiguousarray(t.transpose(0, 3, 2, 1, 4)).reshape(-1)  # rb, cb, i, q, j
-
-
-def pack_e2m1(codes):
-    """[R, K] codes (one per byte, low nibble) -> [R, K/2], element 2i in the low nibble."""
-    c = codes.astype(np.uint8) & 0xF
-    return np.ascontiguousarray(c[:, 0::2] | (c[:, 1::2] << 4))
-
-
 def device_operands(prob):
-    a = inputs.bits(prob.A)                    # [M, K] codes
-    b = inputs.bits(prob.B).T                  # [N, K]: column-major B
-    sa, sb, scale, block = prob.block_scales
-    if prob.a_dtype == "e2m1":
-        a, b = pack_e2m1(a), pack_e2m1(b)
-    SFA = blocked(inputs.bits(sa), ONE[scale])
-    SFB = blocked(np.ascontiguousarray(inputs.bits(sb).T), ONE[scale])
     dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
-    return dev(a), dev(b), dev(SFA), dev(SFB)
+    return tuple(dev(x) for x in inputs.block_scaled_storage(prob))
 
 
 def run_scaled(prob, epilogue="linear", C=None, bias=None):

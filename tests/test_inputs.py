@@ -155,3 +155,22 @@ def test_integer_problems_are_exact_in_fp32():
                           aux_op=p.aux_op)
         assert all(Fraction(float(x)) == y for x, y in zip(got.ravel(), want.ravel()))
         assert max(abs(float(y)) for y in want.ravel()) < 2 ** 23
+
+
+def test_scale_atoms_and_fp4_packing_place_every_code():
+    """The blocked scale layout and the fp4 packing, checked element by
+    element against their definitions (storage only: no arithmetic)."""
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 255, size=(200, 12)).astype(np.uint8)
+    at = I.scale_atoms(codes, 0x7F)
+    assert at.size == 2 * 3 * 512
+    for r in range(256):
+        for c in range(12):
+            off = (r // 128 * 3 + c // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + c % 4
+            assert at[off] == (codes[r, c] if r < 200 else 0x7F)
+    q = rng.integers(0, 16, size=(3, 10)).astype(np.uint8)
+    pk = I.pack_e2m1(q)
+    assert pk.shape == (3, 5)
+    assert np.array_equal(pk & 0xF, q[:, 0::2]) and np.array_equal(pk >> 4, q[:, 1::2])
+    with pytest.raises(ValueError):
+        I.scale_atoms(codes[:, :6], 0x7F)
