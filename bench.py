@@ -444,7 +444,7 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_rd = (torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
                 if args.flush == "write+read" else None)
-    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def l2_flush():
         flush.zero_()
