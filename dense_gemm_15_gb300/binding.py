@@ -25,7 +25,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_
     ERR_DEVICE_FAULT, ERR_NO_DEVICE, ERR_BAD_PLAN = range(10)
 OPT_SCHEDULE, OPT_SPLITS, OPT_CTA_GROUP, OPT_TILE_N, OPT_RASTER, OPT_GRID, \
     OPT_TIMEOUT_US, OPT_FAULT_SKIP_FLAG, OPT_SK_DP_WAVES, OPT_TRACE_ITEMS, OPT_SWAP_AB, \
-    OPT_SPLITK_INLINE = range(12)
+    OPT_SPLITK_INLINE, OPT_L2_HINTS = range(13)
 SCHED_AUTO, SCHED_DP, SCHED_SK, SCHED_SPLIT = range(4)
 
 DTYPES = {"f16": F16, "bf16": BF16, "f32": F32, "e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1}

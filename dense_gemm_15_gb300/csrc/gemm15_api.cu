@@ -40,6 +40,7 @@ struct Options {
     int trace_items = 0;
     int swap_ab = 0;  // 0 automatic, 1 never, 2 always (dense problems)
     int splitk_inline = 0;  // split-K reduced by the last split: 0 automatic, 1 never, 2 always
+    int l2_hints = 0;       // operand L2 policies: 0 none, 1 A evict-last, 2 and B evict-first
 };
 
 // Kernel choice fixed by gemm_plan_autotune for one problem shape.
@@ -781,6 +782,7 @@ gemm15_status_t run_dense(gemm15_plan* plan, const Prob& p, float alpha, float b
     gp.epoch = ++plan->epoch == 0 ? ++plan->epoch : plan->epoch;
     gp.timeout_ns = static_cast<uint64_t>(plan->opt.timeout_us) * 1000ull;
     gp.fault_skip_flag = plan->opt.fault_skip_flag;
+    gp.l2_hints = plan->opt.l2_hints;
     st = attach_trace(plan, gp, d.grid, s);
     if (st != GEMM15_OK) return st;
     if (launch_kernel(plan->elem, d.bn, d.cg, gp, d.grid, s) != cudaSuccess) return GEMM15_ERR_CUDA;
@@ -1597,6 +1599,10 @@ gemm15_status_t gemm_plan_set_option(gemm15_plan_t plan, gemm15_option_t option,
         case GEMM15_OPT_SPLITK_INLINE:
             if (v < 0 || v > 2) return GEMM15_ERR_INVALID_ARG;
             o.splitk_inline = static_cast<int>(v);
+            return GEMM15_OK;
+        case GEMM15_OPT_L2_HINTS:
+            if (v < 0 || v > 2) return GEMM15_ERR_INVALID_ARG;
+            o.l2_hints = static_cast<int>(v);
             return GEMM15_OK;
         case GEMM15_OPT_FAULT_SKIP_FLAG:
             if (v < -1 || v > 100000) return GEMM15_ERR_INVALID_ARG;

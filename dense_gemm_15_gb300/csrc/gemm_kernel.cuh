@@ -620,6 +620,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_prefetch_desc(&p.tmA);
                 tma_prefetch_desc(&p.tmB);
             }
+            // the raster band's A rows are read by every wave of the band: keep
+            // them in L2 (evict-last) when asked; B then streams (evict-first)
+            const uint64_t pol_a = p.l2_hints >= 1 ? l2_policy_evict_last() : 0ull;
+            const uint64_t pol_b = p.l2_hints >= 2 ? l2_policy_evict_first() : 0ull;
             SchedState st;
             sched_init(p, un, st);
             Work w;
@@ -672,23 +676,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t dB = sB + s * TR::B_STAGE;
                     // K coordinate in tensor-map units: elements, or bytes for packed fp4
                     const int32_t k0 = kb * (TR::FP4 ? 128 : TR::BK);
-                    auto load = [&](uint32_t dst, const CUtensorMap* t, int32_t x, int32_t y) {
-                        if constexpr (CG == 2) tma_load_2d_pair(dst, t, fb, x, y);
-                        else tma_load_2d(dst, t, fb, x, y);
+                    // operand loads, with an L2 policy when asked (pol 0 = none)
+                    auto load = [&](uint32_t dst, const CUtensorMap* t, int32_t x, int32_t y, uint64_t pol) {
+                        if constexpr (CG == 2) {
+                            if (pol) tma_load_2d_pair_hint(dst, t, fb, x, y, pol);
+                            else tma_load_2d_pair(dst, t, fb, x, y);
+                        } else {
+                            if (pol) tma_load_2d_hint(dst, t, fb, x, y, pol);
+                            else tma_load_2d(dst, t, fb, x, y);
+                        }
                     };
                     if (p.a_kmajor) {
-                        load(dA, tA, k0, m0);
+                        load(dA, tA, k0, m0, pol_a);
                     } else {
                         constexpr int AW = 128 / TR::ESIZE;  // M elements per 128-byte row
 #pragma unroll
-                        for (int j = 0; j < TILE_M / AW; ++j) load(dA + j * AW * 128, tA, m0 + j * AW, k0);
+                        for (int j = 0; j < TILE_M / AW; ++j) load(dA + j * AW * 128, tA, m0 + j * AW, k0, pol_a);
                     }
                     if (p.b_kmajor) {
-                        load(dB, tB, k0, n0);
+                        load(dB, tB, k0, n0, pol_b);
                     } else {
                         constexpr int BW = 128 / TR::ESIZE;  // N elements per 128-byte row
 #pragma unroll
-                        for (int j = 0; j < TR::B_COLS / BW; ++j) load(dB + j * BW * 128, tB, n0 + j * BW, k0);
+                        for (int j = 0; j < TR::B_COLS / BW; ++j) load(dB + j * BW * 128, tB, n0 + j * BW, k0, pol_b);
                     }
                     ++n_issued;
                 }

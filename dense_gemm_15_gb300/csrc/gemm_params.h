@@ -56,6 +56,8 @@ struct GemmParams {
     int64_t sk_units;                 // SK: (tiles - dp_tiles) * k_blocks
     int32_t sk_partials_only;         // SK partition whose every piece leaves a partial tile
                                       // for the reduction kernel (balanced split-K)
+    int32_t l2_hints;                 // operand loads: 0 default, 1 A evict-last, 2 A
+                                      // evict-last and B evict-first
     int32_t splitk_inline;            // SPLIT: the split that finishes a tile last adds the
                                       // partials and writes it (no reduction kernel); the
                                       // arrival counters are 64-bit words in `flags`

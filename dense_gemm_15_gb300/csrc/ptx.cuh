@@ -138,6 +138,23 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// 2-D tiled load of an SM pair with an L2 cache policy (see tma_load_2d_pair).
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap, uint32_t bar,
+                                                      int32_t x, int32_t y, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
+// L2 cache policy that keeps the lines it touches longest (data reused later).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // L2 cache policy that evicts the lines it touches first (data used once).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;

@@ -279,12 +279,15 @@ typedef enum {
                                       or 128 x 128 single-SM tiles and stores the
                                       tile transposed; GEMM15_OPT_TILE_N and
                                       GEMM15_OPT_CTA_GROUP do not apply to it */
-    GEMM15_OPT_SPLITK_INLINE = 11  /* split-K: 0 auto (when a tile's partials total at
+    GEMM15_OPT_SPLITK_INLINE = 11, /* split-K: 0 auto (when a tile's partials total at
                                       most 256 KiB), 1 never, 2 always: the split that
                                       finishes a tile last (a per-tile arrival
                                       counter) adds all partials in split order and
                                       writes the tile, instead of a separate
                                       reduction kernel; no CTA waits for another */
+    GEMM15_OPT_L2_HINTS = 12       /* L2 policies of the operand loads: 0 none, 1 A
+                                      (the rows a raster band shares) evict-last,
+                                      2 also B evict-first */
 } gemm15_option_t;
 
 /* Sets an option on the plan; INVALID_ARG for unknown options or values. */
