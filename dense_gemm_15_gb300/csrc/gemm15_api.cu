@@ -1452,7 +1452,10 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (order_after_previous(plan, s) != GEMM15_OK) return GEMM15_ERR_CUDA;
 
-    constexpr int BN = 256;
+    // tile width: 128 x 128 tiles keep two accumulators (epilogue overlapped
+    // with the next tile's mainloop) and a deeper ring; 128 x 256 tiles halve
+    // the A traffic per FLOP but have one accumulator
+    const int BN = plan->opt.tile_n == 256 ? 256 : 128;
     Decision d;
     d.cg = 1;
     d.bn = BN;
@@ -1525,16 +1528,26 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     gemm15_status_t st = attach_trace(plan, gp, d.grid, s);
     if (st != GEMM15_OK) return st;
     cudaError_t e;
-    if (sf == SF_MXF8)
-        e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, BN, 1, SF_MXF8>(gp, d.grid, s)
-                                    : launch_gemm<ELEM_E5M2, BN, 1, SF_MXF8>(gp, d.grid, s);
-    else if (sf == SF_MXF4)
-        e = launch_gemm<ELEM_E2M1, BN, 1, SF_MXF4>(gp, d.grid, s);
-    else
-        e = launch_gemm<ELEM_E2M1, BN, 1, SF_NVF4>(gp, d.grid, s);
+    if (BN == 256) {
+        if (sf == SF_MXF8)
+            e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, 256, 1, SF_MXF8>(gp, d.grid, s)
+                                        : launch_gemm<ELEM_E5M2, 256, 1, SF_MXF8>(gp, d.grid, s);
+        else if (sf == SF_MXF4)
+            e = launch_gemm<ELEM_E2M1, 256, 1, SF_MXF4>(gp, d.grid, s);
+        else
+            e = launch_gemm<ELEM_E2M1, 256, 1, SF_NVF4>(gp, d.grid, s);
+    } else {
+        if (sf == SF_MXF8)
+            e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, 128, 1, SF_MXF8>(gp, d.grid, s)
+                                        : launch_gemm<ELEM_E5M2, 128, 1, SF_MXF8>(gp, d.grid, s);
+        else if (sf == SF_MXF4)
+            e = launch_gemm<ELEM_E2M1, 128, 1, SF_MXF4>(gp, d.grid, s);
+        else
+            e = launch_gemm<ELEM_E2M1, 128, 1, SF_NVF4>(gp, d.grid, s);
+    }
     if (e != cudaSuccess) return GEMM15_ERR_CUDA;
     record_config(plan, d, 1);
-    plan->last.stages = gemm_scaled_stages(sf);
+    plan->last.stages = gemm_scaled_stages(sf, BN);
     return mark_done(plan, s);
 }
 

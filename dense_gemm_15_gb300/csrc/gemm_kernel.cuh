@@ -61,8 +61,9 @@ struct Traits {
     static constexpr int SF_COLS = SF_APK * 4 * (1 + SF_BROWS);  // TMEM columns per stage
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE + SF_STAGE;
     // accumulators in TMEM: two (the epilogue of one tile overlaps the next
-    // tile's mainloop), or one when the scale factors need the other half
-    static constexpr int ACC_BUFS = SF == SF_NONE ? 2 : 1;
+    // tile's mainloop), or one when 256-wide block-scaled tiles leave the other
+    // half of the 512 columns to their scale factors
+    static constexpr int ACC_BUFS = (SF != SF_NONE && BN == 256) ? 1 : 2;
     // Epilogue staging: one 32 x 64 box per warp and output chunk of the tile
     // when that leaves room for six stages (the whole C tile is then fetched
     // as soon as the tile starts), else a ring of two boxes per warp (the rest
