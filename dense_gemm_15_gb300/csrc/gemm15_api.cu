@@ -1452,10 +1452,10 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (order_after_previous(plan, s) != GEMM15_OK) return GEMM15_ERR_CUDA;
 
-    // tile width: 128 x 128 tiles keep two accumulators (epilogue overlapped
-    // with the next tile's mainloop) and a deeper ring; 128 x 256 tiles halve
-    // the A traffic per FLOP but have one accumulator
-    const int BN = plan->opt.tile_n == 256 ? 256 : 128;
+    // tile width: 128 x 256 tiles (one accumulator, 3 stages) by default;
+    // 128 x 128 tiles keep two accumulators and a 5-stage ring but measured
+    // slower on GB300 (MXFP8 8192^3: 686 against 531 us; NVFP4: 508 against 381)
+    const int BN = plan->opt.tile_n == 128 ? 128 : 256;
     Decision d;
     d.cg = 1;
     d.bn = BN;

@@ -38,7 +38,7 @@ def run_scaled(prob, epilogue="linear", C=None, bias=None, tile_n=0):
     torch.cuda.synchronize()
     assert plan.query_error() == g.OK
     cfg = plan.last_config()
-    assert cfg["tile_n"] == (tile_n or 128) and cfg["launches"] == 1
+    assert cfg["tile_n"] == (tile_n or 256) and cfg["launches"] == 1
     return inputs.bits(D.cpu())
 
 
