@@ -393,7 +393,10 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const Option
                 set_tiles();
             }
         } else {
-            sched = (G / d.tiles >= 2) ? SCHED_SPLIT : SCHED_SK;
+            // swap-AB decode shapes: stream-K (one launch; measured equal or better
+            // than split-K on every Llama-70B layer at M 16 and 128: o_proj M 128
+            // 48 against 54 us, down M 128 97 against 104)
+            sched = (G / d.tiles >= 2 && !swap) ? SCHED_SPLIT : SCHED_SK;
             if (sched == SCHED_SPLIT && o.cta_group == 0 && cg == 1 && pair_ok && d.bn == 256 &&
                 M >= 512 && clusters > 0) {
                 // pair tiles share each B tile across the pair at the same
