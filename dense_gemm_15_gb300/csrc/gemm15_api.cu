@@ -175,9 +175,9 @@ CUtensorMapDataType tmap_type(int elem16_or_8) {
     }
 }
 
-// 2-D tiled tensor map with 128-byte swizzle and zero fill out of bounds.
+// 2-D tiled tensor map with 128-byte swizzle (or none) and zero fill out of bounds.
 bool make_tmap(CUtensorMap* map, int elem, const void* ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle = true) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -185,7 +185,8 @@ bool make_tmap(CUtensorMap* map, int elem, const void* ptr, uint64_t inner, uint
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, tmap_type(elem), 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1459,26 +1460,39 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     // 128 x 128 tiles keep two accumulators and a 5-stage ring but measured
     // slower on GB300 (MXFP8 8192^3: 686 against 531 us; NVFP4: 508 against 381)
     const int BN = plan->opt.tile_n == 128 ? 128 : 256;
+    const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
+    // SM-pair 256 x 256 tiles (each CTA stages its 128 rows of A and 128 columns
+    // of B, and all of B's scale atoms) unless one-SM tiles are asked for
+    const int clusters = std::min(pair_clusters(plan), G / 2);
+    const int cg = (BN == 256 && clusters > 0 && plan->opt.cta_group != 1) ? 2 : 1;
     Decision d;
-    d.cg = 1;
+    d.cg = cg;
     d.bn = BN;
     d.bk = static_cast<int>(bk);
     d.sched = SCHED_DP;
-    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M));
+    d.m_blocks = static_cast<int32_t>(cdiv(M, TILE_M * cg));
     d.n_blocks = static_cast<int32_t>(cdiv(N, BN));
     d.tiles = d.m_blocks * d.n_blocks;
     d.k_blocks = static_cast<int32_t>(K / bk);
-    const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
-    d.grid = static_cast<int>(std::min<int64_t>(G, d.tiles));
+    d.grid = cg == 2 ? 2 * static_cast<int>(std::min<int64_t>(clusters, d.tiles))
+                     : static_cast<int>(std::min<int64_t>(G, d.tiles));
     d.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, d.m_blocks)
-                                    : std::min<int32_t>(d.m_blocks, 16);
+                                    : std::min<int32_t>(d.m_blocks, cg == 2 ? 8 : 16);
 
     GemmParams gp;
     std::memset(&gp, 0, sizeof(gp));
     // operands as bytes: 128-byte boxes of K, 128 rows of A and 256 of B
     const uint64_t kbytes = static_cast<uint64_t>(fp4 ? K / 2 : K);
     bool ok = make_tmap(&gp.tmA, ELEM_E4M3, a->A, kbytes, M, lda_b, 128, TILE_M);
-    ok = ok && make_tmap(&gp.tmB, ELEM_E4M3, a->B, kbytes, N, ldb_b, 128, BN);
+    ok = ok && make_tmap(&gp.tmB, ELEM_E4M3, a->B, kbytes, N, ldb_b, 128, BN / cg);
+    // scale atoms as rows of 128 bytes (4 per atom), no swizzle: a box of one
+    // k-block's atoms (1, 2 or 4) lands in shared memory byte for byte
+    const int apk = sf == SF_MXF8 ? 1 : sf == SF_MXF4 ? 2 : 4;
+    const int64_t cb = K / block / 4;  // atoms per 128-row block
+    ok = ok && make_tmap(&gp.tmSFA, ELEM_E4M3, a->SFA, 128, static_cast<uint64_t>(cdiv(M, TILE_M) * cb * 4),
+                         128, 128, static_cast<uint32_t>(4 * apk), false);
+    ok = ok && make_tmap(&gp.tmSFB, ELEM_E4M3, a->SFB, 128, static_cast<uint64_t>(cdiv(N, TILE_M) * cb * 4),
+                         128, 128, static_cast<uint32_t>(4 * apk), false);
     Prob po{};
     po.M = M;
     po.N = N;
@@ -1507,10 +1521,7 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     gp.beta = a->beta;
     gp.act = static_cast<int>(plan->desc.epilogue);
     gp.bias = a->bias;
-    gp.sfa = static_cast<const uint8_t*>(a->SFA);
-    gp.sfb = static_cast<const uint8_t*>(a->SFB);
-    gp.sf_cb = static_cast<int32_t>(K / block / 4);
-    gp.sfb_rows = static_cast<int32_t>(cdiv(N, TILE_M));
+    gp.sf_cb = static_cast<int32_t>(cb);
     gp.a_kmajor = gp.b_kmajor = 1;
     gp.a_lbo = gp.b_lbo = 16;
     gp.a_sbo = gp.b_sbo = 1024;
@@ -1521,7 +1532,7 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     // 29-30 and 4-5) are set per MMA by the kernel
     const uint32_t fmt = plan->elem == ELEM_E4M3 ? 0u : 1u;
     gp.idesc = (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-               ((sf == SF_NVF4 ? 0u : 1u) << 23) | (static_cast<uint32_t>(TILE_M >> 4) << 24);
+               ((sf == SF_NVF4 ? 0u : 1u) << 23) | (static_cast<uint32_t>((TILE_M * cg) >> 4) << 24);
     gp.ws = plan->d_ws;
     gp.flags = plan->d_flags;
     gp.status = plan->d_status;
@@ -1531,7 +1542,15 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     gemm15_status_t st = attach_trace(plan, gp, d.grid, s);
     if (st != GEMM15_OK) return st;
     cudaError_t e;
-    if (BN == 256) {
+    if (cg == 2) {
+        if (sf == SF_MXF8)
+            e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, 256, 2, SF_MXF8>(gp, d.grid, s)
+                                        : launch_gemm<ELEM_E5M2, 256, 2, SF_MXF8>(gp, d.grid, s);
+        else if (sf == SF_MXF4)
+            e = launch_gemm<ELEM_E2M1, 256, 2, SF_MXF4>(gp, d.grid, s);
+        else
+            e = launch_gemm<ELEM_E2M1, 256, 2, SF_NVF4>(gp, d.grid, s);
+    } else if (BN == 256) {
         if (sf == SF_MXF8)
             e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, 256, 1, SF_MXF8>(gp, d.grid, s)
                                         : launch_gemm<ELEM_E5M2, 256, 1, SF_MXF8>(gp, d.grid, s);
@@ -1550,7 +1569,7 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     }
     if (e != cudaSuccess) return GEMM15_ERR_CUDA;
     record_config(plan, d, 1);
-    plan->last.stages = gemm_scaled_stages(sf, BN);
+    plan->last.stages = gemm_scaled_stages(sf, BN, cg);
     return mark_done(plan, s);
 }
 

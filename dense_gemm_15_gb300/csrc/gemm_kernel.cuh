@@ -80,7 +80,7 @@ struct Traits {
     // an N-major B stage is whole 128-byte swizzle rows of N
     static_assert(B_COLS * ESIZE >= 128 && (B_COLS * ESIZE) % 128 == 0, "B columns per CTA");
     static_assert(EPI_BUFS <= 8, "C barrier parity bits");
-    static_assert(SF == SF_NONE || (CG == 1 && BN % 128 == 0), "block-scaled tiles");
+    static_assert(SF == SF_NONE || (BN % 128 == 0 && (CG == 1 || BN == 256)), "block-scaled tiles");
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SF = OFF_B + STAGES * B_STAGE;
@@ -621,6 +621,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_prefetch_desc(&p.tmA);
                 tma_prefetch_desc(&p.tmB);
             }
+            if constexpr (SF != SF_NONE) {
+                tma_prefetch_desc(&p.tmSFA);
+                tma_prefetch_desc(&p.tmSFB);
+            }
             // the raster band's A rows are read by every wave of the band: keep
             // them in L2 (evict-last) when asked; B then streams (evict-first)
             const uint64_t pol_a = p.l2_hints >= 1 ? l2_policy_evict_last() : 0ull;
@@ -657,19 +661,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint32_t fb = full_bar(s);
                     if constexpr (CG == 2) fb = map_cluster(fb, 0);
                     if constexpr (SF != SF_NONE) {
-                        // the stage's scale atoms: A's 128 rows, then each 128-row
-                        // block of B that exists (absent ones are not read; their
-                        // columns lie past N)
-                        const int32_t rb0 = w.n_blk * TR::SF_BROWS;
-                        const int32_t nb_live = min(TR::SF_BROWS, p.sfb_rows - rb0);
-                        const uint32_t atoms = TR::SF_APK * 512u;
-                        mbar_arrive_expect_tx(full_bar(s), TR::A_STAGE + TR::B_STAGE + atoms * (1 + nb_live));
+                        // the stage's scale atoms (tensor maps of 128-byte rows, 4 per
+                        // atom): this CTA's 128 rows of A, then every 128-row block of
+                        // the tile's B (each CTA of a pair holds all of B's scales);
+                        // blocks past M or N read as zeros, their outputs are not stored
+                        constexpr uint32_t ATOMS = TR::SF_APK * 512u;
+                        if (leader)
+                            mbar_arrive_expect_tx(full_bar(s), CG * (TR::A_STAGE + TR::B_STAGE + ATOMS * (1 + TR::SF_BROWS)));
                         const uint32_t dS = sSF + s * TR::SF_STAGE;
-                        const int64_t cb0 = static_cast<int64_t>(kb) * TR::SF_APK;
-                        bulk_g2s(dS, p.sfa + (static_cast<int64_t>(w.m_blk) * p.sf_cb + cb0) * 512, atoms, fb);
-                        for (int32_t nb = 0; nb < nb_live; ++nb)
-                            bulk_g2s(dS + (1 + nb) * atoms, p.sfb + (static_cast<int64_t>(rb0 + nb) * p.sf_cb + cb0) * 512,
-                                     atoms, fb);
+                        const int32_t cb0 = kb * TR::SF_APK;
+                        const int32_t rba = w.m_blk * CG + un.rank;
+                        auto load_sf = [&](uint32_t dst, const CUtensorMap* t, int32_t row) {
+                            if constexpr (CG == 2) tma_load_2d_pair(dst, t, fb, 0, row);
+                            else tma_load_2d(dst, t, fb, 0, row);
+                        };
+                        load_sf(dS, &p.tmSFA, (rba * p.sf_cb + cb0) * 4);
+#pragma unroll
+                        for (int nb = 0; nb < TR::SF_BROWS; ++nb)
+                            load_sf(dS + (1 + nb) * ATOMS, &p.tmSFB, ((w.n_blk * TR::SF_BROWS + nb) * p.sf_cb + cb0) * 4);
                     } else if (leader) {
                         mbar_arrive_expect_tx(full_bar(s), CG * TR::STAGE_BYTES);
                     }
@@ -778,11 +787,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t dS = sSF + s * TR::SF_STAGE;
 #pragma unroll
                         for (int j = 0; j < TR::SF_APK; ++j) {
-                            tmem_cp_32x128b_x4(sf_t + 4 * j, sdesc_atom(dS + 512 * j));
+                            tmem_cp_32x128b_x4<CG>(sf_t + 4 * j, sdesc_atom(dS + 512 * j));
 #pragma unroll
                             for (int nb = 0; nb < TR::SF_BROWS; ++nb)
-                                tmem_cp_32x128b_x4(sfb_t + 4 * TR::SF_BROWS * j + 4 * nb,
-                                                   sdesc_atom(dS + (1 + nb) * 512 * TR::SF_APK + 512 * j));
+                                tmem_cp_32x128b_x4<CG>(sfb_t + 4 * TR::SF_BROWS * j + 4 * nb,
+                                                       sdesc_atom(dS + (1 + nb) * 512 * TR::SF_APK + 512 * j));
                         }
 #pragma unroll
                         for (int k = 0; k < TR::KSTEPS; ++k) {
@@ -794,7 +803,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             else if constexpr (SF == SF_MXF4) { atom = k >> 1; id = 2 * (k & 1); }
                             else { atom = k; }
                             const uint32_t idesc = p.idesc | (id << 29) | (id << 4);
-                            umma_block_scaled<SF>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
+                            umma_block_scaled<CG, SF>(d_tmem, sdesc_at(adesc0, a_addr + k * p.a_kstep),
                                                   sdesc_at(bdesc0, b_addr + k * p.b_kstep), idesc,
                                                   sf_t + 4 * atom, sfb_t + 4 * TR::SF_BROWS * atom,
                                                   (kb > w.kb0 || k > 0) ? 1u : 0u);

@@ -77,10 +77,10 @@ struct GemmParams {
                                       // lives at C / D / Z + c * ld + r
     // block-scaled operands: scale factors in the 128 x 4 atom layout (512-byte
     // atoms, one per 128 rows and 4 consecutive scales along K; atom (rb, cb)
-    // at (rb * sf_cb + cb) * 512); sfb_rows = number of 128-row blocks of B
-    const uint8_t* sfa;
-    const uint8_t* sfb;
-    int32_t sf_cb, sfb_rows;
+    // at (rb * sf_cb + cb) * 512), read through 2-D tensor maps of 128-byte
+    // rows (an atom is 4 rows)
+    CUtensorMap tmSFA, tmSFB;
+    int32_t sf_cb;
     // operand layouts in shared memory (bytes) and the MMA instruction descriptor
     uint32_t a_kmajor, b_kmajor;
     uint32_t a_lbo, a_sbo, a_kstep;

@@ -10,7 +10,8 @@ namespace g15 {
 
 // Persistent tcgen05 GEMM: one-SM tiles of 128 x BN (CG = 1, BN = 64, 128 or
 // 256) or SM-pair tiles of 256 x BN (CG = 2, clusters of two CTAs; grid even);
-// SF selects a block-scaled MMA kind (one-SM tiles, BN = 128 or 256).
+// SF selects a block-scaled MMA kind (one-SM tiles of BN = 128 or 256, or
+// SM-pair 256 x 256 tiles).
 template <int ELEM, int BN, int CG = 1, int SF = SF_NONE>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
@@ -26,8 +27,9 @@ cudaError_t launch_reduce(const ReduceParams& p, int grid, int groups, cudaStrea
 // Grid and warps per block of the reduction for its parameters.
 void reduce_shape(const ReduceParams& p, int num_sms, int* grid, int* groups);
 
-// Pipeline depth of the block-scaled kernel of a scale kind and tile width.
-int gemm_scaled_stages(int sf, int bn);
+// Pipeline depth of the block-scaled kernel of a scale kind, tile width and
+// CTA group.
+int gemm_scaled_stages(int sf, int bn, int cg);
 
 // Shared-memory bytes and pipeline depth of a GEMM instantiation.
 int gemm_smem_bytes(int elem, int bn, int cg);

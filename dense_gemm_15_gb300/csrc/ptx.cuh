@@ -297,11 +297,29 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
 // Block-scaled MMA (one CTA): D[tmem] (+)= (A x SFA) . (B x SFB), scale
 // factors read from TMEM at sfa / sfb, the scale-factor IDs (byte selectors)
 // in the instruction descriptor.
-template <int SFK>
+template <int CG, int SFK>
 __device__ __forceinline__ void umma_block_scaled(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                   uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                                   uint32_t accumulate) {
-    if constexpr (SFK == 1)
+    if constexpr (CG == 2 && SFK == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else if constexpr (CG == 2 && SFK == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else if constexpr (CG == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else if constexpr (SFK == 1)
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
@@ -323,9 +341,15 @@ __device__ __forceinline__ void umma_block_scaled(uint32_t d_tmem, uint64_t ades
 
 // Copies a 32-row x 16-byte block of shared memory (one 512-byte scale-factor
 // atom, described by `desc`) to TMEM at taddr: 4 columns of 32 lanes,
-// replicated to the four 32-lane quarters.
+// replicated to the four 32-lane quarters.  With CG = 2 (issued by the pair's
+// MMA thread) each CTA's block at that shared-memory address goes to its own
+// TMEM.
+template <int CG>
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // Shared-memory descriptor of a no-swizzle 32 x 16-byte block: 8-row core
@@ -337,15 +361,6 @@ __device__ __forceinline__ uint64_t sdesc_atom(uint32_t addr) {
     d |= static_cast<uint64_t>((128u >> 4) & 0x3FFF) << 32;
     d |= 1ull << 46;
     return d;
-}
-
-// Untiled bulk copy global -> this CTA's shared memory, completion on `bar`
-// (both addresses 16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
 }
 
 // Arrive once on `bar` (this CTA) when all prior tcgen05 async ops of the

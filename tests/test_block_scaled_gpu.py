@@ -22,12 +22,14 @@ def device_operands(prob):
     return tuple(dev(x) for x in inputs.block_scaled_storage(prob))
 
 
-def run_scaled(prob, epilogue="linear", C=None, bias=None, tile_n=0):
+def run_scaled(prob, epilogue="linear", C=None, bias=None, tile_n=0, cta_group=0):
     kind = g.SCALE_NV if prob.block_scales[2] == "e4m3" else g.SCALE_MX
     plan = g.Plan(prob.a_dtype, "bf16", epilogue=epilogue, layout_a=g.ROW_MAJOR,
                   layout_b=g.COL_MAJOR)
     if tile_n:
         plan.set(g.OPT_TILE_N, tile_n)
+    if cta_group:
+        plan.set(g.OPT_CTA_GROUP, cta_group)
     A, B, SFA, SFB = device_operands(prob)
     D = torch.full((prob.M, prob.N), float("nan"), dtype=torch.bfloat16, device="cuda")
     st = g.gemm_run_block_scaled(plan.handle, A, B, SFA, SFB, D, prob.M, prob.N, prob.K,
@@ -39,6 +41,8 @@ def run_scaled(prob, epilogue="linear", C=None, bias=None, tile_n=0):
     assert plan.query_error() == g.OK
     cfg = plan.last_config()
     assert cfg["tile_n"] == (tile_n or 256) and cfg["launches"] == 1
+    want_cg = 1 if tile_n == 128 else (cta_group or 2)
+    assert cfg["cta_group"] == want_cg and cfg["tile_m"] == 128 * want_cg
     return inputs.bits(D.cpu())
 
 
@@ -46,17 +50,21 @@ FORMATS = [("e4m3", 32, "ue8m0"), ("e5m2", 32, "ue8m0"), ("e2m1", 32, "ue8m0"),
            ("e2m1", 16, "e4m3")]
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+TILES = [(128, 1), (256, 1), (256, 2)]  # (tile_n, cta_group): one-SM 128 x {128, 256}, pair 256 x 256
+
+
+@pytest.mark.parametrize("tile_n,cta_group", TILES)
 @pytest.mark.parametrize("elem,block,scale", FORMATS)
-@pytest.mark.parametrize("shape", [(256, 512, 1024), (200, 392, 512), (130, 296, 1536)])
-def test_block_scaled_matches_oracle(elem, block, scale, shape, tile_n):
+@pytest.mark.parametrize("shape", [(256, 512, 1024), (200, 392, 512), (130, 296, 1536),
+                                   (520, 264, 768)])
+def test_block_scaled_matches_oracle(elem, block, scale, shape, tile_n, cta_group):
     """N(0,1) values with a per-block spread of 2^U{-8..8}, quantised by the
     format's own rules; ragged M and N (the second 128-row block of B's
     scales is absent for N = 296 in the last tile)."""
     M, N, K = shape
     prob = inputs.block_scaled_problem(M, N, K, elem=elem, block=block, scale=scale,
                                        alpha=0.75 if scale == "e4m3" else 1.0)
-    assert_matches_oracle(prob, run_scaled(prob, tile_n=tile_n))
+    assert_matches_oracle(prob, run_scaled(prob, tile_n=tile_n, cta_group=cta_group))
 
 
 @pytest.mark.parametrize("elem,block,scale", FORMATS)
@@ -96,13 +104,13 @@ def _exact_problem(elem, block, scale, M, N, K, seed=0):
     return p
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n,cta_group", TILES)
 @pytest.mark.parametrize("elem,block,scale", FORMATS)
-def test_block_scaled_bit_exact(elem, block, scale, tile_n):
+def test_block_scaled_bit_exact(elem, block, scale, tile_n, cta_group):
     """392 x 520 x 2048 (ragged in M and N, more k-blocks than pipeline
     stages): equal to the oracle's rounded result bit for bit."""
     prob = _exact_problem(elem, block, scale, 392, 520, 2048)
-    d = run_scaled(prob, tile_n=tile_n)
+    d = run_scaled(prob, tile_n=tile_n, cta_group=cta_group)
     import oracle
     a, b = inputs.bits(prob.A), inputs.bits(prob.B)
     sa, sb, sc, blk = prob.block_scales
