@@ -779,36 +779,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t a_addr = sA + s * TR::A_STAGE;
                     const uint32_t b_addr = sB + s * TR::B_STAGE;
                     if constexpr (SF != SF_NONE) {
-                        // a stage's scale atoms go to its TMEM slot (after the
+                        // the stage's scale atoms into its TMEM slot (after the
                         // accumulator): A's atom j at +4j, B's atom j of row block
-                        // nb at +4*APK + 4*SF_BROWS*j + 4*nb.  The copy of the next
-                        // k-block's atoms is issued before this k-block's MMAs, so
-                        // that no MMA waits behind the copy of its own scales.
-                        auto copy_scales = [&](int st) {
-                            const uint32_t t = tmem_base + ACC_BUFS * BN + st * TR::SF_COLS;
-                            const uint32_t dS = sSF + st * TR::SF_STAGE;
-#pragma unroll
-                            for (int j = 0; j < TR::SF_APK; ++j) {
-                                tmem_cp_32x128b_x4<CG>(t + 4 * j, sdesc_atom(dS + 512 * j));
-#pragma unroll
-                                for (int nb = 0; nb < TR::SF_BROWS; ++nb)
-                                    tmem_cp_32x128b_x4<CG>(t + 4 * TR::SF_APK + 4 * TR::SF_BROWS * j + 4 * nb,
-                                                           sdesc_atom(dS + (1 + nb) * 512 * TR::SF_APK + 512 * j));
-                            }
-                        };
-                        if (kb == w.kb0) copy_scales(s);
-                        if (kb + 1 < w.kb1) {
-                            const uint32_t n1 = n_used + 1;
-                            const int s1 = static_cast<int>(n1 % STAGES);
-                            if (!wait_bar(ctl, full_bar(s1), (n1 / STAGES) & 1u)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            copy_scales(s1);
-                        }
+                        // nb at +4*APK + 4*SF_BROWS*j + 4*nb
                         const uint32_t sf_t = tmem_base + ACC_BUFS * BN + s * TR::SF_COLS;
                         const uint32_t sfb_t = sf_t + 4 * TR::SF_APK;
+                        const uint32_t dS = sSF + s * TR::SF_STAGE;
+#pragma unroll
+                        for (int j = 0; j < TR::SF_APK; ++j) {
+                            tmem_cp_32x128b_x4<CG>(sf_t + 4 * j, sdesc_atom(dS + 512 * j));
+#pragma unroll
+                            for (int nb = 0; nb < TR::SF_BROWS; ++nb)
+                                tmem_cp_32x128b_x4<CG>(sfb_t + 4 * TR::SF_BROWS * j + 4 * nb,
+                                                       sdesc_atom(dS + (1 + nb) * 512 * TR::SF_APK + 512 * j));
+                        }
 #pragma unroll
                         for (int k = 0; k < TR::KSTEPS; ++k) {
                             // MXFP8: one scale per row and MMA, byte k of atom 0;
