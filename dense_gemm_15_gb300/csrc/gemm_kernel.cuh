@@ -982,15 +982,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (preload && rows_live) {
                 for (int c = 0; c < nch; ++c) {
                     const int32_t col0 = c * EPI_COLS;
+                    // float4 groups of the chunk inside N (partials past N are never written)
+                    const int nq = min(16, (N - (n0 + col0) + 3) / 4);
                     // the whole chunk of the first peer in flight at once (16 loads)
                     float4 ps[16];
                     const float4* src0 = peer_src(w, pb0, col0);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) ps[i] = ld_global_cg_hint(src0 + 32 * i, pol_once);
+                    for (int i = 0; i < 16; ++i)
+                        ps[i] = i < nq ? ld_global_cg_hint(src0 + 32 * i, pol_once) : make_float4(0.f, 0.f, 0.f, 0.f);
                     for (int32_t pb = next_peer(w, pb0 + 1); pb >= 0; pb = next_peer(w, pb + 1)) {
                         const float4* src = peer_src(w, pb, col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
+                            if (i >= nq) continue;
                             const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
                             ps[i].x += t.x;
                             ps[i].y += t.y;
@@ -1034,6 +1038,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
             for (int c = 0; ok && rows_live && c < nch; ++c) {
                 const int32_t col0 = c * EPI_COLS;
+                // float4 groups of the chunk inside N: partial tiles are written
+                // and read only there (a swap-AB tile of a 16-token problem has 4)
+                const int nq = min(16, (N - (n0 + col0) + 3) / 4);
                 const uint32_t b = WHOLE ? static_cast<uint32_t>(c) : (n_chunk & 1u);
                 const uint32_t buf = ebuf0 + b * EPI_BUF_BYTES;
                 // bias by output column: lane j < 8 fetches columns 8j..8j+7 of the chunk
@@ -1069,6 +1076,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                 p.ws + static_cast<size_t>(slot0 + sp) * TILE_M * BN) + peer_off(col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
+                            if (i >= nq) continue;
                             const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
                             v[4 * i + 0] += t.x;
                             v[4 * i + 1] += t.y;
@@ -1104,6 +1112,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const float4* src = peer_src(w, pb, col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
+                            if (i >= nq) continue;
                             const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
                             v[4 * i + 0] += t.x;
                             v[4 * i + 1] += t.y;
@@ -1120,13 +1129,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         dst += peer_off(col0);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            __stcg(dst + 32 * i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                            if (i < nq)
+                                __stcg(dst + 32 * i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
                     } else {
                         // split-K partials: row-major tiles, as the reduction kernel reads them
                         dst += (static_cast<size_t>(q * 32 + lane) * BN + col0) / 4;
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                            if (i < nq)
+                                __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
                     }
                     continue;
                 }
