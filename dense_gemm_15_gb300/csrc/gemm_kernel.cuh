@@ -1122,6 +1122,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 }  // from TMEM
+                if (tr && w.kind == WK_OWNER && c == 0) tr[7] = globaltimer_ns();  // peers added
                 if (to_ws) {
                     float4* dst = reinterpret_cast<float4*>(p.ws + static_cast<size_t>(w.slot) * TILE_M * BN);
                     if (w.kind == WK_PEER || p.splitk_inline) {

@@ -108,7 +108,8 @@ constexpr int TRACE_WORDS = 8;
 // epilogue thread, [4] 1 if thread 0 saw the first epilogue thread's
 // pre-barrier write after the barrier.  item record: [0] tile | kind << 32, [1] kb0 | kb1 << 32,
 // [2] MMA start, [3] MMA issue done, [4] accumulator ready (epilogue),
-// [5] chunk loop start, [6] epilogue done, [7] partial published.
+// [5] chunk loop start, [6] epilogue done, [7] partial published (stream-K
+// peer) or the peers' partials of the first chunk added (owner).
 
 struct ReduceParams {
     const float* ws;

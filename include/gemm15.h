@@ -357,7 +357,8 @@ gemm15_status_t gemm_plan_forget_tuning(gemm15_plan_t plan);
  * the first epilogue thread wrote before it.  Item: tile | kind << 32 (0 whole tile, 1
  * stream-K peer part, 2 stream-K owner part, 3 split-K part), kb0 | kb1 << 32,
  * MMA start, MMA issued, accumulator ready, epilogue chunks start, epilogue
- * done, partial published; unused items are zero.  INVALID_ARG if tracing is
+ * done, partial published (stream-K peer part) or the peers' partials of the
+ * first chunk added (owner part); unused items are zero.  INVALID_ARG if tracing is
  * off or `capacity` is too small (*ctas and *items are still set). */
 gemm15_status_t gemm_plan_trace(gemm15_plan_t plan, void* out, int64_t capacity, int32_t* ctas,
                                 int32_t* items);
