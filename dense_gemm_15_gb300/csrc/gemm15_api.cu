@@ -673,8 +673,15 @@ const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& key, bool has_c) 
     GemmParams& gp = e.gp;
     std::memset(&gp, 0, sizeof(gp));
     if (!operand_maps(plan, p, d.bn / d.cg, &gp.tmA, &gp.tmB)) return nullptr;
-    // a transposed output is read and written element-wise (no tensor maps)
+    // a transposed output: C, Z and Y element-wise; D through a tensor map of
+    // its storage seen transposed (inner dimension = the computed rows), stored
+    // from 32 x 64 boxes that the epilogue fills transposed
     if (!p.out_trans && !output_maps(plan, p, has_c, &gp.tmC, &gp.tmD)) return nullptr;
+    if (p.out_trans) {
+        if (!make_tmap(&gp.tmD, plan->out_elem, p.D, p.M, p.N, p.ldd * 2, 32, EPI_COLS, false))
+            return nullptr;
+        gp.out_tma = 1;
+    }
     gp.out_trans = p.out_trans ? 1 : 0;
     gp.D = p.D;
     gp.ldd = p.ldd;

@@ -1190,7 +1190,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             v[i] = aux_apply(v[i], z, p.aux_op);
                         }
                     }
-                    if (live) {
+                    if (p.out_tma) {
+                        // the chunk transposed into the warp's staging box (row i = computed
+                        // column i: this warp's 32 computed rows, 64 bytes; conflict-free),
+                        // then one TMA store through the transposed tensor map, which
+                        // clips rows and columns past the edges
+#pragma unroll
+                        for (int i = 0; i < 64; i += 2) {
+                            const uint32_t pr = pack2<ELEM>(v[i], v[i + 1]);
+                            st_shared_u16(buf + i * 64 + lane * 2, static_cast<uint16_t>(pr));
+                            st_shared_u16(buf + (i + 1) * 64 + lane * 2, static_cast<uint16_t>(pr >> 16));
+                        }
+                        fence_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d_hint(tD, buf, row0, n0 + col0, pol_once);
+                            bulk_commit();
+                        }
+                        ++n_chunk;
+                        __syncwarp();
+                    } else if (live) {
                         uint16_t* db = reinterpret_cast<uint16_t*>(Dptr) + my_row;
 #pragma unroll
                         for (int i = 0; i < 64; i += 2) {

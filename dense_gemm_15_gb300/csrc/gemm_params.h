@@ -75,6 +75,8 @@ struct GemmParams {
     int32_t out_trans;                // 1: the computed tile is the transpose of the stored
                                       // one (swap-AB): element (r, c) of the computed output
                                       // lives at C / D / Z + c * ld + r
+    int32_t out_tma;                  // out_trans: tmD maps the stored D transposed (inner
+                                      // dimension = computed rows, 32 x 64 boxes, no swizzle)
     // block-scaled operands: scale factors in the 128 x 4 atom layout (512-byte
     // atoms, one per 128 rows and 4 consecutive scales along K; atom (rb, cb)
     // at (rb * sf_cb + cb) * 512), read through 2-D tensor maps of 128-byte
