@@ -95,9 +95,14 @@ struct gemm15_plan {
     cudaEvent_t done_ev = nullptr;
     cudaStream_t last_stream = nullptr;
     bool has_last = false;
-    // gemm_run_host: a second stream for the B copy, with fork / join events
+    // gemm_run_host: a second stream for the B copy, with fork / join events;
+    // for the column-chunked pipeline a stream for the D downloads and events
+    // per chunk (B chunk uploaded, D chunk computed)
     cudaStream_t copy_stream = nullptr;
     cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+    cudaStream_t d2h_stream = nullptr;
+    cudaEvent_t a_ev = nullptr, d2h_ev = nullptr;
+    cudaEvent_t up_ev[8] = {}, done_evs[8] = {};
     // launch parameters of recent dense problems (see LaunchCache)
     void* cache = nullptr;
 };
@@ -946,6 +951,13 @@ gemm15_status_t gemm_plan_destroy(gemm15_plan_t plan) {
     if (plan->fork_ev) cudaEventDestroy(plan->fork_ev);
     if (plan->join_ev) cudaEventDestroy(plan->join_ev);
     if (plan->copy_stream) cudaStreamDestroy(plan->copy_stream);
+    if (plan->d2h_stream) cudaStreamDestroy(plan->d2h_stream);
+    if (plan->a_ev) cudaEventDestroy(plan->a_ev);
+    if (plan->d2h_ev) cudaEventDestroy(plan->d2h_ev);
+    for (int i = 0; i < 8; ++i) {
+        if (plan->up_ev[i]) cudaEventDestroy(plan->up_ev[i]);
+        if (plan->done_evs[i]) cudaEventDestroy(plan->done_evs[i]);
+    }
     delete static_cast<LaunchCache*>(plan->cache);
     plan->magic = PLAN_DEAD;
     delete plan;
@@ -1172,6 +1184,79 @@ gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB
     void* dA = plan->d_host_path[0];
     void* dB = plan->d_host_path[1];
     void* dCD = plan->d_host_path[2];  // C is copied in and D overwrites it in place
+    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
+    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
+    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
+
+    // Large row-major problems: a pipeline over column chunks of B, C and D.
+    // The copy stream uploads A, then each chunk of B (and C) with a strided
+    // copy; `stream` computes chunk k once its columns are up; a third stream
+    // downloads chunk k of D while chunk k + 1 computes.
+    const int64_t min_cols = 2048;
+    int chunks = 1;
+    if (a_row && b_row && cd_row && K > 0 && bytes[1] + bytes[2] >= (static_cast<size_t>(64) << 20))
+        chunks = static_cast<int>(std::min<int64_t>(8, N / min_cols));
+    if (chunks > 1 && plan->elem != ELEM_E4M3) {
+        if (!plan->d2h_stream) {
+            if (cudaStreamCreateWithFlags(&plan->d2h_stream, cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&plan->a_ev, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&plan->d2h_ev, cudaEventDisableTiming) != cudaSuccess)
+                return GEMM15_ERR_CUDA;
+            for (int i = 0; i < 8; ++i)
+                if (cudaEventCreateWithFlags(&plan->up_ev[i], cudaEventDisableTiming) != cudaSuccess ||
+                    cudaEventCreateWithFlags(&plan->done_evs[i], cudaEventDisableTiming) != cudaSuccess)
+                    return GEMM15_ERR_CUDA;
+        }
+        // chunk widths: whole 256-column tiles, the last one takes the rest
+        const int64_t w = (N / chunks + 255) / 256 * 256;
+        const size_t ea = static_cast<size_t>(es), ed = static_cast<size_t>(eo);
+        if (cudaEventRecord(plan->fork_ev, s) != cudaSuccess ||
+            cudaStreamWaitEvent(plan->copy_stream, plan->fork_ev, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(plan->d2h_stream, plan->fork_ev, 0) != cudaSuccess ||
+            cudaMemcpyAsync(dA, hA, bytes[0], cudaMemcpyHostToDevice, plan->copy_stream) != cudaSuccess ||
+            cudaEventRecord(plan->a_ev, plan->copy_stream) != cudaSuccess ||
+            cudaStreamWaitEvent(s, plan->a_ev, 0) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        int nc = 0;
+        for (int64_t n0 = 0; n0 < N; n0 += w, ++nc) {
+            const int64_t cw = std::min<int64_t>(w, N - n0);
+            auto colp = [&](const void* base, size_t e) {
+                return static_cast<const uint8_t*>(base) + static_cast<size_t>(n0) * e;
+            };
+            if (cudaMemcpy2DAsync(const_cast<uint8_t*>(colp(dB, ea)), N * ea, colp(hB, ea), N * ea, cw * ea, K,
+                                  cudaMemcpyHostToDevice, plan->copy_stream) != cudaSuccess)
+                return GEMM15_ERR_CUDA;
+            if (beta != 0.0f &&
+                cudaMemcpy2DAsync(const_cast<uint8_t*>(colp(dCD, ed)), N * ed, colp(hC, ed), N * ed, cw * ed, M,
+                                  cudaMemcpyHostToDevice, plan->copy_stream) != cudaSuccess)
+                return GEMM15_ERR_CUDA;
+            if (cudaEventRecord(plan->up_ev[nc], plan->copy_stream) != cudaSuccess ||
+                cudaStreamWaitEvent(s, plan->up_ev[nc], 0) != cudaSuccess)
+                return GEMM15_ERR_CUDA;
+            void* dchunk = const_cast<uint8_t*>(colp(dCD, ed));
+            Prob p = normalise(plan, M, cw, K, dA, K, colp(dB, ea), N, dchunk, N, dchunk, N);
+            gemm15_status_t st = run_dense(plan, p, alpha, beta, nullptr, nullptr, s);
+            if (st != GEMM15_OK) return st;
+            if (cudaEventRecord(plan->done_evs[nc], s) != cudaSuccess ||
+                cudaStreamWaitEvent(plan->d2h_stream, plan->done_evs[nc], 0) != cudaSuccess ||
+                cudaMemcpy2DAsync(static_cast<uint8_t*>(hD) + static_cast<size_t>(n0) * ed, N * ed, dchunk,
+                                  N * ed, cw * ed, M, cudaMemcpyDeviceToHost, plan->d2h_stream) != cudaSuccess)
+                return GEMM15_ERR_CUDA;
+        }
+        if (cudaEventRecord(plan->d2h_ev, plan->d2h_stream) != cudaSuccess ||
+            cudaStreamWaitEvent(s, plan->d2h_ev, 0) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        int32_t status = 0;
+        if (cudaMemcpy(&status, plan->d_status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return GEMM15_ERR_CUDA;
+        if (status != 0) {
+            if (cudaMemset(plan->d_status, 0, sizeof(int32_t)) != cudaSuccess) return GEMM15_ERR_CUDA;
+            if (status < 0 || status > GEMM15_ERR_BAD_PLAN) return GEMM15_ERR_DEVICE_FAULT;
+        }
+        return static_cast<gemm15_status_t>(status);
+    }
+
     // B goes up on the plan's copy stream while A (and C) go up on `stream`
     if (K > 0) {
         if (cudaEventRecord(plan->fork_ev, s) != cudaSuccess ||
@@ -1195,9 +1280,6 @@ gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB
         sa = plan->d_scales;
         sb = plan->d_scales + 1;
     }
-    const bool a_row = plan->desc.layout_a == GEMM15_ROW_MAJOR;
-    const bool b_row = plan->desc.layout_b == GEMM15_ROW_MAJOR;
-    const bool cd_row = plan->desc.layout_cd == GEMM15_ROW_MAJOR;
     Prob p = normalise(plan, M, N, K, dA, a_row ? K : M, dB, b_row ? N : K, dCD, cd_row ? N : M,
                        dCD, cd_row ? N : M);
     gemm15_status_t st = run_dense(plan, p, alpha, beta, sa, sb, s);

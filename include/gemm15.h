@@ -197,9 +197,14 @@ gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* args, voi
 
 /* End-to-end variant for callers holding HOST buffers (packed layouts as in
  * gemm_run; pinned memory recommended).  Copies A, B (and C when beta != 0)
- * into plan-owned device buffers, runs the GEMM and copies D back, all on
- * `stream`, then synchronises the stream and returns the device status.
- * scale_a / scale_b are HOST floats here (1.0 for 16-bit plans). */
+ * into plan-owned device buffers, runs the GEMM and copies D back, then
+ * synchronises `stream` and returns (and clears) the device status.  Large
+ * 16-bit row-major problems (B and D together at least 64 MiB, N >= 4096)
+ * run as a pipeline over up to 8 column chunks: the chunks of B and C go up on
+ * a plan-owned copy stream, each chunk's GEMM runs on `stream` as soon as its
+ * columns are up, and its D comes back on another plan-owned stream while the
+ * next chunk computes.  scale_a / scale_b are HOST floats here (1.0 for 16-bit
+ * plans). */
 gemm15_status_t gemm_run_host(gemm15_plan_t plan, const void* hA, const void* hB,
                               const void* hC, void* hD, int64_t M, int64_t N, int64_t K,
                               float alpha, float beta, float scale_a, float scale_b,

@@ -468,6 +468,19 @@ def test_gemm_run_host_bit_exact(dtype, beta):
         assert_bit_exact(prob, d)
 
 
+@pytest.mark.parametrize("dtype,M,N", [("bf16", 512, 8192), ("f16", 136, 10000)])
+def test_gemm_run_host_column_pipeline_bit_exact(dtype, M, N):
+    """Large enough for the column-chunked pipeline (B and D over 64 MiB: 4
+    chunks; N = 10000 leaves a ragged last chunk), with C: bit-exact, twice."""
+    prob = inputs.integer_problem(M, N, 4096, dtype=dtype, beta=0.5, act="relu")
+    plan = _plan(prob)
+    want = oracle_bits(prob)
+    for _ in range(2):
+        st, d = _run_host(plan, prob)
+        assert st == g.OK, g.status_string(st)
+        assert_bit_exact(prob, d, want=want)
+
+
 def test_gemm_run_host_k_zero_and_empty():
     prob = inputs.integer_problem(70, 136, 0, dtype="f16", act="relu")
     prob.A = torch.empty(70, 0, dtype=torch.float16)
