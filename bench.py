@@ -297,10 +297,12 @@ def cpu_oracle_sample(probs, budget_s=10.0, max_rows=None):
                     scales=(scales[0][:rows], scales[1], scales[2], scales[3]) if scales else None)
         return time.perf_counter() - t0
 
+    # grow the sample until one run takes about half the budget, so that the
+    # oracle's per-call setup (decoding B once) is a small part of the time
     rows = min(p.M, max(1, threads))
     dt = run(rows)
-    while dt < 0.25 * budget_s and rows < p.M:
-        rows = min(p.M, max(rows + 1, int(rows * min(8.0, 0.5 * budget_s / max(dt, 1e-3)))))
+    while dt < 0.5 * budget_s and rows < p.M:
+        rows = min(p.M, max(rows + 1, int(rows * min(8.0, 0.8 * budget_s / max(dt, 1e-3)))))
         if max_rows:
             rows = min(rows, max_rows)
         dt = run(rows)
