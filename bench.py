@@ -33,6 +33,7 @@ METRIC = "GEMM TFLOP/s and % of GB300 dense tensor peak per shape (1 GPU)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+ROTATE_BYTES = 2 * (129 << 20)  # --flush rotate: the copies of the inputs fill twice the L2
 KERNEL_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "gemm15_api.cu")
 
 
@@ -443,12 +444,31 @@ def run_gpu(args):
     if p0.a_dtype == "e4m3":
         scales = (torch.tensor([p0.scale_a], device=dev), torch.tensor([p0.scale_b], device=dev))
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # "rotate": the dense and block-scaled workloads cycle through copies of
+    # their inputs whose total is at least twice the L2, so that no step finds
+    # its inputs cached and no flush kernel runs between steps
+    rotate = args.flush == "rotate" and not grouped and not batched
+    copies = 1
+    if rotate:
+        in_bytes = sum(t.numel() * t.element_size() for t in dv[0][:3] if t is not None)
+        if scaled:
+            in_bytes += sum(t.numel() * t.element_size() for t in st_arrays[2:])
+        copies = max(2, min(64, -(-ROTATE_BYTES // max(in_bytes, 1))))
+        if scaled:
+            rot = [tuple(st_arrays)] + [tuple(t.clone() for t in st_arrays) for _ in range(copies - 1)]
+        else:
+            A0, B0, C0, D0 = dv[0]
+            rot = [(A0, B0, C0)] + [(A0.clone(), B0.clone(), C0.clone() if C0 is not None else None)
+                                    for _ in range(copies - 1)]
+    rot_i = [0]
+    flush = torch.empty(L2_FLUSH_BYTES // 4 if not rotate else 1, dtype=torch.float32, device=dev)
     flush_rd = (torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
                 if args.flush == "write+read" else None)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def l2_flush():
+        if rotate:
+            return
         flush.zero_()
         if flush_rd is not None:
             # leave the L2 holding clean lines: the written ones are evicted here
@@ -462,9 +482,14 @@ def run_gpu(args):
         del dv[1:]
 
     def step():
+        r = rot_i[0] % copies
+        rot_i[0] += 1
         if scaled:
             A, B, _, D = dv[0]
-            st = g.gemm_run_block_scaled(plan.handle, A, B, st_arrays[2], st_arrays[3], D,
+            sfa, sfb = st_arrays[2], st_arrays[3]
+            if rotate:
+                A, B, sfa, sfb = rot[r]
+            st = g.gemm_run_block_scaled(plan.handle, A, B, sfa, sfb, D,
                                          p0.M, p0.N, p0.K, scale_kind=scaled_kind,
                                          alpha=p0.alpha, stream=stream)
             if st != g.OK:
@@ -477,6 +502,8 @@ def run_gpu(args):
             plan.grouped(table, alpha=p0.alpha, beta=p0.beta, stream=stream)
         else:
             A, B, C, D = dv[0]
+            if rotate:
+                A, B, C = rot[r]
             plan.run(A, B, C, D, p0.M, p0.N, p0.K, alpha=p0.alpha, beta=p0.beta,
                      scale_a=scales[0] if scales else None,
                      scale_b=scales[1] if scales else None, stream=stream, bias=bias_dev)
@@ -609,7 +636,10 @@ def run_gpu(args):
                        "layout": ("A row-major, B column-major (TN), D row-major; %s block %d"
                                   % (p0.block_scales[2], p0.block_scales[3]) if scaled
                                   else "row-major A, B, C, D"),
-                       "l2": ("flushed between steps (256 MiB write%s, outside the step events)"
+                       "l2": (("inputs larger than L2: %d copies of the inputs (%.0f MB in all) "
+                               "used in turn, no flush between steps" % (copies, copies * in_bytes / 1e6))
+                              if rotate else
+                              "flushed between steps (256 MiB write%s, outside the step events)"
                               % (" then 256 MiB read" if args.flush == "write+read" else "")),
                        "parallelism": "replicas" if ws > 1 else "single",
                        "kernel": cfg, "autotuned": tuned},
@@ -652,11 +682,14 @@ def main(argv=None):
     ap.add_argument("--autotune", action="store_true",
                     help="time every kernel configuration first and keep the fastest")
     ap.add_argument("--trace", help="after timing, save one step's per-CTA timeline (.npy)")
-    ap.add_argument("--flush", choices=["write", "write+read"], default="write+read",
-                    help="L2 flush between timed steps: a 256 MiB write, then (default) a "
+    ap.add_argument("--flush", choices=["write", "write+read", "rotate"], default="write+read",
+                    help="L2 between timed steps: a 256 MiB write, then (default) a "
                          "256 MiB read so that the L2 holds clean lines: after the write "
                          "alone the next kernel first pays for writing back ~L2-size dirty "
-                         "lines (~19 us at HBM speed), a cost of the flush, not of the GEMM")
+                         "lines (~19 us at HBM speed), a cost of the flush, not of the GEMM; "
+                         "or 'rotate': no flush, the steps use copies of the inputs in turn "
+                         "(twice the L2 in all), so the inputs are never cached but the "
+                         "kernel's code stays in L2 as it does when one GEMM follows another")
     args = ap.parse_args(argv)
     if args.list:
         print("\n".join(workloads()))

@@ -720,6 +720,7 @@ const LaunchEntry* launch_entry(gemm15_plan* plan, const Prob& key, bool has_c) 
     fill_layout(plan, gp, p.a_kmajor, p.b_kmajor, d.bn, d.cg);
     gp.groups = nullptr;
     gp.num_groups = 0;
+    set_sched_divisors(gp, d.grid / d.cg);
     e.p = key;
     e.pe = p;
     e.swap = swap;
@@ -1449,6 +1450,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
     gp.groups = plan->d_groups;
     gp.num_groups = ng;
     const int grid = std::min(G, tiles) * cg;
+    set_sched_divisors(gp, grid / cg);
     {
         gemm15_status_t tst = attach_trace(plan, gp, grid, s);
         if (tst != GEMM15_OK) return tst;
@@ -1611,6 +1613,7 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     gp.act = static_cast<int>(plan->desc.epilogue);
     gp.bias = a->bias;
     gp.sf_cb = static_cast<int32_t>(cb);
+    set_sched_divisors(gp, d.grid / cg);
     gp.a_kmajor = gp.b_kmajor = 1;
     gp.a_lbo = gp.b_lbo = 16;
     gp.a_sbo = gp.b_sbo = 1024;

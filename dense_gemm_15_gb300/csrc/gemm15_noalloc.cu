@@ -248,6 +248,7 @@ extern "C" gemm15_status_t gemm_run_splitk_noalloc(
         gp.timeout_ns = 2000000000ull;
         gp.fault_skip_flag = -1;
         const int grid = static_cast<int>(std::min<int64_t>(ds->num_sms, tiles * sp));
+        set_sched_divisors(gp, grid);
         cudaError_t e;
         if (elem == ELEM_F16)
             e = bn == 128 ? launch_gemm<ELEM_F16, 128>(gp, grid, s) : launch_gemm<ELEM_F16, 256>(gp, grid, s);

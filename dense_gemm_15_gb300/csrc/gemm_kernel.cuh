@@ -321,13 +321,33 @@ struct SchedState {
     int64_t o_begin;    // stream-K: start of the head piece (u_end if none)
 };
 
+// The rare 64-bit division, out of line so that the call sites stay short.
+static __device__ __noinline__ int64_t div64(int64_t x, int64_t d) { return x / d; }
+
+// x / d for 0 <= x and 0 < d, in 32-bit arithmetic when both fit: a 64-bit
+// division is a long dependent software sequence.
+__device__ __forceinline__ int64_t idiv(int64_t x, int64_t d) {
+    if (((x | d) >> 31) == 0)
+        return static_cast<int64_t>(static_cast<uint32_t>(x) / static_cast<uint32_t>(d));
+    return div64(x, d);
+}
+
+// x / f.d for 0 <= x by the launch's precomputed multiplier (FastDiv): the
+// scheduler divides a few dozen times before a CTA's first copy, and even a
+// 32-bit division is a dependent chain of a few hundred cycles.
+__device__ __forceinline__ int64_t fdiv(int64_t x, const FastDiv& f) {
+    if (static_cast<uint64_t>(x) < (1ull << 31))
+        return static_cast<int64_t>((static_cast<uint64_t>(x) * f.mul) >> f.shift);
+    return div64(x, f.d);
+}
+
 __device__ __forceinline__ int64_t sk_begin(const GemmParams& p, const Unit& un, int64_t unit) {
-    return (p.sk_units * unit) / un.count;
+    return fdiv(p.sk_units * unit, p.fd_units);
 }
 
 // The unit whose range holds stream-K iteration x.
 __device__ __forceinline__ int32_t sk_unit_of(const GemmParams& p, const Unit& un, int64_t x) {
-    int64_t u = (x * un.count) / p.sk_units;  // sk_begin(u) <= x up to rounding
+    int64_t u = fdiv(x * un.count, p.fd_sk);  // sk_begin(u) <= x up to rounding
     while (u > 0 && sk_begin(p, un, u) > x) --u;
     while (u + 1 < un.count && sk_begin(p, un, u + 1) <= x) ++u;
     return static_cast<int32_t>(u);
@@ -342,8 +362,9 @@ __device__ __forceinline__ int64_t sk_piece_finish(const GemmParams& p, const Un
     const int64_t kb = p.k_blocks;
     const int64_t b = sk_begin(p, un, v), e = sk_begin(p, un, v + 1);
     const int64_t len = min(e, t0 + kb) - max(b, t0);
-    if (b >= t0 || b % kb == 0) return len;
-    return (min(e, (b / kb + 1) * kb) - b) + len;
+    const int64_t bt = fdiv(b, p.fd_kb);  // the tile b lies in
+    if (b >= t0 || b == bt * kb) return len;
+    return (min(e, (bt + 1) * kb) - b) + len;
 }
 
 // Workspace slot / flag of unit v's partial tile: each unit holds at most a
@@ -382,10 +403,11 @@ __device__ __forceinline__ void sched_init(const GemmParams& p, const Unit& un, 
         s.u0 = sk_begin(p, un, un.id);
         s.u_end = sk_begin(p, un, un.id + 1);
         // end of the tail piece (u0 itself when the range starts on a tile)
-        s.u = (s.u0 % kb) ? min(s.u_end, (s.u0 / kb + 1) * kb) : s.u0;
+        const int64_t first_tile = fdiv(s.u0, p.fd_kb) * kb;
+        s.u = (s.u0 != first_tile) ? min(s.u_end, first_tile + kb) : s.u0;
         // start of the head piece (u_end when the range ends on a tile)
-        const int64_t last_tile = (s.u_end / kb) * kb;
-        s.o_begin = (s.u_end % kb && last_tile >= s.u) ? last_tile : s.u_end;
+        const int64_t last_tile = fdiv(s.u_end, p.fd_kb) * kb;
+        s.o_begin = (s.u_end != last_tile && last_tile >= s.u) ? last_tile : s.u_end;
     }
 }
 
@@ -403,11 +425,22 @@ __device__ __forceinline__ void fill_coords(const GemmParams& p, Work& w) {
         w.kb0 = 0;
         w.kb1 = g.k_blocks;
     } else {
+        // raster_coords with the launch's divisors
         w.group = 0;
-        raster_coords(w.tile, p.m_blocks, p.n_blocks, p.raster, w.m_blk, w.n_blk);
+        const int32_t band = static_cast<int32_t>(fdiv(w.tile, p.fd_band));
+        const int32_t first_m = band * p.raster;
+        const int32_t local = w.tile - band * p.raster * p.n_blocks;
+        const bool full = first_m + p.raster <= p.m_blocks;
+        const int32_t rows = full ? p.raster : p.m_blocks - first_m;
+        const int32_t q = static_cast<int32_t>(full ? fdiv(local, p.fd_raster) : fdiv(local, p.fd_last));
+        w.m_blk = first_m + (local - q * rows);
+        w.n_blk = q;
     }
 }
 
+// OWNER = false skips who owns a split tile (h0, h1 and the kind of a piece),
+// which only the epilogue reads.
+template <bool OWNER = true>
 __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, SchedState& s,
                                            Work& w) {
     const int32_t G = un.count;
@@ -415,11 +448,11 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
         const int32_t j = un.id + s.i * G;
         if (j >= p.tiles * p.splits) return false;
         ++s.i;
-        w.tile = j / p.splits;
+        w.tile = static_cast<int32_t>(fdiv(j, p.fd_splits));
         const int32_t sp = j - w.tile * p.splits;
         fill_coords(p, w);
-        w.kb0 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * sp) / p.splits);
-        w.kb1 = static_cast<int32_t>((static_cast<int64_t>(p.k_blocks) * (sp + 1)) / p.splits);
+        w.kb0 = static_cast<int32_t>(fdiv(static_cast<int64_t>(p.k_blocks) * sp, p.fd_splits));
+        w.kb1 = static_cast<int32_t>(fdiv(static_cast<int64_t>(p.k_blocks) * (sp + 1), p.fd_splits));
         w.kind = WK_SPLIT;
         w.h0 = w.h1 = un.id;
         // slots are indexed by 128-row block so the reduction sees one layout
@@ -468,7 +501,7 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
             b1 = s.u + kb;
             s.u = b1;
         }
-        const int32_t rel = static_cast<int32_t>(b0 / kb);
+        const int32_t rel = static_cast<int32_t>(fdiv(b0, p.fd_kb));
         const int64_t tile_u0 = static_cast<int64_t>(rel) * kb;
         w.tile = p.dp_tiles + rel;
         fill_coords(p, w);
@@ -478,6 +511,8 @@ __device__ __forceinline__ bool sched_next(const GemmParams& p, const Unit& un, 
         w.h0 = w.h1 = un.id;
         if (w.kb0 == 0 && w.kb1 == kb) {
             w.kind = WK_FULL;
+        } else if (!OWNER) {
+            w.kind = WK_PEER;  // not known here
         } else {
             // owner: the holder with the latest expected finish (lowest unit on ties)
             w.h0 = sk_unit_of(p, un, tile_u0);
@@ -524,6 +559,113 @@ __device__ __forceinline__ uint32_t count_arrival(unsigned long long* ctr, uint3
         old = prev;
     }
     return 0u;
+}
+
+// ------------------------------------------------------------------ partial tiles
+
+// Adds n fp32 partial chunks, in order, into acc (the first one assigned when
+// `assign`).  src_of(j) is this thread's first float4 of partial j; its nq
+// float4 groups lie 32 float4 apart (a warp's 512 contiguous bytes each).  The
+// loads of 16 / NQP partials are in flight together, so n partials cost about
+// n * NQP / 16 round trips to L2 instead of n.
+template <int NQP, class SrcOf>
+__device__ __forceinline__ void sum_partials_n(const SrcOf& src_of, int32_t n, int nq,
+                                               float (&acc)[64], bool assign, uint64_t pol) {
+    constexpr int P = 16 / NQP;
+    for (int32_t j0 = 0; j0 < n; j0 += P) {
+        float4 t[16];
+#pragma unroll
+        for (int jj = 0; jj < P; ++jj) {
+            const bool live = j0 + jj < n;
+            const float4* src = live ? src_of(j0 + jj) : nullptr;
+#pragma unroll
+            for (int i = 0; i < NQP; ++i)
+                t[jj * NQP + i] = (live && i < nq) ? ld_global_cg_hint(src + 32 * i, pol)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int jj = 0; jj < P; ++jj) {
+            if (j0 + jj >= n) break;
+            const bool first = assign && j0 + jj == 0;
+#pragma unroll
+            for (int i = 0; i < NQP; ++i) {
+                if (i >= nq) continue;
+                const float4 x = t[jj * NQP + i];
+                if (first) {
+                    acc[4 * i + 0] = x.x;
+                    acc[4 * i + 1] = x.y;
+                    acc[4 * i + 2] = x.z;
+                    acc[4 * i + 3] = x.w;
+                } else {
+                    acc[4 * i + 0] += x.x;
+                    acc[4 * i + 1] += x.y;
+                    acc[4 * i + 2] += x.z;
+                    acc[4 * i + 3] += x.w;
+                }
+            }
+        }
+    }
+}
+
+// The same for any nq <= 16: four partials at a time for chunks of at most
+// four groups (a swap-AB tile of a 16-token problem), else one.
+template <class SrcOf>
+__device__ __forceinline__ void sum_partials(const SrcOf& src_of, int32_t n, int nq,
+                                             float (&acc)[64], bool assign, uint64_t pol) {
+    if (nq <= 4) sum_partials_n<4>(src_of, n, nq, acc, assign, pol);
+    else sum_partials_n<16>(src_of, n, nq, acc, assign, pol);
+}
+
+// ------------------------------------------------------------------ four-column epilogue
+
+// The epilogue of the REDUCE_COLS (4) computed outputs (m, n .. n + 3) from
+// the sum of their products: D = act(alpha * acc + beta * C + bias) [op Z],
+// Y (pre) = the value before act, columns past N skipped; each output stored
+// as computed, or for a transposed output (swap-AB) at row n + t, column m.
+// P is GemmParams or ReduceParams (the same field names).
+template <int ELEM, class P>
+__device__ __forceinline__ void epilogue_cols4(const P& p, float alpha, int32_t m, int32_t n, float4 acc) {
+    constexpr int V = REDUCE_COLS;
+    const float av[V] = {acc.x, acc.y, acc.z, acc.w};
+    const int nvalid = min(V, p.N - n);
+    float bias[V];
+#pragma unroll
+    for (int t = 0; t < V; ++t) bias[t] = 0.0f;
+    if (p.bias) {
+        const uint16_t* bv = static_cast<const uint16_t*>(p.bias);
+#pragma unroll
+        for (int t = 0; t < V; ++t) {
+            if (p.bias_rows) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + m));
+            else if (t < nvalid) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + n + t));
+        }
+    }
+    auto at = [&](int64_t ld, int t) -> int64_t {
+        return p.out_trans ? static_cast<int64_t>(n + t) * ld + m : static_cast<int64_t>(m) * ld + n + t;
+    };
+    const uint16_t* cb = static_cast<const uint16_t*>(p.C);
+    uint16_t* db = static_cast<uint16_t*>(p.D);
+    float o[V];
+#pragma unroll
+    for (int t = 0; t < V; ++t) {
+        float x = alpha * av[t];
+        if (p.has_c && t < nvalid) x = fmaf(p.beta, half_bits_to_float<ELEM>(cb[at(p.ldc, t)]), x);
+        x += bias[t];
+        if (p.pre && t < nvalid) {
+            const uint32_t pr = pack2<ELEM>(x, x);
+            static_cast<uint16_t*>(p.pre)[at(p.ldpre, t)] = static_cast<uint16_t>(pr);
+        }
+        o[t] = activate(x, p.act);
+        if (p.aux_op && t < nvalid) {
+            const uint16_t z = static_cast<const uint16_t*>(p.aux)[at(p.ldaux, t)];
+            o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);
+        }
+    }
+    const uint32_t pk[2] = {pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3])};
+    if (nvalid == V && !p.out_trans) {
+        *reinterpret_cast<uint2*>(db + at(p.ldd, 0)) = make_uint2(pk[0], pk[1]);
+    } else {
+        for (int t = 0; t < nvalid; ++t) db[at(p.ldd, t)] = static_cast<uint16_t>(pk[t >> 1] >> (16 * (t & 1)));
+    }
 }
 
 // ------------------------------------------------------------------ tracing
@@ -635,7 +777,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t n_issued = 0;
             bool ok = true;
             int last_group = -1;
-            while (ok && sched_next(p, un, st, w)) {
+            while (ok && sched_next<false>(p, un, st, w)) {
                 const CUtensorMap* tA = &p.tmA;
                 const CUtensorMap* tB = &p.tmB;
                 if (p.groups) {
@@ -757,7 +899,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     umma_commit_pair(map_cluster(bar, 1));
                 }
             };
-            while (ok && sched_next(p, un, st, w)) {
+            while (ok && sched_next<false>(p, un, st, w)) {
                 const uint32_t ab = ACC_BUFS == 2 ? (n_acc & 1u) : 0u;
                 const uint32_t aph = ACC_BUFS == 2 ? ((n_acc >> 1) & 1u) : (n_acc & 1u);
                 if (!wait_bar(ctl, acce_bar(ab), aph ^ 1u)) {
@@ -861,10 +1003,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             return reinterpret_cast<const float4*>(p.ws + static_cast<size_t>(slot) * TILE_M * BN) +
                    peer_off(col0);
         };
-        // the first peer >= v of the tile held by units [w.h0, w.h1], or -1
-        auto next_peer = [&](const Work& w, int32_t v) -> int32_t {
-            if (v == un.id) ++v;
-            return v <= w.h1 ? v : -1;
+        // the peers of an owner item: units h0..h1 but this one, in unit order
+        auto n_peers = [&](const Work& w) -> int32_t {
+            return (w.h1 - w.h0 + 1) - ((un.id >= w.h0 && un.id <= w.h1) ? 1 : 0);
+        };
+        auto peer_at = [&](const Work& w, int32_t j) -> int32_t {
+            const int32_t v = w.h0 + j;
+            return (un.id >= w.h0 && v >= un.id) ? v + 1 : v;
         };
 
         // Bounded barrier of the four epilogue warps (mbarrier with count 4):
@@ -953,20 +1098,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
             // stream-K owner: wait until every peer unit's partial is published
             if (w.kind == WK_OWNER) {
-                if (threadIdx.x == 64) {
-                    for (int32_t v = next_peer(w, w.h0); v >= 0; v = next_peer(w, v + 1)) {
-                        const uint32_t* flag = p.flags + sk_slot(un, v, v == w.h0);
-                        const uint64_t t0 = globaltimer_ns();
-                        uint32_t it = 0;
-                        while (ld_acquire_gpu(flag) != p.epoch) {
-                            if ((++it & 15u) == 0) {
-                                if (*abort_flag) break;
-                                if (globaltimer_ns() - t0 > p.timeout_ns) {
-                                    raise_error(ctl.abort, ctl.status, DEV_ERR_TIMEOUT);
-                                    break;
+                if (threadIdx.x >= 64 && threadIdx.x < 96) {
+                    // one lane per peer: every flag is polled at the same time
+                    const int32_t np = n_peers(w);
+                    for (int32_t j0 = 0; j0 < np; j0 += 32) {
+                        if (j0 + lane < np) {
+                            const int32_t v = peer_at(w, j0 + lane);
+                            const uint32_t* flag = p.flags + sk_slot(un, v, v == w.h0);
+                            const uint64_t t0 = globaltimer_ns();
+                            uint32_t it = 0;
+                            while (ld_acquire_gpu(flag) != p.epoch) {
+                                if ((++it & 15u) == 0) {
+                                    if (*abort_flag) break;
+                                    if (globaltimer_ns() - t0 > p.timeout_ns) {
+                                        raise_error(ctl.abort, ctl.status, DEV_ERR_TIMEOUT);
+                                        break;
+                                    }
                                 }
                             }
                         }
+                        __syncwarp();
                         if (*abort_flag) break;
                     }
                 }
@@ -977,41 +1128,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // accumulator idle (the MMA warp has no further item): the sum of
             // the peers' partial tiles is loaded into it while this item's
             // mainloop still runs, so the fix-up reads TMEM instead of L2.
-            const int32_t pb0 = w.kind == WK_OWNER ? next_peer(w, w.h0) : -1;
-            const bool preload = ACC_BUFS == 2 && pb0 >= 0 && sched_sk_last(st) && ok;
+            const bool preload = ACC_BUFS == 2 && w.kind == WK_OWNER && n_peers(w) > 0 &&
+                                 sched_sk_last(st) && ok;
             if (preload && rows_live) {
                 for (int c = 0; c < nch; ++c) {
                     const int32_t col0 = c * EPI_COLS;
                     // float4 groups of the chunk inside N (partials past N are never written)
                     const int nq = min(16, (N - (n0 + col0) + 3) / 4);
-                    // the whole chunk of the first peer in flight at once (16 loads)
-                    float4 ps[16];
-                    const float4* src0 = peer_src(w, pb0, col0);
+                    float ps[64];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        ps[i] = i < nq ? ld_global_cg_hint(src0 + 32 * i, pol_once) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int32_t pb = next_peer(w, pb0 + 1); pb >= 0; pb = next_peer(w, pb + 1)) {
-                        const float4* src = peer_src(w, pb, col0);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (i >= nq) continue;
-                            const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
-                            ps[i].x += t.x;
-                            ps[i].y += t.y;
-                            ps[i].z += t.z;
-                            ps[i].w += t.w;
-                        }
-                    }
+                    for (int i = 0; i < 64; ++i) ps[i] = 0.0f;
+                    sum_partials([&](int32_t j) { return peer_src(w, peer_at(w, j), col0); },
+                                 n_peers(w), nq, ps, true, pol_once);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t r[32];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            r[4 * i + 0] = __float_as_uint(ps[8 * h + i].x);
-                            r[4 * i + 1] = __float_as_uint(ps[8 * h + i].y);
-                            r[4 * i + 2] = __float_as_uint(ps[8 * h + i].z);
-                            r[4 * i + 3] = __float_as_uint(ps[8 * h + i].w);
-                        }
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(ps[32 * h + i]);
                         tmem_st32(tmem_base + lane_base + (ab ^ 1u) * BN + col0 + h * 32, r);
                     }
                 }
@@ -1071,19 +1204,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i) v[i] = 0.0f;
                     const int32_t slot0 = (w.slot / p.splits) * p.splits;
-                    for (int32_t sp = 0; sp < p.splits; ++sp) {
-                        const float4* src = reinterpret_cast<const float4*>(
+                    sum_partials([&](int32_t sp) {
+                                     return reinterpret_cast<const float4*>(
                                                 p.ws + static_cast<size_t>(slot0 + sp) * TILE_M * BN) + peer_off(col0);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (i >= nq) continue;
-                            const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
-                            v[4 * i + 0] += t.x;
-                            v[4 * i + 1] += t.y;
-                            v[4 * i + 2] += t.z;
-                            v[4 * i + 3] += t.w;
-                        }
-                    }
+                                 },
+                                 p.splits, nq, v, false, pol_once);
                 } else {
                 uint32_t r[2][32];
                 const uint32_t taddr = tmem_base + lane_base + ab * BN + col0;
@@ -1108,18 +1233,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else if (w.kind == WK_OWNER) {
                     // add the peer units' partial tiles in unit order (deterministic)
-                    for (int32_t pb = next_peer(w, w.h0); pb >= 0; pb = next_peer(w, pb + 1)) {
-                        const float4* src = peer_src(w, pb, col0);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (i >= nq) continue;
-                            const float4 t = ld_global_cg_hint(src + 32 * i, pol_once);
-                            v[4 * i + 0] += t.x;
-                            v[4 * i + 1] += t.y;
-                            v[4 * i + 2] += t.z;
-                            v[4 * i + 3] += t.w;
-                        }
-                    }
+                    sum_partials([&](int32_t j) { return peer_src(w, peer_at(w, j), col0); },
+                                 n_peers(w), nq, v, false, pol_once);
                 }
                 }  // from TMEM
                 if (tr && w.kind == WK_OWNER && c == 0) tr[7] = globaltimer_ns();  // peers added
@@ -1438,7 +1553,7 @@ __global__ void __launch_bounds__(32 * REDUCE_MAX_GROUPS) splitk_reduce_kernel(c
     for (int64_t bt = blockIdx.x; bt < batches; bt += gridDim.x) {  // uniform per block
         const int64_t idx = bt * 32 + lane;
         const bool live = idx < total;
-        const int32_t m = live ? static_cast<int32_t>(idx / nv) : 0;
+        const int32_t m = live ? static_cast<int32_t>(idiv(idx, nv)) : 0;
         const int32_t n = live ? static_cast<int32_t>(idx - static_cast<int64_t>(m) * nv) * V : 0;
         float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (live && (p.units > 0 || p.splits > 0)) {
@@ -1451,9 +1566,9 @@ __global__ void __launch_bounds__(32 * REDUCE_MAX_GROUPS) splitk_reduce_kernel(c
             int64_t P, h0 = 0;
             if (p.units > 0) {
                 const int64_t t0 = static_cast<int64_t>(raster_tile(mb, nb, p.m_blocks, p.n_blocks, p.raster)) * p.k_blocks;
-                auto begin = [&](int64_t u) { return (p.sk_units * u) / p.units; };
+                auto begin = [&](int64_t u) { return idiv(p.sk_units * u, p.units); };
                 auto unit_of = [&](int64_t x) {
-                    int64_t u = (x * p.units) / p.sk_units;
+                    int64_t u = idiv(x * p.units, p.sk_units);
                     while (u > 0 && begin(u) > x) --u;
                     while (u + 1 < p.units && begin(u + 1) <= x) ++u;
                     return u;
@@ -1468,7 +1583,7 @@ __global__ void __launch_bounds__(32 * REDUCE_MAX_GROUPS) splitk_reduce_kernel(c
                 const int64_t slot = p.units > 0 ? (j == 0 ? 2 * h0 + 1 : 2 * (h0 + j)) : j;
                 return reinterpret_cast<const float4*>(base + slot * tile_elems);
             };
-            const int64_t j0 = P * g / G, j1 = P * (g + 1) / G;
+            const int64_t j0 = idiv(P * g, G), j1 = idiv(P * (g + 1), G);
             constexpr int U = 8;
             int64_t j = j0;
             for (; j + U <= j1; j += U) {
@@ -1492,47 +1607,7 @@ __global__ void __launch_bounds__(32 * REDUCE_MAX_GROUPS) splitk_reduce_kernel(c
                 const float4 a = group_sum[gg][lane];
                 acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
             }
-            const float av[V] = {acc.x, acc.y, acc.z, acc.w};
-            const int nvalid = min(V, p.N - n);
-            float bias[V];
-#pragma unroll
-            for (int t = 0; t < V; ++t) bias[t] = 0.0f;
-            if (p.bias) {
-                const uint16_t* bv = static_cast<const uint16_t*>(p.bias);
-#pragma unroll
-                for (int t = 0; t < V; ++t) {
-                    if (p.bias_rows) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + m));
-                    else if (t < nvalid) bias[t] = half_bits_to_float<ELEM>(__ldg(bv + n + t));
-                }
-            }
-            // element (m, n + t) of the computed output: row-major, or transposed (swap-AB)
-            auto at = [&](int64_t ld, int t) -> int64_t {
-                return p.out_trans ? static_cast<int64_t>(n + t) * ld + m : static_cast<int64_t>(m) * ld + n + t;
-            };
-            const uint16_t* cb = static_cast<const uint16_t*>(p.C);
-            uint16_t* db = static_cast<uint16_t*>(p.D);
-            float o[V];
-#pragma unroll
-            for (int t = 0; t < V; ++t) {
-                float x = alpha * av[t];
-                if (p.has_c && t < nvalid) x = fmaf(p.beta, half_bits_to_float<ELEM>(cb[at(p.ldc, t)]), x);
-                x += bias[t];
-                if (p.pre && t < nvalid) {
-                    const uint32_t pr = pack2<ELEM>(x, x);
-                    static_cast<uint16_t*>(p.pre)[at(p.ldpre, t)] = static_cast<uint16_t>(pr);
-                }
-                o[t] = activate(x, p.act);
-                if (p.aux_op && t < nvalid) {
-                    const uint16_t z = static_cast<const uint16_t*>(p.aux)[at(p.ldaux, t)];
-                    o[t] = aux_apply(o[t], half_bits_to_float<ELEM>(z), p.aux_op);
-                }
-            }
-            const uint32_t pk[2] = {pack2<ELEM>(o[0], o[1]), pack2<ELEM>(o[2], o[3])};
-            if (nvalid == V && !p.out_trans) {
-                *reinterpret_cast<uint2*>(db + at(p.ldd, 0)) = make_uint2(pk[0], pk[1]);
-            } else {
-                for (int t = 0; t < nvalid; ++t) db[at(p.ldd, t)] = static_cast<uint16_t>(pk[t >> 1] >> (16 * (t & 1)));
-            }
+            epilogue_cols4<ELEM>(p, alpha, m, n, acc);
         }
         __syncthreads();  // group_sum is reused by the next batch
     }

@@ -27,6 +27,31 @@ constexpr int EPI_BUF_BYTES = 32 * 128;  // one 32-row x 128-byte epilogue stagi
 constexpr int REDUCE_COLS = 4;      // split-K reduction: output columns per element
 constexpr int REDUCE_MAX_GROUPS = 8; // split-K reduction: warps (split groups) per block
 
+// Division by a launch constant d (1 <= d) of dividends 0 <= n < 2^31 as a
+// multiply and a shift: q = (n * mul) >> shift, shift = 31 + ceil(log2 d),
+// mul = ceil(2^shift / d) (Granlund and Montgomery, "Division by invariant
+// integers using multiplication").  With mul = 2^shift / d + e, 0 <= e < 1,
+// the error n * e / 2^shift stays below 2^-ceil(log2 d) <= 1/d, which is not
+// enough to reach the next integer above n / d: the floor is exact.  mul <=
+// 2^32, so n * mul < 2^63.  Larger dividends fall back to a division by d.
+struct FastDiv {
+    uint64_t mul;
+    int64_t d;
+    uint32_t shift;
+    uint32_t pad;
+};
+
+inline FastDiv make_fastdiv(int64_t d) {
+    FastDiv f{};
+    if (d < 1) d = 1;
+    f.d = d;
+    uint32_t l = 0;
+    while ((int64_t{1} << l) < d) ++l;  // ceil(log2 d)
+    f.shift = 31 + l;
+    if (f.shift < 63) f.mul = ((uint64_t{1} << f.shift) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d);
+    return f;  // d >= 2^32: every dividend takes the fallback
+}
+
 // One group of a grouped GEMM as the kernel reads it from device memory.
 struct alignas(128) GroupEntry {
     CUtensorMap tmA, tmB, tmC, tmD;
@@ -54,6 +79,9 @@ struct GemmParams {
     int32_t splits;                   // SPLIT: k-splits per tile
     int32_t has_c;                    // beta != 0 (C is read)
     int64_t sk_units;                 // SK: (tiles - dp_tiles) * k_blocks
+    // the scheduler's divisors: scheduling units (CTAs or SM pairs), k_blocks,
+    // sk_units, raster * n_blocks, raster, the last raster band's M-blocks, splits
+    FastDiv fd_units, fd_kb, fd_sk, fd_band, fd_raster, fd_last, fd_splits;
     int32_t sk_partials_only;         // SK partition whose every piece leaves a partial tile
                                       // for the reduction kernel (balanced split-K)
     int32_t l2_hints;                 // operand loads: 0 default, 1 A evict-last, 2 A
@@ -103,6 +131,19 @@ struct GemmParams {
     uint64_t* trace;
     int32_t trace_items;
 };
+
+// Sets the scheduler's divisors from the schedule fields and the number of
+// scheduling units the launch has (grid / CTAs per tile).
+inline void set_sched_divisors(GemmParams& gp, int32_t units) {
+    gp.fd_units = make_fastdiv(units);
+    gp.fd_kb = make_fastdiv(gp.k_blocks);
+    gp.fd_sk = make_fastdiv(gp.sk_units);
+    const int32_t raster = gp.raster > 0 ? gp.raster : 1;
+    gp.fd_band = make_fastdiv(static_cast<int64_t>(raster) * gp.n_blocks);
+    gp.fd_raster = make_fastdiv(raster);
+    gp.fd_last = make_fastdiv(gp.m_blocks > 0 ? gp.m_blocks - ((gp.m_blocks - 1) / raster) * raster : 1);
+    gp.fd_splits = make_fastdiv(gp.splits);
+}
 
 constexpr int TRACE_WORDS = 8;
 // header record: [0] globaltimer at kernel start, [1] SM id, [2] / [3]
