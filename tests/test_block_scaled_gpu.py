@@ -41,7 +41,8 @@ def run_scaled(prob, epilogue="linear", C=None, bias=None, tile_n=0, cta_group=0
     assert plan.query_error() == g.OK
     cfg = plan.last_config()
     assert cfg["tile_n"] == (tile_n or 256) and cfg["launches"] == 1
-    want_cg = 1 if tile_n == 128 else (cta_group or 2)
+    # default: SM pairs for MXFP8, one SM for the fp4 kinds
+    want_cg = 1 if tile_n == 128 else (cta_group or (2 if prob.a_dtype != "e2m1" else 1))
     assert cfg["cta_group"] == want_cg and cfg["tile_m"] == 128 * want_cg
     return inputs.bits(D.cpu())
 
