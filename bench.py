@@ -46,6 +46,8 @@ def workloads():
         "fp16_1024_uniform": lambda: [I.config1("b")],
         "fp16_1024_ones": lambda: [I.config1("a")],
         "fp16_grouped_32": lambda: I.config4(),
+        # the same group shapes in fp8 with per-group scales (CuteDSL page, section 5.1)
+        "e4m3_grouped_32": lambda: I.config4_e4m3(),
         "e4m3_8192": lambda: [I.config5b()],
         # the bias + ReLU epilogue example of the kwkr.cn blog, section 5.2
         "fp16_bias_relu_512x1024x768": lambda: [I.random_problem(512, 1024, 768, act="relu",
@@ -474,6 +476,10 @@ def run_gpu(args):
             # leave the L2 holding clean lines: the written ones are evicted here
             torch.sum(flush_rd, dim=0, out=flush_sink)
     table = [dict(M=p.M, N=p.N, K=p.K, A=A, B=B, C=C, D=D) for p, (A, B, C, D) in zip(probs, dv)]
+    if grouped and p0.a_dtype == "e4m3":  # per-group fp8 scales
+        for t, p in zip(table, probs):
+            t["scale_a"] = torch.tensor([p.scale_a], dtype=torch.float32, device=dev)
+            t["scale_b"] = torch.tensor([p.scale_b], dtype=torch.float32, device=dev)
     if batched:
         # one buffer per operand, entries at packed strides
         bA = torch.stack([A for A, _, _, _ in dv])

@@ -70,7 +70,8 @@ class Problem(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
                 ("D", ctypes.c_void_p), ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64),
-                ("ldc", ctypes.c_int64), ("ldd", ctypes.c_int64)]
+                ("ldc", ctypes.c_int64), ("ldd", ctypes.c_int64),
+                ("scale_a", ctypes.c_void_p), ("scale_b", ctypes.c_void_p)]
 
 
 class Config(ctypes.Structure):
@@ -218,7 +219,8 @@ def gemm_run_host(plan, hA, hB, hC, hD, M, N, K, alpha=1.0, beta=0.0, scale_a=1.
 
 
 def grouped_gemm_run(plan, problems, alpha=1.0, beta=0.0, stream=None):
-    """problems: sequence of (M, N, K, A, B, C, D) or dicts with optional ld*."""
+    """problems: sequence of (M, N, K, A, B, C, D) or dicts with optional ld*
+    and, for e4m3 plans, scale_a / scale_b (device float tensors)."""
     arr = (Problem * max(len(problems), 1))()
     for i, pr in enumerate(problems):
         if isinstance(pr, dict):
@@ -227,7 +229,7 @@ def grouped_gemm_run(plan, problems, alpha=1.0, beta=0.0, stream=None):
             q = dict(zip(("M", "N", "K", "A", "B", "C", "D"), pr))
         arr[i] = Problem(q["M"], q["N"], q["K"], _ptr(q["A"]), _ptr(q["B"]), _ptr(q.get("C")),
                          _ptr(q["D"]), q.get("lda", 0), q.get("ldb", 0), q.get("ldc", 0),
-                         q.get("ldd", 0))
+                         q.get("ldd", 0), _ptr(q.get("scale_a")), _ptr(q.get("scale_b")))
     return load().grouped_gemm_run(plan, arr, len(problems), alpha, beta, _stream(stream))
 
 

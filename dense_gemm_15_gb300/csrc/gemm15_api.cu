@@ -1316,10 +1316,13 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
 
     // validate every group first: nothing is launched on an argument error
     std::vector<Prob> probs;
+    std::vector<const gemm15_problem_t*> src;  // the problem each entry of probs came from
     probs.reserve(count);
+    src.reserve(count);
     for (int32_t i = 0; i < count; ++i) {
         const gemm15_problem_t& q = problems[i];
         if (q.M < 0 || q.N < 0 || q.K < 0) return GEMM15_ERR_INVALID_ARG;
+        if ((q.scale_a || q.scale_b) && plan->elem != ELEM_E4M3) return GEMM15_ERR_INVALID_ARG;
         if (q.M == 0 || q.N == 0) continue;
         if (q.K == 0) return GEMM15_ERR_UNSUPPORTED;
         const int64_t lda = q.lda ? q.lda : (a_row ? q.K : q.M);
@@ -1330,6 +1333,7 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
         gemm15_status_t st = check_operands(plan, p, beta);
         if (st != GEMM15_OK) return st;
         probs.push_back(p);
+        src.push_back(&q);
     }
     const int ng = static_cast<int>(probs.size());
     if (ng == 0) {
@@ -1410,6 +1414,9 @@ gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* pro
             e.ldd = p.ldd;
             e.C = has_c ? p.C : nullptr;
             e.ldc = p.ldc;
+            // (s_a * s_b is symmetric: a group computed as D^T = B^T A^T keeps both)
+            e.scale_a = src[i]->scale_a;
+            e.scale_b = src[i]->scale_b;
             e.raster = plan->opt.raster > 0 ? std::min<int32_t>(plan->opt.raster, e.m_blocks)
                                             : std::min<int32_t>(e.m_blocks, cg == 2 ? 8 : 16);
             const int64_t t = static_cast<int64_t>(e.m_blocks) * e.n_blocks;

@@ -1051,6 +1051,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 has_c = g.has_c;
                 Dptr = static_cast<OutT*>(g.D);
                 ldd = g.ldd;
+                alpha = p.alpha;  // the group's own fp8 scales
+                if (g.scale_a) alpha *= __ldg(g.scale_a);
+                if (g.scale_b) alpha *= __ldg(g.scale_b);
                 if (lane == 0 && w.group != last_group) {
                     tensormap_acquire(tC);
                     tensormap_acquire(tD);

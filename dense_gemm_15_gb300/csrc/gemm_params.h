@@ -62,6 +62,8 @@ struct alignas(128) GroupEntry {
     int64_t ldd;
     const void* C;                    // read directly by the epilogue
     int64_t ldc;
+    const float* scale_a;             // fp8 per-tensor scales of A_g / B_g (device), or null
+    const float* scale_b;
 };
 
 struct GemmParams {

@@ -182,6 +182,21 @@ def config4(groups=32, N=4096, K=2048, seed=0, m_sizes=None):
     return probs
 
 
+def config4_e4m3(groups=32, N=4096, K=2048, seed=0, m_sizes=None):
+    """The grouped shapes of config4 in fp8: e4m3 A_g, B_g ~ N(0,1) clamped to
+    +-448, per-group per-tensor scales 2^U{-3..0}, bf16 out, beta 0."""
+    ms = m_sizes if m_sizes is not None else grouped_sizes(groups, seed=seed)
+    e = rng(4, 999, seed).integers(-3, 0, size=(len(ms), 2), endpoint=True)
+    probs = []
+    for g, m in enumerate(ms):
+        A = normal((m, K), 1.0, "e4m3", 4, 1000 + 2 * g, seed)
+        B = normal((K, N), 1.0, "e4m3", 4, 1001 + 2 * g, seed)
+        probs.append(Problem("e4m3_grouped_g%d" % g, A, B, None, m, N, K, alpha=1.0, beta=0.0,
+                             a_dtype="e4m3", b_dtype="e4m3", c_dtype="bf16", d_dtype="bf16",
+                             scale_a=float(2.0 ** e[g, 0]), scale_b=float(2.0 ** e[g, 1])))
+    return probs
+
+
 def config5a(M, N, K, seed=0) -> Problem:
     """fp16 stream-K stress shape, entries U[-1,1], alpha = beta = 1."""
     wid = 5

@@ -219,16 +219,20 @@ typedef struct {
     const void* C;
     void* D;
     int64_t lda, ldb, ldc, ldd;
+    const float* scale_a; /* E4M3 plans: DEVICE floats, the per-tensor scales of */
+    const float* scale_b; /* A_g and B_g (NULL = 1); other plans: NULL */
 } gemm15_problem_t;
 
-/* Grouped GEMM: D_g = act(alpha * (A_g . B_g) + beta * C_g) for every g in one
+/* Grouped GEMM: D_g = act(alpha * s_a,g * s_b,g * (A_g . B_g) + beta * C_g) for every g in one
  * launch ("Python packages associated with CUTLASS", "Current functionality";
  * "Generating State-of-the-Art GEMMs with TorchInductor's CuteDSL backend",
  * grouped mm).  `problems` is a HOST array of `count` entries, read during the
  * call only.  The plan copies a problem table (shapes, pointers, tensor maps)
  * to device memory on `stream`.  Groups with M, N == 0 are skipped; K == 0
  * groups are not supported (UNSUPPORTED).  Every group must pass the same
- * alignment rules as gemm_run_ex. */
+ * alignment rules as gemm_run_ex.  E4M3 plans take per-group fp32 scales of
+ * A_g and B_g (the grouped fp8 mm of the CuteDSL page, section 5.1), read by
+ * the kernel like gemm_run_ex's; a scale on a 16-bit plan is INVALID_ARG. */
 gemm15_status_t grouped_gemm_run(gemm15_plan_t plan, const gemm15_problem_t* problems,
                                  int32_t count, float alpha, float beta, void* stream);
 

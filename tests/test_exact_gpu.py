@@ -341,6 +341,41 @@ def test_grouped_bit_exact(cg):
         assert_bit_exact(p, inputs.bits(t["D"].cpu()))
 
 
+@pytest.mark.parametrize("cg", [1, 2])
+def test_grouped_e4m3_per_group_scales_bit_exact(cg):
+    """Grouped fp8: every group has its own per-tensor scales of A_g and B_g
+    (one group without any), folded into its alpha in the epilogue."""
+    sizes = [(64, 256, 1024), (200, 400, 2176), (385, 512, 640), (520, 1040, 1152), (256, 256, 4096)]
+    scales = [(0.5, 0.25), (1.0, 2.0), (None, None), (4.0, 0.125), (0.25, None)]
+    probs = [inputs.integer_problem(M, N, K, dtype="e4m3", seed=i,
+                                    scale_a=sa if sa is not None else 1.0,
+                                    scale_b=sb if sb is not None else 1.0)
+             for i, ((M, N, K), (sa, sb)) in enumerate(zip(sizes, scales))]
+    plan = _plan(probs[0], cta_group=cg)
+    dev = []
+    for p, (sa, sb) in zip(probs, scales):
+        f = lambda v: torch.tensor([v], dtype=torch.float32, device="cuda") if v is not None else None
+        dev.append(dict(M=p.M, N=p.N, K=p.K, A=p.A.cuda(), B=p.B.cuda(), C=p.C.cuda(),
+                        D=torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda"),
+                        scale_a=f(sa), scale_b=f(sb)))
+    plan.grouped(dev, alpha=probs[0].alpha, beta=probs[0].beta)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    assert plan.last_config()["cta_group"] == cg
+    for p, t in zip(probs, dev):
+        assert_bit_exact(p, inputs.bits(t["D"].cpu()))
+
+
+def test_grouped_scales_need_an_fp8_plan():
+    prob = inputs.integer_problem(64, 256, 1024, dtype="f16")
+    plan = _plan(prob)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    D = torch.empty(64, 256, dtype=torch.float16, device="cuda")
+    st = g.grouped_gemm_run(plan.handle, [dict(M=64, N=256, K=1024, A=prob.A.cuda(), B=prob.B.cuda(),
+                                               C=None, D=D, scale_a=one)], alpha=1.0, beta=0.0)
+    assert st == g.ERR_INVALID_ARG
+
+
 def test_batched_bit_exact():
     batch, M, N, K = 5, 264, 392, 1040
     probs = [inputs.integer_problem(M, N, K, dtype="bf16", seed=b) for b in range(batch)]
