@@ -200,7 +200,7 @@ gemm15_status_t gemm_run_args(gemm15_plan_t plan, const gemm15_args_t* args, voi
  * into plan-owned device buffers, runs the GEMM and copies D back, then
  * synchronises `stream` and returns (and clears) the device status.  Large
  * 16-bit row-major problems (B and D together at least 64 MiB, N >= 4096)
- * run as a pipeline over up to 8 column chunks: the chunks of B and C go up on
+ * run as a pipeline over 4 column chunks: the chunks of B and C go up on
  * a plan-owned copy stream, each chunk's GEMM runs on `stream` as soon as its
  * columns are up, and its D comes back on another plan-owned stream while the
  * next chunk computes.  scale_a / scale_b are HOST floats here (1.0 for 16-bit
