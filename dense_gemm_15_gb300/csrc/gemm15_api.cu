@@ -1570,7 +1570,7 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     // against 514; MXFP4 306 against 320, NVFP4 377 against 405 on one SM)
     const int clusters = std::min(pair_clusters(plan), G / 2);
     const bool want_pair = plan->opt.cta_group == 2 || (plan->opt.cta_group == 0 && sf == SF_MXF8);
-    const int cg = (BN == 256 && clusters > 0 && want_pair) ? 2 : 1;
+    const int cg = (clusters > 0 && want_pair && (BN == 256 || plan->opt.cta_group == 2)) ? 2 : 1;
     Decision d;
     d.cg = cg;
     d.bn = BN;
@@ -1649,7 +1649,15 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     gemm15_status_t st = attach_trace(plan, gp, d.grid, s);
     if (st != GEMM15_OK) return st;
     cudaError_t e;
-    if (cg == 2) {
+    if (cg == 2 && BN == 128) {
+        if (sf == SF_MXF8)
+            e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, 128, 2, SF_MXF8>(gp, d.grid, s)
+                                        : launch_gemm<ELEM_E5M2, 128, 2, SF_MXF8>(gp, d.grid, s);
+        else if (sf == SF_MXF4)
+            e = launch_gemm<ELEM_E2M1, 128, 2, SF_MXF4>(gp, d.grid, s);
+        else
+            e = launch_gemm<ELEM_E2M1, 128, 2, SF_NVF4>(gp, d.grid, s);
+    } else if (cg == 2) {
         if (sf == SF_MXF8)
             e = plan->elem == ELEM_E4M3 ? launch_gemm<ELEM_E4M3, 256, 2, SF_MXF8>(gp, d.grid, s)
                                         : launch_gemm<ELEM_E5M2, 256, 2, SF_MXF8>(gp, d.grid, s);

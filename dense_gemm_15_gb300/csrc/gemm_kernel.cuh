@@ -78,9 +78,11 @@ struct Traits {
     static constexpr int STAGES_FIT = (SMEM_FIXED - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
     // an N-major B stage is whole 128-byte swizzle rows of N
-    static_assert(B_COLS * ESIZE >= 128 && (B_COLS * ESIZE) % 128 == 0, "B columns per CTA");
+    // (block-scaled B is always K-major: any multiple of 8 rows)
+    static_assert(SF != SF_NONE || (B_COLS * ESIZE >= 128 && (B_COLS * ESIZE) % 128 == 0),
+                  "B columns per CTA");
     static_assert(EPI_BUFS <= 8, "C barrier parity bits");
-    static_assert(SF == SF_NONE || (BN % 128 == 0 && (CG == 1 || BN == 256)), "block-scaled tiles");
+    static_assert(SF == SF_NONE || BN % 128 == 0, "block-scaled tiles");
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SF = OFF_B + STAGES * B_STAGE;

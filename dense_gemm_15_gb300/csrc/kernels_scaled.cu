@@ -14,6 +14,13 @@ template cudaError_t launch_gemm<ELEM_E2M1, 128, 1, SF_MXF4>(const GemmParams&, 
 template cudaError_t launch_gemm<ELEM_E2M1, 128, 1, SF_NVF4>(const GemmParams&, int, cudaStream_t);
 
 int gemm_scaled_stages(int sf, int bn, int cg) {
+    if (cg == 2 && bn == 128) {
+        switch (sf) {
+            case SF_MXF8: return Traits<ELEM_E4M3, 128, 2, SF_MXF8>::STAGES;
+            case SF_MXF4: return Traits<ELEM_E2M1, 128, 2, SF_MXF4>::STAGES;
+            default: return Traits<ELEM_E2M1, 128, 2, SF_NVF4>::STAGES;
+        }
+    }
     if (cg == 2) {
         switch (sf) {
             case SF_MXF8: return Traits<ELEM_E4M3, 256, 2, SF_MXF8>::STAGES;

@@ -417,8 +417,9 @@ typedef struct {
  * (kind::mxf8f6f4 for MXFP8, kind::mxf4 for MXFP4, kind::mxf4nvf4 for NVFP4;
  * scale factors copied to tensor memory beside the accumulator).  Tiles: SM-pair
  * 256 x 256 (cta_group::2) for MXFP8 and one-SM 128 x 256 for the fp4 kinds by
- * default; GEMM15_OPT_CTA_GROUP = 1 / 2 forces one-SM / SM-pair 256-wide tiles,
- * GEMM15_OPT_TILE_N = 128 one-SM 128 x 128 tiles.  The plan
+ * default; GEMM15_OPT_CTA_GROUP = 1 / 2 forces one-SM / SM-pair tiles and
+ * GEMM15_OPT_TILE_N = 128 selects 128 x 128 (one SM) or 256 x 128 (SM pair)
+ * tiles.  The plan
  * must have layout_a ROW_MAJOR, layout_b COL_MAJOR, layout_cd ROW_MAJOR
  * (UNSUPPORTED otherwise).  K must be a multiple of 128 (fp8) or 256 (fp4)
  * (UNSUPPORTED otherwise); pointers 16-byte aligned and leading dimensions

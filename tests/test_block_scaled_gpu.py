@@ -42,7 +42,7 @@ def run_scaled(prob, epilogue="linear", C=None, bias=None, tile_n=0, cta_group=0
     cfg = plan.last_config()
     assert cfg["tile_n"] == (tile_n or 256) and cfg["launches"] == 1
     # default: SM pairs for MXFP8, one SM for the fp4 kinds
-    want_cg = 1 if tile_n == 128 else (cta_group or (2 if prob.a_dtype != "e2m1" else 1))
+    want_cg = cta_group or (1 if tile_n == 128 or prob.a_dtype == "e2m1" else 2)
     assert cfg["cta_group"] == want_cg and cfg["tile_m"] == 128 * want_cg
     return inputs.bits(D.cpu())
 
@@ -51,7 +51,8 @@ FORMATS = [("e4m3", 32, "ue8m0"), ("e5m2", 32, "ue8m0"), ("e2m1", 32, "ue8m0"),
            ("e2m1", 16, "e4m3")]
 
 
-TILES = [(128, 1), (256, 1), (256, 2)]  # (tile_n, cta_group): one-SM 128 x {128, 256}, pair 256 x 256
+# (tile_n, cta_group): one-SM 128 x {128, 256}, SM-pair 256 x {256, 128}
+TILES = [(128, 1), (256, 1), (256, 2), (128, 2)]
 
 
 @pytest.mark.parametrize("tile_n,cta_group", TILES)
