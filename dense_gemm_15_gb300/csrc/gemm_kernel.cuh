@@ -710,9 +710,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile uint32_t* tmem_slot = misc;
     volatile uint32_t* abort_flag = misc + 1;
 
-    // a programmatic dependent (the split-K reduction) may be scheduled now;
-    // it waits for this grid's completion before it reads anything
+    // a programmatic dependent (the split-K reduction, or the next GEMM) may be
+    // scheduled now; it waits for this grid's completion before it touches
+    // global memory.  This grid, itself launched as a programmatic dependent,
+    // waits for the kernel before it (griddepcontrol.wait) before its first
+    // global access: its roles do so after their set-up, a traced or grouped
+    // launch (trace records, the problem table) here.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.trace || p.groups) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     Ctl ctl{abort_flag, p.status, p.timeout_ns};
@@ -777,6 +782,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             sched_init(p, un, st);
             Work w;
             uint32_t n_issued = 0;
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             bool ok = true;
             int last_group = -1;
             while (ok && sched_next<false>(p, un, st, w)) {
@@ -981,6 +987,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int e = warp - 2;                 // epilogue warp index (buffers)
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t ebuf0 = sEpi + e * EPI_BUFS * EPI_BUF_BYTES;
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // before any global access
         float alpha = p.alpha;
         if (p.scale_a) alpha *= __ldg(p.scale_a);
         if (p.scale_b) alpha *= __ldg(p.scale_b);

@@ -19,24 +19,25 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
         if (err != cudaSuccess) return err;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    if constexpr (CG == 1) {
-        gemm_tc_kernel<ELEM, BN, 1, SF><<<grid, NUM_THREADS, TR::SMEM_BYTES, stream>>>(p);
-        return cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = TR::SMEM_BYTES;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<ELEM, BN, 2, SF>, p);
-    }
+    // A programmatic dependent launch: when the kernel before it in the stream
+    // triggers (every GEMM kernel does at entry), this grid's CTAs may start
+    // as SMs free up, run their set-up, and wait (griddepcontrol.wait) before
+    // touching global memory until that kernel has completed.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = TR::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CG;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CG == 2 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<ELEM, BN, CG, SF>, p);
 }
 
 template <int ELEM>

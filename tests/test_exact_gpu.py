@@ -376,6 +376,60 @@ def test_grouped_scales_need_an_fp8_plan():
     assert st == g.ERR_INVALID_ARG
 
 
+# ------------------------------------------------------------------ back-to-back launches
+
+def test_back_to_back_dependent_gemms_bit_exact():
+    """A chain of GEMMs on one stream with no synchronisation: each reads the
+    previous one's D (every GEMM kernel is a programmatic dependent launch that
+    waits for the kernel before it before touching global memory), through
+    data-parallel, stream-K and split-K-with-reduction-kernel launches."""
+    import oracle
+    M, K = 256, 64
+    p1 = inputs.integer_problem(M, 512, K, dtype="bf16", alpha=1.0, beta=0.0, act="linear", seed=1)
+    d1_want = oracle_bits(p1)  # |D1| <= 256: exact in bf16
+    # |D2| <= 256 * 512 = 2^17 and |D3| <= 2^17 * 64 = 2^23: every sum exact in fp32
+    B2 = inputs.integers((512, 64), -1, 1, "bf16", 8, 77, 0)
+    B3 = inputs.integers((64, 640), -1, 1, "bf16", 8, 78, 0)
+    plans = [_plan(p1, schedule=g.SCHED_DP), _plan(p1, schedule=g.SCHED_SK, grid=24),
+             _plan(p1, schedule=g.SCHED_SPLIT, splits=4, splitk_inline=1, cta_group=1)]
+    for plan2 in plans:
+        A1, B1 = p1.A.cuda(), p1.B.cuda()
+        D1 = torch.full((M, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        D2 = torch.full((M, 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+        D3 = torch.full((M, 640), float("nan"), dtype=torch.bfloat16, device="cuda")
+        plans[0].run(A1, B1, None, D1, M, 512, K)
+        plan2.run(D1, B2.cuda(), None, D2, M, 64, 512)
+        plans[0].run(D2, B3.cuda(), None, D3, M, 640, 64)
+        torch.cuda.synchronize()
+        assert plans[0].query_error() == g.OK and plan2.query_error() == g.OK
+        d1 = inputs.bits(D1.cpu())
+        assert np.array_equal(d1, d1_want)
+        d2_want = oracle.round_to(oracle.gemm(d1_want, "bf16", inputs.bits(B2), "bf16"), "bf16")
+        assert np.array_equal(inputs.bits(D2.cpu()), d2_want)
+        d3_want = oracle.round_to(oracle.gemm(d2_want, "bf16", inputs.bits(B3), "bf16"), "bf16")
+        assert np.array_equal(inputs.bits(D3.cpu()), d3_want)
+
+
+@pytest.mark.parametrize("sched,opts", [(g.SCHED_SK, dict(grid=40)),
+                                        (g.SCHED_SPLIT, dict(splits=5, splitk_inline=2)),
+                                        (g.SCHED_SPLIT, dict(splits=5, splitk_inline=1))])
+def test_back_to_back_launches_of_one_plan_bit_exact(sched, opts):
+    """Three launches of one plan back to back without synchronisation: the
+    plan's workspace, flags and counters serve each in turn, so a launch that
+    touched them before the previous one finished would corrupt its partials."""
+    probs = [inputs.integer_problem(384, 520, 4096, dtype="f16", seed=s) for s in range(3)]
+    plan = _plan(probs[0], schedule=sched, cta_group=1, tile_n=128, **opts)
+    outs = []
+    for p in probs:
+        D = torch.full((p.M, p.N), float("nan"), dtype=torch.float16, device="cuda")
+        plan.run(p.A.cuda(), p.B.cuda(), p.C.cuda(), D, p.M, p.N, p.K, alpha=p.alpha, beta=p.beta)
+        outs.append(D)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    for p, D in zip(probs, outs):
+        assert_bit_exact(p, inputs.bits(D.cpu()))
+
+
 def test_batched_bit_exact():
     batch, M, N, K = 5, 264, 392, 1040
     probs = [inputs.integer_problem(M, N, K, dtype="bf16", seed=b) for b in range(batch)]
