@@ -16,7 +16,7 @@ def shape(M, N, K, dtype="f16", beta=0.0, bias=False, aux=False):
                            bias=object() if bias else None, aux=object() if aux else None)
 
 
-def test_algorithmic_bytes_of_the_survey_workloads():
+def test_algorithmic_bytes_of_the_named_workloads():
     # fp16 4096^3 with beta != 0: A, B, C, D of 32 MiB each
     assert bench.algorithmic_bytes([shape(4096, 4096, 4096, beta=0.5)]) == 4 * 32 * 2 ** 20
     # e4m3 8192^3, beta 0: A, B one byte per element, D bf16
@@ -72,7 +72,7 @@ def test_roofline_bound_switches_exactly_at_the_ridge():
     assert below["bound"] == "hbm" and above["bound"] == "tensor"
 
 
-def test_named_workloads_cover_the_survey_configs():
+def test_named_workloads_cover_the_five_configs():
     names = set(bench.workloads())
     assert bench.DEFAULT_WORKLOAD in names and bench.BATCHED_WORKLOAD in names
     for n in ("fp16_1024_uniform", "fp16_1024_ones", "fp16_grouped_32", "e4m3_8192",
