@@ -612,10 +612,13 @@ def run_gpu(args):
             g.gemm_run_host(plan.handle, hA, hB, hC, hD, p0.M, p0.N, p0.K, p0.alpha, p0.beta,
                             p0.scale_a, p0.scale_b, stream)
         barrier(dist)
+        per_call = []
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
+            t1 = time.perf_counter()
             s = g.gemm_run_host(plan.handle, hA, hB, hC, hD, p0.M, p0.N, p0.K, p0.alpha,
                                 p0.beta, p0.scale_a, p0.scale_b, stream)
+            per_call.append(time.perf_counter() - t1)
             if s != g.OK:
                 raise RuntimeError("gemm_run_host: " + g.status_string(s))
         t_e2e = (time.perf_counter() - t0) / e2e_steps
@@ -623,8 +626,12 @@ def run_gpu(args):
         h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
         if hC is not None and p0.beta != 0.0:
             h2d += hC.numel() * hC.element_size()
+        # value: total work / total time of the calls; the median call shows the
+        # steady state apart from the occasional host stall of a shared machine
         e2e = {"value": total_flops / t_e2e / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": hD.numel() * hD.element_size()}
+               "d2h_bytes_per_step": hD.numel() * hD.element_size(),
+               "ms_per_call": 1e3 * t_e2e, "ms_per_call_median": 1e3 * statistics.median(per_call),
+               "ms_per_call_max": 1e3 * max(per_call), "calls": e2e_steps}
 
     pk, pk_kind = peaks()
     peak = tensor_peak(p0.a_dtype, pk)
