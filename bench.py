@@ -277,43 +277,54 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle baseline
 
+def _column_sample(p, cols):
+    """Views of the operands for columns 0..cols of D (B's first cols columns,
+    C's and the bias's too): the oracle decodes only those columns of B."""
+    from dense_gemm_15_gb300 import inputs as I
+    b = I.bits(p.B)
+    b = b[:cols, :] if p.b_col_major else b[:, :cols]
+    c = I.bits(p.C)[:, :cols] if p.C is not None and p.beta != 0.0 else None
+    bv = I.bits(p.bias)[:cols] if p.bias is not None else None
+    sc = getattr(p, "block_scales", None)
+    scales = (I.bits(sc[0]), I.bits(sc[1])[:, :cols], sc[2], sc[3]) if sc is not None else None
+    return b, c, bv, scales
+
+
 def cpu_oracle_sample(probs, budget_s=10.0, max_rows=None):
-    """Times the oracle (as it stands) on a bounded row sample of the workload.
+    """Times the oracle (as it stands) on a bounded sample of the workload:
+    rows 0..r and columns 0..c of D (whole K), growing first c up to 2048,
+    then r up to M, then c up to N, until one run takes about half the budget.
     Returns (flops/s, cores, description, seconds)."""
     import oracle
     from dense_gemm_15_gb300 import inputs as I
     p = max(probs, key=lambda q: q.flops)
     threads = oracle.default_threads()
-    a, b = I.bits(p.A), I.bits(p.B)
-    c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
-    bv = I.bits(p.bias) if p.bias is not None else None
+    a = I.bits(p.A)
 
-    sc = getattr(p, "block_scales", None)
-    scales = (I.bits(sc[0]), I.bits(sc[1]), sc[2], sc[3]) if sc is not None else None
-
-    def run(rows):
+    def run(rows, cols):
+        b, c, bv, scales = _column_sample(p, cols)
         t0 = time.perf_counter()
         oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
                     act=p.act, bias=bv, bias_dtype=p.d_dtype, scale_a=p.scale_a,
                     scale_b=p.scale_b, a_col_major=p.a_col_major, b_col_major=p.b_col_major,
-                    rows=(0, rows), threads=threads,
-                    scales=(scales[0][:rows], scales[1], scales[2], scales[3]) if scales else None)
+                    rows=(0, rows), threads=threads, scales=scales)
         return time.perf_counter() - t0
 
-    # grow the sample until one run takes about half the budget, so that the
-    # oracle's per-call setup (decoding B once) is a small part of the time
+    cols = min(p.N, 2048)
     rows = min(p.M, max(1, threads))
-    dt = run(rows)
-    while dt < 0.5 * budget_s and rows < p.M:
-        rows = min(p.M, max(rows + 1, int(rows * min(8.0, 0.8 * budget_s / max(dt, 1e-3)))))
-        if max_rows:
-            rows = min(rows, max_rows)
-        dt = run(rows)
-        if max_rows and rows >= max_rows:
-            break
-    flops = 2.0 * rows * p.N * p.K
-    desc = "rows 0..%d of %s (all N=%d columns, full K=%d)" % (rows, p.name, p.N, p.K)
-    return flops / dt, threads, desc, dt
+    dt = run(rows, cols)
+    while dt < 0.5 * budget_s and (rows < p.M or cols < p.N):
+        grow = min(8.0, 0.8 * budget_s / max(dt, 1e-3))
+        if rows < p.M and not (max_rows and rows >= max_rows):
+            rows = min(p.M, max(rows + 1, int(rows * grow)))
+            if max_rows:
+                rows = min(rows, max_rows)
+        else:
+            cols = min(p.N, max(cols + 1, int(cols * grow)))
+        dt = run(rows, cols)
+    flops = 2.0 * rows * cols * p.K
+    desc = "rows 0..%d x columns 0..%d of %s (full K=%d)" % (rows, cols, p.name, p.K)
+    return flops / dt, threads, desc, dt, rows, cols
 
 
 # ------------------------------------------------------------------ distributed
@@ -370,18 +381,16 @@ def run_reference(args):
     from dense_gemm_15_gb300 import inputs as I
     probs = get_workload(args.workload)
     per_step = min(args.cpu_budget, 120.0 / max(1, args.steps + args.warmup))
-    _, cores, desc, _ = cpu_oracle_sample(probs, budget_s=per_step)
+    _, cores, desc, _, rows, cols = cpu_oracle_sample(probs, budget_s=per_step)
     p = max(probs, key=lambda q: q.flops)
-    rows = int(desc.split("..")[1].split()[0])
-    a, b = I.bits(p.A), I.bits(p.B)
-    c = I.bits(p.C) if p.C is not None and p.beta != 0.0 else None
-    bv = I.bits(p.bias) if p.bias is not None else None
+    a = I.bits(p.A)
+    b, c, bv, scales = _column_sample(p, cols)
 
     def step():
         oracle.gemm(a, p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha, beta=p.beta,
                     act=p.act, bias=bv, bias_dtype=p.d_dtype, scale_a=p.scale_a,
                     scale_b=p.scale_b, a_col_major=p.a_col_major, b_col_major=p.b_col_major,
-                    rows=(0, rows), threads=cores)
+                    rows=(0, rows), threads=cores, scales=scales)
 
     for _ in range(args.warmup):
         step()
@@ -389,7 +398,7 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     t = (time.perf_counter() - t0) / max(1, args.steps)
-    value = 2.0 * rows * p.N * p.K / t / 1e12
+    value = 2.0 * rows * cols * p.K / t / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
@@ -642,7 +651,7 @@ def run_gpu(args):
     clocks = clk.summary()
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        fl_s, cores, desc, secs = cpu_oracle_sample(probs, budget_s=args.cpu_budget)
+        fl_s, cores, desc, secs, _, _ = cpu_oracle_sample(probs, budget_s=args.cpu_budget)
         cpu = {"value": fl_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": desc, "seconds": secs}
 
