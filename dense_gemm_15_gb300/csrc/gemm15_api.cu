@@ -1558,9 +1558,10 @@ gemm15_status_t gemm_run_block_scaled(gemm15_plan_t plan, const gemm15_scaled_ar
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (order_after_previous(plan, s) != GEMM15_OK) return GEMM15_ERR_CUDA;
 
-    // tile width: 128 x 256 tiles (one accumulator, 3 stages) by default;
-    // 128 x 128 tiles keep two accumulators and a 5-stage ring but measured
-    // slower on GB300 (MXFP8 8192^3: 686 against 531 us; NVFP4: 508 against 381)
+    // tile width: 256 columns (one accumulator per CTA) by default; 128-wide
+    // tiles keep two accumulators but measured slower on GB300 (one SM, MXFP8
+    // 8192^3: 686 against 531 us, NVFP4 508 against 381; SM pairs: MXFP8 755
+    // against 484 us)
     const int BN = plan->opt.tile_n == 128 ? 128 : 256;
     const int G = plan->opt.grid > 0 ? std::min(plan->opt.grid, plan->num_sms) : plan->num_sms;
     // SM-pair 256 x 256 tiles (each CTA stages its 128 rows of A and 128 columns
