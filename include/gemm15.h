@@ -36,6 +36,13 @@
  *     to the plan's status word; read them with gemm_plan_query_error after
  *     synchronising the stream.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - GEMM kernels are launched as programmatic dependents of the kernel
+ *     before them in the stream: their set-up may overlap that kernel's tail,
+ *     but they read and write no memory before it has completed, so stream
+ *     order holds as usual.  They also allow the kernel after them to start
+ *     early; a kernel that asks for that (programmatic stream serialization)
+ *     must itself wait (griddepcontrol.wait / cudaGridDependencySynchronize)
+ *     before reading what the GEMM wrote.
  *   - A plan may be used from one host thread at a time.  Its device state
  *     (workspace, stream-K flags, status word, grouped table, host-path
  *     buffers) serves every call, so calls on one plan never run concurrently
