@@ -144,3 +144,35 @@ def test_block_scaled_peaks_and_bytes():
     p = shape(8192, 8192, 8192, "e2m1")
     p.block_scales = (None, None, "e4m3", 16)
     assert bench.algorithmic_bytes([p]) == 2 * 8192 * 4096 + 8192 * 8192 * 2 + 2 * 8192 * 512
+
+
+@pytest.mark.parametrize("name", ["custom_f16_96x264x128_b0.5_relu_bias",
+                                  "custom_bf16_40x136x192_bcol_acol"])
+def test_cpu_sample_is_a_block_of_the_full_result(name):
+    """The CPU baseline's sample (rows 0..r, columns 0..c of D) computes exactly
+    that block of the full problem: the column views of B, C and the bias line
+    up with the rows the oracle is asked for."""
+    import numpy as np
+    import oracle
+    from dense_gemm_15_gb300 import inputs as I
+    p = bench.get_workload(name)[0]
+    full = oracle.gemm(I.bits(p.A), p.a_dtype, I.bits(p.B), p.b_dtype,
+                       I.bits(p.C) if p.C is not None and p.beta != 0.0 else None, p.c_dtype,
+                       alpha=p.alpha, beta=p.beta, act=p.act,
+                       bias=I.bits(p.bias) if p.bias is not None else None,
+                       bias_dtype=p.d_dtype, a_col_major=p.a_col_major,
+                       b_col_major=p.b_col_major)
+    rows, cols = 17, 40
+    b, c, bv, scales = bench._column_sample(p, cols)
+    part = oracle.gemm(I.bits(p.A), p.a_dtype, b, p.b_dtype, c, p.c_dtype, alpha=p.alpha,
+                       beta=p.beta, act=p.act, bias=bv, bias_dtype=p.d_dtype,
+                       a_col_major=p.a_col_major, b_col_major=p.b_col_major, rows=(0, rows),
+                       scales=scales)
+    assert np.array_equal(part, full[:rows, :cols])
+
+
+def test_cpu_sample_grows_to_its_budget():
+    r = bench.cpu_oracle_sample(bench.get_workload("custom_f16_64x4096x256")[0:1], budget_s=0.2)
+    flops_s, cores, desc, secs, rows, cols = r
+    assert flops_s > 0 and cores >= 1 and 1 <= rows <= 64 and 1 <= cols <= 4096
+    assert ("rows 0..%d x columns 0..%d" % (rows, cols)) in desc
