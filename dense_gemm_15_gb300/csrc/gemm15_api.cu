@@ -368,7 +368,10 @@ Decision decide(gemm15_plan* plan, int64_t M, int64_t N, int64_t K, const Option
     int cg = 1;
     // SM-pair tiles 256 x 128 exist for 16-bit operands only (an fp8 half-tile
     // of B would be narrower than one 128-byte swizzle row)
-    const bool pair_ok = !swap && (d.bn == 256 || plan->elem != ELEM_E4M3);
+    // swap-AB tiles pair only when asked (16-bit, 128 tokens wide: each CTA of
+    // the pair stages 64 of them)
+    const bool pair_ok = swap ? (o.cta_group == 2 && d.bn == 128 && plan->elem != ELEM_E4M3)
+                              : (d.bn == 256 || plan->elem != ELEM_E4M3);
     const int clusters = std::min(pair_clusters(plan), G1 / 2);
     if (pair_ok && o.cta_group != 1) {
         const int64_t tiles2 = cdiv(M, 2 * TILE_M) * cdiv(N, 256);

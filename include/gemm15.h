@@ -293,8 +293,10 @@ typedef enum {
                                       1 never, 2 always.  Swap-AB computes
                                       D^T = B^T . A^T on 128 x 64 (16-bit, M <= 64)
                                       or 128 x 128 single-SM tiles and stores the
-                                      tile transposed; GEMM15_OPT_TILE_N and
-                                      GEMM15_OPT_CTA_GROUP do not apply to it */
+                                      tile transposed; GEMM15_OPT_TILE_N does not
+                                      apply to it, GEMM15_OPT_CTA_GROUP = 2 puts
+                                      16-bit 128-wide swap tiles on SM pairs
+                                      (256 x 128) */
     GEMM15_OPT_SPLITK_INLINE = 11, /* split-K: 0 auto (when a tile's partials total at
                                       most 256 KiB), 1 never, 2 always: the split that
                                       finishes a tile last (a per-tile arrival

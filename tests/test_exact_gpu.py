@@ -243,6 +243,20 @@ def test_swap_ab_bit_exact(sched, M, dtype):
     assert_bit_exact(prob, d)
 
 
+@pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("M", [72, 128])
+def test_swap_ab_sm_pair_tiles_bit_exact(sched, M):
+    """Swap-AB on SM-pair 256 x 128 tiles (each CTA stages 64 of the tokens),
+    stored transposed, with C, a bias, Z and the pre-activation output."""
+    prob = inputs.integer_problem(M, 1160, 2112, dtype="bf16", bias=True, aux_op="add")
+    plan = _plan(prob, schedule=sched, swap_ab=2, cta_group=2)
+    d, y = _run_args(plan, prob, with_pre=True)
+    cfg = plan.last_config()
+    assert cfg["swap_ab"] == 1 and cfg["cta_group"] == 2 and cfg["tile_n"] == 128
+    assert_bit_exact(prob, d)
+    assert_bit_exact(_linear_part(prob), y)
+
+
 @pytest.mark.parametrize("a_col,b_col", [(True, False), (False, True), (True, True)])
 @pytest.mark.parametrize("sched", [g.SCHED_SK, g.SCHED_SPLIT])
 def test_swap_ab_operand_layouts_bit_exact(a_col, b_col, sched):
