@@ -17,7 +17,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgemm15.so")
 UNITS = ["gemm15_api.cu", "gemm15_noalloc.cu", "kernels_f16.cu", "kernels_bf16.cu",
-         "kernels_e4m3.cu", "kernels_scaled.cu", "kernels_scaled_pair.cu"]
+         "kernels_e4m3.cu", "kernels_scaled.cu", "kernels_scaled_128.cu",
+         "kernels_scaled_pair.cu", "kernels_scaled_pair_128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,6 +1,6 @@
-// Instantiations of the block-scaled sm_103a GEMM kernels (MXFP8 with E4M3 or
-// E5M2 elements, MXFP4 and NVFP4 with packed E2M1 elements; 128 x 256 tiles with
-// one accumulator, 128 x 128 tiles with two).
+// Instantiations of the block-scaled sm_103a GEMM kernels on one-SM 128 x 256
+// tiles with one accumulator (MXFP8 with E4M3 or E5M2 elements, MXFP4 and NVFP4
+// with packed E2M1 elements), and the pipeline depth of every block-scaled form.
 #include "launch_impl.cuh"
 
 namespace g15 {
@@ -8,10 +8,6 @@ template cudaError_t launch_gemm<ELEM_E4M3, 256, 1, SF_MXF8>(const GemmParams&, 
 template cudaError_t launch_gemm<ELEM_E5M2, 256, 1, SF_MXF8>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_E2M1, 256, 1, SF_MXF4>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_E2M1, 256, 1, SF_NVF4>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E4M3, 128, 1, SF_MXF8>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E5M2, 128, 1, SF_MXF8>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E2M1, 128, 1, SF_MXF4>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E2M1, 128, 1, SF_NVF4>(const GemmParams&, int, cudaStream_t);
 
 int gemm_scaled_stages(int sf, int bn, int cg) {
     if (cg == 2 && bn == 128) {

@@ -1,7 +1,6 @@
 // Instantiations of the block-scaled sm_103a GEMM kernels on SM-pair 256 x 256
-// tiles (one accumulator per CTA) and 256 x 128 tiles (two) -- tcgen05
-// cta_group::2: MXFP8 with E4M3 or E5M2 elements, MXFP4 and NVFP4 with packed
-// E2M1 elements.
+// tiles (tcgen05 cta_group::2, one accumulator per CTA): MXFP8 with E4M3 or E5M2
+// elements, MXFP4 and NVFP4 with packed E2M1 elements.
 #include "launch_impl.cuh"
 
 namespace g15 {
@@ -9,8 +8,4 @@ template cudaError_t launch_gemm<ELEM_E4M3, 256, 2, SF_MXF8>(const GemmParams&, 
 template cudaError_t launch_gemm<ELEM_E5M2, 256, 2, SF_MXF8>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_E2M1, 256, 2, SF_MXF4>(const GemmParams&, int, cudaStream_t);
 template cudaError_t launch_gemm<ELEM_E2M1, 256, 2, SF_NVF4>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E4M3, 128, 2, SF_MXF8>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E5M2, 128, 2, SF_MXF8>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E2M1, 128, 2, SF_MXF4>(const GemmParams&, int, cudaStream_t);
-template cudaError_t launch_gemm<ELEM_E2M1, 128, 2, SF_NVF4>(const GemmParams&, int, cudaStream_t);
 }  // namespace g15
