@@ -891,6 +891,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ============================ MMA issuer (one thread of the leader CTA)
         if (lane == 0 && leader) {
+            // no global access here, but the bounded waits below must not start
+            // timing while the kernel before this one is still running
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             const uint64_t adesc0 = sdesc_base(p.a_lbo, p.a_sbo);
             const uint64_t bdesc0 = sdesc_base(p.b_lbo, p.b_sbo);
             SchedState st;
