@@ -616,7 +616,7 @@ def run_gpu(args):
         hA, hB = p0.A.pin_memory(), p0.B.pin_memory()
         hC = p0.C.pin_memory() if p0.C is not None else None
         hD = torch.empty(p0.M, p0.N, dtype=I.TORCH_DTYPE[p0.d_dtype]).pin_memory()
-        e2e_steps = max(3, min(args.steps, 20))
+        e2e_steps = max(3, min(args.steps, 50))
         for _ in range(2):
             g.gemm_run_host(plan.handle, hA, hB, hC, hD, p0.M, p0.N, p0.K, p0.alpha, p0.beta,
                             p0.scale_a, p0.scale_b, stream)
