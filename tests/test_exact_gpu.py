@@ -380,6 +380,33 @@ def test_grouped_e4m3_per_group_scales_bit_exact(cg):
         assert_bit_exact(p, inputs.bits(t["D"].cpu()))
 
 
+@pytest.mark.parametrize("dtype,a_col,b_col", [("f16", False, False), ("bf16", True, False),
+                                               ("f16", False, True), ("e4m3", False, False)])
+def test_grouped_column_major_c_d_bit_exact(dtype, a_col, b_col):
+    """Grouped GEMM on a plan with column-major C and D (each group computed as
+    D_g^T = B_g^T . A_g^T): ragged groups, fp8 groups with their own scales."""
+    sizes = [(64, 256, 1024), (200, 400, 2176), (8, 16, 128), (392, 512, 640)]  # ld = M: M % 8 == 0
+    e4 = dtype == "e4m3"
+    probs = [inputs.integer_problem(M, N, K, dtype=dtype, seed=10 + i, a_col_major=a_col,
+                                    b_col_major=b_col, beta=0.0 if e4 else 0.5,
+                                    scale_a=0.5 if e4 else 1.0, scale_b=2.0 if e4 else 1.0)
+             for i, (M, N, K) in enumerate(sizes)]
+    plan = _plan(probs[0], layout_cd=g.COL_MAJOR)
+    dt = inputs.TORCH_DTYPE[probs[0].d_dtype]
+    dev = []
+    for p in probs:
+        f = lambda v: torch.tensor([v], dtype=torch.float32, device="cuda")
+        dev.append(dict(M=p.M, N=p.N, K=p.K, A=p.A.cuda(), B=p.B.cuda(),
+                        C=p.C.t().contiguous().cuda() if p.C is not None else None,
+                        D=torch.full((p.N, p.M), float("nan"), dtype=dt, device="cuda"),
+                        scale_a=f(p.scale_a) if e4 else None, scale_b=f(p.scale_b) if e4 else None))
+    plan.grouped(dev, alpha=probs[0].alpha, beta=probs[0].beta)
+    torch.cuda.synchronize()
+    assert plan.query_error() == g.OK
+    for p, t in zip(probs, dev):
+        assert_bit_exact(p, inputs.bits(t["D"].cpu().t().contiguous()))
+
+
 def test_grouped_scales_need_an_fp8_plan():
     prob = inputs.integer_problem(64, 256, 1024, dtype="f16")
     plan = _plan(prob)
