@@ -61,6 +61,20 @@ def test_activation_and_bias(act, bias, dtype):
     assert_matches_oracle(prob, _run(_plan(prob), prob))
 
 
+@pytest.mark.parametrize("act", ["sigmoid", "tanh"])
+@pytest.mark.parametrize("sched", [g.SCHED_SK, g.SCHED_SPLIT])
+@pytest.mark.parametrize("M", [24, 96])
+def test_activations_on_swap_ab_tiles(act, sched, M):
+    """Sigmoid and tanh in the transposed (swap-AB) epilogue, with C and a
+    bias that runs along the computed rows, on random operands."""
+    prob = inputs.random_problem(M, 1160, 2048, dtype="bf16", alpha=0.5, beta=0.5, act=act,
+                                 bias=True)
+    plan = _plan(prob, schedule=sched, swap_ab=2)
+    d = _run(plan, prob)
+    assert plan.last_config()["swap_ab"] == 1
+    assert_matches_oracle(prob, d)
+
+
 @pytest.mark.parametrize("sched", [g.SCHED_DP, g.SCHED_SK, g.SCHED_SPLIT])
 @pytest.mark.parametrize("col_major_cd", [False, True])
 def test_bias_under_every_schedule_and_output_layout(sched, col_major_cd):
