@@ -69,16 +69,17 @@ def test_block_scaled_matches_oracle(elem, block, scale, shape, tile_n, cta_grou
     assert_matches_oracle(prob, run_scaled(prob, tile_n=tile_n, cta_group=cta_group))
 
 
+@pytest.mark.parametrize("act", ["relu", "tanh"])
 @pytest.mark.parametrize("elem,block,scale", FORMATS)
-def test_block_scaled_epilogue_matches_oracle(elem, block, scale):
-    """alpha, beta * C, a bias and ReLU after the block-scaled product."""
+def test_block_scaled_epilogue_matches_oracle(elem, block, scale, act):
+    """alpha, beta * C, a bias and an activation after the block-scaled product."""
     M, N, K = 264, 520, 512
     prob = inputs.block_scaled_problem(M, N, K, elem=elem, block=block, scale=scale, alpha=0.5)
     prob.beta = 0.5
     prob.C = inputs.uniform((M, N), -4, 4, "bf16", 12, 1)
     prob.bias = inputs.uniform((N,), -2, 2, "bf16", 12, 2)
-    prob.act = "relu"
-    assert_matches_oracle(prob, run_scaled(prob, epilogue="relu", C=prob.C, bias=prob.bias))
+    prob.act = act
+    assert_matches_oracle(prob, run_scaled(prob, epilogue=act, C=prob.C, bias=prob.bias))
 
 
 def _exact_problem(elem, block, scale, M, N, K, seed=0):
